@@ -1,0 +1,379 @@
+"""Benchmark of the 1-bit Adam compression-stage optimizer step on GB300.
+
+A "step" is one compression-stage optimizer step over the whole synthetic parameter buffer with n
+simulated workers: worker momentum + error feedback + 1-bit compression (worker kernel), worker
+scales, server average + error feedback + recompression (server kernel), server scales, and the
+preconditioned update.  Default workload: the BERT-Large-sized flat buffer (d = 340e6 fp32
+parameters, n = 16 workers, fp16 gradients), warmed up with 20 uncompressed Adam steps before the
+variance freeze.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl gb300|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the method's workers
+are simulated inside one GPU, so there is nothing to exchange across GPUs); the timed region is
+bracketed by a barrier and a device synchronisation and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HBM_NOMINAL_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(n: int, gb: int) -> dict:
+    """Bytes per element each kernel must move in a steady-state compression step (m carried as
+    the broadcast's sign bits + one scale per shard; errors rebuilt from the stored c and a)."""
+    k1 = n * (gb + 4 + 4 + 1 / 8) + 1 / 8      # g_i, c_i read, c_i write, worker bits; server bits
+    k2 = n / 8 + 4 + 4 + 1 / 8                  # n worker bit rows; a read + write; server bits
+    k3 = 1 / 8 + 4 + 4 + 4                      # server bits; den; x read + write
+    return {"worker": k1, "server": k2, "update": k3, "step": k1 + k2 + k3}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profiles(name: str):
+    """DRAM bytes per element of a kernel from the committed ncu summary, if one exists."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(name)
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------- dist
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_max(value: float, device=None) -> float:
+    """Maximum of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------- oracle
+
+def oracle_sample(w, seconds: float = 12.0, d_sample: int = 1 << 21):
+    """Time the oracle (single-threaded C) on a bounded sample of the workload: the same worker
+    count, gradient dtype and law on a flat buffer of d_sample parameters; one warm-up step, the
+    freeze, then compression steps until `seconds` of CPU time are spent.  Returns params/s."""
+    import numpy as np
+
+    import oracle
+    from communication_compressed_optimizer_compress_gb300 import workloads as W
+
+    ws = w.with_(numel=(d_sample,))
+    src = W.GradSource(ws, "cpu")
+    x0 = W.params(ws, "cpu")[0].numpy()
+    o = oracle.OneBitAdamOracle([d_sample], ws.n_workers, x0, ws.beta1, ws.beta2, ws.eps, ws.lr,
+                                grad_dtype=ws.grad_dtype)
+    sets = [[W.to_numpy_grad(t) for t in src.grads(s)] for s in range(2)]
+    o.warmup_step(sets[0])
+    o.freeze()
+    times = []
+    t_all = time.perf_counter()
+    k = 0
+    while True:
+        t0 = time.perf_counter()
+        o.compress_step(sets[k % 2])
+        times.append(time.perf_counter() - t0)
+        k += 1
+        if time.perf_counter() - t_all > seconds and k >= 1:
+            break
+    per = statistics.median(times)
+    return {"value": d_sample / per, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"{ws.name} law, flat d={d_sample}, n={ws.n_workers}, "
+                      f"{W.DTYPE_NAME[ws.grad_dtype]} grads, {k} compression steps (median), single thread",
+            "s_per_step": per, "steps": k}
+
+
+# ---------------------------------------------------------------------------------------- main
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from communication_compressed_optimizer_compress_gb300 import workloads as W
+
+    seconds = max(3.0, min(60.0, 2.0 * (args.steps + args.warmup)))
+    base = oracle_sample(w, seconds=seconds)
+    ab = algorithmic_bytes(w.n_workers, W.GRAD_BYTES[w.grad_dtype])
+    line = {
+        "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "params/s", "n_gpus": world,
+        "steps": base["steps"], "warmup": 1, "ms_per_step": base["s_per_step"] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, args),
+        "step_gbs": base["value"] * ab["step"] / 1e9,
+        "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": base["value"], "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "compression-stage optimizer step params/s and HBM GB/s (% of 8 TB/s) at 1 GB300"
+
+
+def workload_config(w, args):
+    from communication_compressed_optimizer_compress_gb300 import workloads as W
+
+    desc = (f"{w.name}: {w.n_tensors} tensor(s), d={w.d} fp32 params, n={w.n_workers} simulated workers, "
+            f"{W.DTYPE_NAME[w.grad_dtype]} grads ({w.law}), T_w={w.warmup_steps} Adam steps then timed "
+            f"compression steps")
+    return {"workload": desc, "d": w.d, "n_tensors": w.n_tensors, "n_workers": w.n_workers,
+            "grad_dtype": W.DTYPE_NAME[w.grad_dtype], "warmup_adam_steps": w.warmup_steps,
+            "l2": "inputs larger than L2 (working set per step >> 129 MB); no flush needed",
+            "parallelism": f"replicas x{dist_env()[0]} (workers simulated in one GPU)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="bert_large")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--d", type=int, default=0, help="override the parameter count (flat workloads)")
+    ap.add_argument("--tw", type=int, default=-1, help="override the number of warm-up Adam steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    from communication_compressed_optimizer_compress_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.config]
+    if args.d:
+        w = w.with_(numel=(args.d,))
+    if args.tw >= 0:
+        w = w.with_(warmup_steps=max(1, args.tw))
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    import communication_compressed_optimizer_compress_gb300 as ob
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    ob.lib()  # fail loudly if the library is missing
+
+    # ---- inputs resident in HBM: parameters, two gradient sets alternated between steps
+    params = [p.to(dev) for p in W.params(w, dev)]
+    src = W.GradSource(w, dev)
+    gsets = [src.grads(s) for s in range(2)]
+    opt = ob.OneBitAdam(params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr,
+                        grad_dtype=W.TORCH_DTYPE[w.grad_dtype])
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(w.warmup_steps):
+        opt.warmup_step(gsets[s % 2])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = t0.elapsed_time(t1) / max(1, w.warmup_steps)
+    opt.freeze_variance()
+    for s in range(max(3, args.warmup)):
+        opt.compress_step(gsets[s % 2])
+    assert opt.get_status() == ob.OK, "non-finite state after warm-up"
+
+    # ---- timed region
+    opt.set_timing(True)
+    opt.kernel_times()  # reset
+    launches0 = opt.launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t0.record(stream)
+        for s in range(args.steps):
+            opt.compress_step(gsets[s % 2])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    launches = opt.launch_count() - launches0
+    kt = opt.kernel_times()
+    opt.set_timing(False)
+    max_ms = dist_max(elapsed_ms, dev)
+    status = opt.get_status()
+
+    ab = algorithmic_bytes(w.n_workers, W.GRAD_BYTES[w.grad_dtype])
+    ms_per_step = max_ms / args.steps
+    value = world * w.d * args.steps / (max_ms / 1e3)
+    step_gbs = w.d * ab["step"] / (ms_per_step / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    k1_ms = kt["worker"][0] / max(1, kt["worker"][1])
+    k1_gbs = w.d * ab["worker"] / (k1_ms / 1e3) / 1e9
+    per_kernel = {}
+    for name in ("worker", "worker_scale", "server", "server_scale", "update"):
+        ms, cnt = kt[name]
+        avg = ms / max(1, cnt)
+        entry = {"avg_ms": avg, "launches": cnt, "share": ms / max(1e-9, sum(v[0] for v in kt.values()))}
+        if name in ab:
+            entry["gbs"] = w.d * ab[name] / (avg / 1e3) / 1e9
+            entry["bytes_per_elem"] = ab[name]
+        per_kernel[name] = entry
+
+    # ---- end to end through the C ABI with host gradient buffers (H2D copies inside the timing)
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for g in gsets[0]:
+            hb = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+            hb.copy_(g)
+            host.append(hb)
+        h2d = sum(t.numel() * t.element_size() for t in host)
+        out = torch.empty(w.n_tensors * w.n_workers, dtype=torch.float32).pin_memory()
+        e2e_steps = max(1, min(args.steps, 5))
+        opt.compress_step_host(host)  # first call allocates the library's staging buffer
+        torch.cuda.synchronize()
+        barrier()
+        t0.record(stream)
+        for s in range(e2e_steps):
+            opt.compress_step_host(host)
+            out.copy_(opt.export_state(ob.STATE_SERVER_SCALES), non_blocking=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = dist_max(t0.elapsed_time(t1), dev)
+        e2e = {"value": world * w.d * e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 4,
+               "ms_per_step": e2e_ms / e2e_steps,
+               "path": "onebit_adam_compress_step_host (pinned host grads) + D2H of the server scales"}
+        del host
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(w)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(w, args),
+            "step_gbs": step_gbs, "step_pct_of_8tbs": 100.0 * step_gbs / HBM_NOMINAL_GBS,
+            "step_frac_of_measured_peak": step_gbs / peak,
+            "bytes_per_elem": ab["step"],
+            "roofline": {"bound": "hbm", "kernel": "k_worker (momentum + error + sign pack + norm partials)",
+                         "achieved": k1_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": k1_gbs / peak, "traffic": traffic_from_profiles("k_worker"),
+                         "bytes_per_elem": ab["worker"], "elems_per_launch": w.d},
+            "kernels": per_kernel,
+            "warmup_adam_ms_per_step": warm_ms,
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "status": ob.error_string(status),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    opt.free()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

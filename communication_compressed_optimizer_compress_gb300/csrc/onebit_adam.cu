@@ -1,0 +1,871 @@
+// onebit_adam.cu -- host side of the C ABI declared in include/onebit_adam.h.
+//
+// The handle owns: the chunk plan (the multi-tensor launcher's work table), the workspace layout,
+// the phase machine (warm-up -> freeze -> compression), the representation flags of the lazily
+// materialised state (see onebit_kernels.cuh), a small ring of device-side gradient pointer tables,
+// and optional per-kernel CUDA-event timing.  Every hot-path operation runs in the kernels.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/onebit_adam.h"
+#include "onebit_kernels.cuh"
+
+using namespace onebit;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kPtrRing = 4;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int64_t round32(int64_t v) { return (v + 31) / 32 * 32; }
+
+struct Plan {
+  int n = 0, T = 0;
+  std::vector<int64_t> numel;
+  std::vector<int64_t> seg_off;   // padded offsets
+  std::vector<int64_t> seg_uoff;  // unpadded offsets
+  int64_t Dp = 0, D = 0, Wp = 0;
+  std::vector<Chunk> chunks;
+  std::vector<Range> seg_ranges;    // [T]
+  std::vector<Range> shard_ranges;  // [T*n]
+};
+
+// Server shard j of a tensor of L elements: [j*S, min((j+1)*S, L)), S = 32*ceil(L/(32n)).
+void shard_bounds(int64_t L, int n, int j, int64_t* lo, int64_t* hi) {
+  const int64_t per = 32 * ((L + 32 * (int64_t)n - 1) / (32 * (int64_t)n));
+  *lo = std::min<int64_t>((int64_t)j * per, L);
+  *hi = std::min<int64_t>((int64_t)(j + 1) * per, L);
+}
+
+onebit_status_t check_config(const onebit_adam_config_t* cfg) {
+  if (!cfg || !cfg->numel) return ONEBIT_ERR_INVALID_ARG;
+  if (cfg->n_workers < 1 || cfg->n_workers > kMaxWorkers) return ONEBIT_ERR_INVALID_ARG;
+  if (cfg->n_tensors < 1) return ONEBIT_ERR_INVALID_ARG;
+  if (cfg->grad_dtype < ONEBIT_F32 || cfg->grad_dtype > ONEBIT_BF16) return ONEBIT_ERR_INVALID_ARG;
+  if (!(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) || !(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f))
+    return ONEBIT_ERR_INVALID_ARG;
+  if (!(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) || !std::isfinite(cfg->lr)) return ONEBIT_ERR_INVALID_ARG;
+  if (cfg->warmup_steps < 1) return ONEBIT_ERR_INVALID_ARG;
+  if (cfg->bias_correction != 0 && cfg->bias_correction != 1) return ONEBIT_ERR_INVALID_ARG;
+  int64_t total = 0;
+  for (int k = 0; k < cfg->n_tensors; ++k) {
+    if (cfg->numel[k] < 0) return ONEBIT_ERR_INVALID_ARG;
+    total += cfg->numel[k];
+  }
+  if (total < 1) return ONEBIT_ERR_INVALID_ARG;
+  return ONEBIT_OK;
+}
+
+// The multi-tensor launcher's table: chunks of at most kChunk elements that never cross a tensor
+// or a server-shard boundary.  Shard boundaries are multiples of 32 inside a tensor, so every chunk
+// starts on a sign-word boundary and only a tensor's last chunk can have a ragged end.
+onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
+  P->n = cfg->n_workers;
+  P->T = cfg->n_tensors;
+  P->numel.assign(cfg->numel, cfg->numel + cfg->n_tensors);
+  P->seg_off.resize(P->T);
+  P->seg_uoff.resize(P->T);
+  P->seg_ranges.resize(P->T);
+  P->shard_ranges.resize((size_t)P->T * P->n);
+  int64_t off = 0, uoff = 0;
+  for (int k = 0; k < P->T; ++k) {
+    const int64_t L = P->numel[k];
+    P->seg_off[k] = off;
+    P->seg_uoff[k] = uoff;
+    Range sr{(int32_t)P->chunks.size(), 0, L};
+    for (int j = 0; j < P->n; ++j) {
+      int64_t lo, hi;
+      shard_bounds(L, P->n, j, &lo, &hi);
+      Range hr{(int32_t)P->chunks.size(), 0, hi - lo};
+      for (int64_t s = lo; s < hi; s += kChunk) {
+        Chunk c{};
+        c.off = off + s;
+        c.uoff = uoff + s;
+        c.start = s;
+        c.seg = k;
+        c.shard = j;
+        c.len = (int32_t)std::min<int64_t>(kChunk, hi - s);
+        P->chunks.push_back(c);
+        if (P->chunks.size() > (size_t)INT32_MAX) return ONEBIT_ERR_UNSUPPORTED;
+      }
+      hr.count = (int32_t)P->chunks.size() - hr.first;
+      P->shard_ranges[(size_t)k * P->n + j] = hr;
+    }
+    sr.count = (int32_t)P->chunks.size() - sr.first;
+    P->seg_ranges[k] = sr;
+    off += round32(L);
+    uoff += L;
+  }
+  P->Dp = off;
+  P->D = uoff;
+  P->Wp = off / 32;
+  return ONEBIT_OK;
+}
+
+struct Layout {
+  size_t m, v, a, c, wbits, sbits, wscale, sscale, wpart, spart, chunks, seg_ranges, shard_ranges, gptr, pptr,
+      status, total;
+};
+
+Layout make_layout(const Plan& P) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + std::max<size_t>(bytes, 1), kAlign);
+    return at;
+  };
+  const size_t n = P.n, T = P.T, C = P.chunks.size();
+  L.m = take(P.Dp * 4);
+  L.v = take(P.Dp * 4);
+  L.a = take(P.Dp * 4);
+  L.c = take(n * P.Dp * 4);
+  L.wbits = take(n * P.Wp * 4);
+  L.sbits = take(P.Wp * 4);
+  L.wscale = take(2 * n * T * 4);
+  L.sscale = take(2 * n * T * 4);
+  L.wpart = take(n * C * 8);
+  L.spart = take(C * 8);
+  L.chunks = take(C * sizeof(Chunk));
+  L.seg_ranges = take(T * sizeof(Range));
+  L.shard_ranges = take(T * n * sizeof(Range));
+  L.gptr = take(kPtrRing * n * T * sizeof(void*));
+  L.pptr = take(T * sizeof(void*));
+  L.status = take(256);
+  L.total = o;
+  return L;
+}
+
+struct TimedLaunch {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+
+}  // namespace
+
+struct onebit_adam {
+  onebit_adam_config_t cfg{};
+  Plan plan;
+  Layout lay{};
+  int device = 0;
+  int num_sms = 0;
+  uint8_t* ws = nullptr;
+  bool ws_owned = false;
+  std::vector<float*> params;
+  bool params_aligned = true;
+  // phase machine
+  int64_t t = 0;
+  int32_t phase = ONEBIT_PHASE_WARMUP;
+  int64_t compress_steps = 0;  // parity of the scale buffers
+  bool m_dense = true;
+  bool werr_zero = true;
+  bool serr_zero = true;
+  // gradient pointer table ring
+  std::vector<std::vector<const void*>> ring;
+  int ring_next = 0;
+  // host-gradient staging
+  uint8_t* staging = nullptr;
+  // timing
+  bool timing = false;
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> event_pool;
+  int64_t launches = 0;
+  std::unordered_map<const void*, int> occupancy;
+  std::string last_error;
+
+  template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+onebit_status_t cuda_fail(onebit_adam* h, cudaError_t e, const char* where) {
+  if (h) h->last_error = std::string(where) + ": " + cudaGetErrorString(e);
+  return ONEBIT_ERR_CUDA;
+}
+
+#define ONEBIT_CUDA(h, call)                                  \
+  do {                                                        \
+    cudaError_t e_ = (call);                                  \
+    if (e_ != cudaSuccess) return cuda_fail((h), e_, #call);  \
+  } while (0)
+
+cudaStream_t as_stream(onebit_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int grid_for(onebit_adam* h, const void* fn, int threads, int64_t units) {
+  auto it = h->occupancy.find(fn);
+  int per_sm;
+  if (it == h->occupancy.end()) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    h->occupancy[fn] = per_sm;
+  } else {
+    per_sm = it->second;
+  }
+  const int64_t full = (int64_t)h->num_sms * per_sm;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(units, full));
+}
+
+cudaEvent_t take_event(onebit_adam* h) {
+  if (!h->event_pool.empty()) {
+    cudaEvent_t e = h->event_pool.back();
+    h->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launch one kernel on `stream`, bracketed by timing events when timing is on.
+template <typename Kern, typename Arg>
+onebit_status_t launch(onebit_adam* h, int kid, Kern kern, int grid, int threads, cudaStream_t stream,
+                       const Arg& arg) {
+  TimedLaunch tl{kid, nullptr, nullptr};
+  if (h->timing) {
+    tl.start = take_event(h);
+    tl.stop = take_event(h);
+    if (tl.start) cudaEventRecord(tl.start, stream);
+  }
+  kern<<<grid, threads, 0, stream>>>(arg);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  ++h->launches;
+  if (h->timing && tl.start && tl.stop) {
+    cudaEventRecord(tl.stop, stream);
+    h->timed.push_back(tl);
+  }
+  return ONEBIT_OK;
+}
+
+StepArgs base_args(onebit_adam* h) {
+  const Plan& P = h->plan;
+  const Layout& L = h->lay;
+  StepArgs A{};
+  A.chunks = h->at<Chunk>(L.chunks);
+  A.n_chunks = (int32_t)P.chunks.size();
+  A.n = P.n;
+  A.T = P.T;
+  A.pow2 = (P.n & (P.n - 1)) == 0;
+  A.Dp = P.Dp;
+  A.Wp = P.Wp;
+  A.pptr = h->at<float*>(L.pptr);
+  A.m = h->at<float>(L.m);
+  A.v = h->at<float>(L.v);
+  A.c = h->at<float>(L.c);
+  A.a = h->at<float>(L.a);
+  A.wbits = h->at<uint32_t>(L.wbits);
+  A.sbits = h->at<uint32_t>(L.sbits);
+  const int cur = (int)(h->compress_steps & 1), prev = cur ^ 1;
+  const size_t nt = (size_t)P.n * P.T;
+  A.wscale_prev = h->at<float>(L.wscale) + prev * nt;
+  A.wscale_cur = h->at<float>(L.wscale) + cur * nt;
+  A.sscale_prev = h->at<float>(L.sscale) + prev * nt;
+  A.sscale_cur = h->at<float>(L.sscale) + cur * nt;
+  A.wpart = h->at<double>(L.wpart);
+  A.spart = h->at<double>(L.spart);
+  A.seg_ranges = h->at<Range>(L.seg_ranges);
+  A.shard_ranges = h->at<Range>(L.shard_ranges);
+  A.status = h->at<unsigned int>(L.status);
+  const onebit_adam_config_t& c = h->cfg;
+  A.b1 = c.beta1;
+  A.omb1 = 1.0f - c.beta1;  // fp32 arithmetic, as the method's constants are fp32
+  A.b2 = c.beta2;
+  A.omb2 = 1.0f - c.beta2;
+  A.lr = c.lr;
+  A.eps = c.eps;
+  A.nf = (float)P.n;
+  A.inv_n = 1.0f / (float)P.n;
+  A.bc1 = 1.0f;
+  A.bc2 = 1.0f;
+  return A;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Upload (or reuse) the [n*T] gradient pointer table; reports whether every gradient pointer allows
+// the vector loads of the kernels.
+onebit_status_t bind_grads(onebit_adam* h, const void* const* grads, cudaStream_t stream, const void* const** dev,
+                           bool* vec) {
+  const size_t cnt = (size_t)h->plan.n * h->plan.T;
+  const size_t galign = h->cfg.grad_dtype == ONEBIT_F32 ? 32 : 16;
+  bool ok = true;
+  for (size_t q = 0; q < cnt; ++q) {
+    const int k = (int)(q % h->plan.T);
+    if (!grads[q] && h->plan.numel[k] > 0) return ONEBIT_ERR_INVALID_ARG;
+    if (!aligned(grads[q], galign)) ok = false;
+  }
+  *vec = ok;
+  const void** base = h->at<const void*>(h->lay.gptr);
+  for (int r = 0; r < kPtrRing; ++r) {
+    if (h->ring[r].size() == cnt && std::equal(h->ring[r].begin(), h->ring[r].end(), grads)) {
+      *dev = base + (size_t)r * cnt;
+      return ONEBIT_OK;
+    }
+  }
+  const int r = h->ring_next;
+  h->ring_next = (h->ring_next + 1) % kPtrRing;
+  h->ring[r].assign(grads, grads + cnt);
+  ONEBIT_CUDA(h, cudaMemcpyAsync(base + (size_t)r * cnt, h->ring[r].data(), cnt * sizeof(void*),
+                                 cudaMemcpyHostToDevice, stream));
+  *dev = base + (size_t)r * cnt;
+  return ONEBIT_OK;
+}
+
+template <typename GT>
+onebit_status_t run_warmup(onebit_adam* h, StepArgs A, bool vec, cudaStream_t st) {
+  const int C = A.n_chunks;
+  const bool bc = h->cfg.bias_correction != 0;
+  auto pick = [&](auto kern) { return launch(h, ONEBIT_K_WARMUP, kern, grid_for(h, (const void*)kern, kThreads, C), kThreads, st, A); };
+  if (bc) return vec ? pick(k_warmup<GT, true, true>) : pick(k_warmup<GT, true, false>);
+  return vec ? pick(k_warmup<GT, false, true>) : pick(k_warmup<GT, false, false>);
+}
+
+template <typename GT, bool DM, bool HE>
+onebit_status_t run_worker_v(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
+  const int64_t units = (int64_t)A.n_chunks * A.n;
+  if (vec) {
+    auto k = k_worker<GT, DM, HE, true>;
+    return launch(h, ONEBIT_K_WORKER, k, grid_for(h, (const void*)k, kThreads, units), kThreads, st, A);
+  }
+  auto k = k_worker<GT, DM, HE, false>;
+  return launch(h, ONEBIT_K_WORKER, k, grid_for(h, (const void*)k, kThreads, units), kThreads, st, A);
+}
+
+template <typename GT>
+onebit_status_t run_worker(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
+  const bool dm = h->m_dense, he = !h->werr_zero;
+  if (dm && he) return run_worker_v<GT, true, true>(h, A, vec, st);
+  if (dm) return run_worker_v<GT, true, false>(h, A, vec, st);
+  if (he) return run_worker_v<GT, false, true>(h, A, vec, st);
+  return run_worker_v<GT, false, false>(h, A, vec, st);
+}
+
+onebit_status_t do_warmup(onebit_adam* h, const void* const* grads, cudaStream_t st) {
+  if (h->phase != ONEBIT_PHASE_WARMUP) return ONEBIT_ERR_PHASE;
+  if (h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
+  StepArgs A = base_args(h);
+  bool vec = false;
+  onebit_status_t s = bind_grads(h, grads, st, &A.gptr, &vec);
+  if (s) return s;
+  const int64_t t = h->t + 1;
+  A.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, (double)t));
+  A.bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)t));
+  vec = vec && h->params_aligned;
+  switch (h->cfg.grad_dtype) {
+    case ONEBIT_F32: s = run_warmup<float>(h, A, vec, st); break;
+    case ONEBIT_F16: s = run_warmup<__half>(h, A, vec, st); break;
+    default: s = run_warmup<__nv_bfloat16>(h, A, vec, st); break;
+  }
+  if (s) return s;
+  h->t = t;
+  return ONEBIT_OK;
+}
+
+onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream_t st) {
+  if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+  StepArgs A = base_args(h);
+  bool vec = false;
+  onebit_status_t s = bind_grads(h, grads, st, &A.gptr, &vec);
+  if (s) return s;
+  switch (h->cfg.grad_dtype) {
+    case ONEBIT_F32: s = run_worker<float>(h, A, vec, st); break;
+    case ONEBIT_F16: s = run_worker<__half>(h, A, vec, st); break;
+    default: s = run_worker<__nv_bfloat16>(h, A, vec, st); break;
+  }
+  if (s) return s;
+  const int nt = h->plan.n * h->plan.T;
+  if ((s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale, nt, kScaleThreads, st, A))) return s;
+  if (h->serr_zero) {
+    auto k = k_server<false>;
+    s = launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+  } else {
+    auto k = k_server<true>;
+    s = launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+  }
+  if (s) return s;
+  if ((s = launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale, nt, kScaleThreads, st, A))) return s;
+  if (h->params_aligned) {
+    auto k = k_update<true>;
+    s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+  } else {
+    auto k = k_update<false>;
+    s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+  }
+  if (s) return s;
+  h->compress_steps += 1;
+  h->t += 1;
+  h->m_dense = false;
+  h->werr_zero = false;
+  h->serr_zero = false;
+  return ONEBIT_OK;
+}
+
+// Export kinds on the padded state, written into the caller's unpadded buffer.
+onebit_status_t run_export(onebit_adam* h, int kind, const float* src, const uint32_t* bits, const float* scales,
+                           int seg_mul, int shard_mul, float* dst, cudaStream_t st) {
+  ExportArgs X{};
+  X.chunks = h->at<Chunk>(h->lay.chunks);
+  X.n_chunks = (int32_t)h->plan.chunks.size();
+  X.kind = kind;
+  X.scale_seg_mul = seg_mul;
+  X.scale_shard_mul = shard_mul;
+  X.src = src;
+  X.bits = bits;
+  X.scales = scales;
+  X.dst = dst;
+  return launch(h, ONEBIT_K_EXPORT, k_export, grid_for(h, (const void*)k_export, kThreads, X.n_chunks), kThreads, st, X);
+}
+
+// scales written by the last compression step
+float* last_wscale(onebit_adam* h) {
+  const size_t nt = (size_t)h->plan.n * h->plan.T;
+  return h->at<float>(h->lay.wscale) + ((h->compress_steps + 1) & 1) * nt;
+}
+float* last_sscale(onebit_adam* h) {
+  const size_t nt = (size_t)h->plan.n * h->plan.T;
+  return h->at<float>(h->lay.sscale) + ((h->compress_steps + 1) & 1) * nt;
+}
+
+onebit_status_t export_m(onebit_adam* h, float* dst, cudaStream_t st) {
+  if (h->m_dense) return run_export(h, kExportCopy, h->at<float>(h->lay.m), nullptr, nullptr, 0, 0, dst, st);
+  return run_export(h, kExportBits, nullptr, h->at<uint32_t>(h->lay.sbits), last_sscale(h), h->plan.n, 1, dst, st);
+}
+
+onebit_status_t stage_copy(onebit_adam* h, const void* const* host_grads, cudaStream_t st, std::vector<const void*>* dev) {
+  const int n = h->plan.n, T = h->plan.T;
+  const size_t gb = h->cfg.grad_dtype == ONEBIT_F32 ? 4 : 2;
+  if (!host_grads) return ONEBIT_ERR_INVALID_ARG;
+  if (!h->staging) {
+    size_t bytes = 0;
+    for (int i = 0; i < n; ++i)
+      for (int k = 0; k < T; ++k) bytes += align_up(h->plan.numel[k] * gb, kAlign);
+    if (cudaMalloc(&h->staging, std::max<size_t>(bytes, 1)) != cudaSuccess) {
+      cudaGetLastError();
+      h->staging = nullptr;
+      return ONEBIT_ERR_NOMEM;
+    }
+  }
+  dev->resize((size_t)n * T);
+  size_t off = 0;
+  for (int i = 0; i < n; ++i)
+    for (int k = 0; k < T; ++k) {
+      const size_t bytes = h->plan.numel[k] * gb;
+      const size_t q = (size_t)i * T + k;
+      if (bytes && !host_grads[q]) return ONEBIT_ERR_INVALID_ARG;
+      (*dev)[q] = h->staging + off;
+      if (bytes) ONEBIT_CUDA(h, cudaMemcpyAsync(h->staging + off, host_grads[q], bytes, cudaMemcpyHostToDevice, st));
+      off += align_up(bytes, kAlign);
+    }
+  return ONEBIT_OK;
+}
+
+}  // namespace
+
+// =================================================================================== C ABI
+
+extern "C" {
+
+const char* onebit_adam_error_string(onebit_status_t s) {
+  switch (s) {
+    case ONEBIT_OK: return "ok";
+    case ONEBIT_ERR_INVALID_ARG: return "invalid argument";
+    case ONEBIT_ERR_PHASE: return "call not legal in the current phase";
+    case ONEBIT_ERR_CUDA: return "CUDA runtime error";
+    case ONEBIT_ERR_NOMEM: return "out of device memory";
+    case ONEBIT_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case ONEBIT_ERR_NONFINITE: return "non-finite scale (NaN or Inf in the gradients or state)";
+    case ONEBIT_ERR_UNSUPPORTED: return "unsupported request";
+  }
+  return "unknown status";
+}
+
+const char* onebit_adam_last_error(const onebit_adam_t* h) { return h ? h->last_error.c_str() : ""; }
+
+onebit_status_t onebit_adam_workspace_size(const onebit_adam_config_t* cfg, size_t* bytes) {
+  if (!bytes) return ONEBIT_ERR_INVALID_ARG;
+  onebit_status_t s = check_config(cfg);
+  if (s) return s;
+  Plan P;
+  if ((s = make_plan(cfg, &P))) return s;
+  *bytes = make_layout(P).total;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_plan_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap, int64_t* count) {
+  if (!count || (cap > 0 && !rows)) return ONEBIT_ERR_INVALID_ARG;
+  onebit_status_t s = check_config(cfg);
+  if (s) return s;
+  Plan P;
+  if ((s = make_plan(cfg, &P))) return s;
+  *count = (int64_t)P.chunks.size();
+  for (int64_t q = 0; q < std::min<int64_t>(cap, *count); ++q) {
+    const Chunk& c = P.chunks[q];
+    rows[q * 5 + 0] = c.seg;
+    rows[q * 5 + 1] = c.shard;
+    rows[q * 5 + 2] = c.start;
+    rows[q * 5 + 3] = c.len;
+    rows[q * 5 + 4] = c.off;
+  }
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* params, void* workspace,
+                                 size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out) {
+  if (!out || !params) return ONEBIT_ERR_INVALID_ARG;
+  *out = nullptr;
+  onebit_status_t s = check_config(cfg);
+  if (s) return s;
+  for (int k = 0; k < cfg->n_tensors; ++k)
+    if (!params[k] && cfg->numel[k] > 0) return ONEBIT_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, kAlign)) return ONEBIT_ERR_WORKSPACE;
+
+  onebit_adam* h = new (std::nothrow) onebit_adam();
+  if (!h) return ONEBIT_ERR_NOMEM;
+  h->cfg = *cfg;
+  if ((s = make_plan(cfg, &h->plan))) {
+    delete h;
+    return s;
+  }
+  h->cfg.numel = nullptr;  // the plan keeps its own copy
+  h->lay = make_layout(h->plan);
+  if (workspace && workspace_bytes < h->lay.total) {
+    delete h;
+    return ONEBIT_ERR_WORKSPACE;
+  }
+  cudaStream_t st = as_stream(stream);
+  auto fail = [&](onebit_status_t code) {
+    onebit_adam_free(h);
+    return code;
+  };
+  if (cudaGetDevice(&h->device) != cudaSuccess) return fail(cuda_fail(h, cudaGetLastError(), "cudaGetDevice"));
+  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
+    return fail(cuda_fail(h, cudaGetLastError(), "cudaDeviceGetAttribute"));
+  if (workspace) {
+    h->ws = static_cast<uint8_t*>(workspace);
+  } else {
+    if (cudaMalloc(&h->ws, h->lay.total) != cudaSuccess) {
+      cudaGetLastError();
+      h->ws = nullptr;
+      return fail(ONEBIT_ERR_NOMEM);
+    }
+    h->ws_owned = true;
+  }
+  h->params.assign(params, params + cfg->n_tensors);
+  h->params_aligned = true;
+  for (float* p : h->params)
+    if (!aligned(p, 32)) h->params_aligned = false;
+  h->ring.assign(kPtrRing, {});
+
+  // zero every piece of state, then upload the tables
+  if (cudaMemsetAsync(h->ws, 0, h->lay.total, st) != cudaSuccess)
+    return fail(cuda_fail(h, cudaGetLastError(), "cudaMemsetAsync"));
+  const Plan& P = h->plan;
+  std::vector<uint8_t> tables(h->lay.gptr - h->lay.chunks);
+  std::memcpy(tables.data(), P.chunks.data(), P.chunks.size() * sizeof(Chunk));
+  std::memcpy(tables.data() + (h->lay.seg_ranges - h->lay.chunks), P.seg_ranges.data(), P.T * sizeof(Range));
+  std::memcpy(tables.data() + (h->lay.shard_ranges - h->lay.chunks), P.shard_ranges.data(),
+              (size_t)P.T * P.n * sizeof(Range));
+  if (cudaMemcpyAsync(h->ws + h->lay.chunks, tables.data(), tables.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return fail(cuda_fail(h, cudaGetLastError(), "upload tables"));
+  if (cudaMemcpyAsync(h->ws + h->lay.pptr, h->params.data(), P.T * sizeof(float*), cudaMemcpyHostToDevice, st) !=
+      cudaSuccess)
+    return fail(cuda_fail(h, cudaGetLastError(), "upload params"));
+  // the pageable sources above are staged before the copies return; wait anyway so that the
+  // tables vector may go out of scope with no doubt
+  if (cudaStreamSynchronize(st) != cudaSuccess) return fail(cuda_fail(h, cudaGetLastError(), "init sync"));
+  *out = h;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_free(onebit_adam_t* h) {
+  if (!h) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  cudaDeviceSynchronize();
+  for (auto& tl : h->timed) {
+    cudaEventDestroy(tl.start);
+    cudaEventDestroy(tl.stop);
+  }
+  for (auto e : h->event_pool) cudaEventDestroy(e);
+  if (h->ws_owned && h->ws) cudaFree(h->ws);
+  if (h->staging) cudaFree(h->staging);
+  delete h;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_warmup_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
+  if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  return do_warmup(h, grads, as_stream(stream));
+}
+
+onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
+  if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  return do_compress(h, grads, as_stream(stream));
+}
+
+onebit_status_t onebit_adam_warmup_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream) {
+  if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
+  if (h->phase != ONEBIT_PHASE_WARMUP || h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
+  DeviceGuard g(h->device);
+  std::vector<const void*> dev;
+  onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev);
+  if (s) return s;
+  return do_warmup(h, dev.data(), as_stream(stream));
+}
+
+onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream) {
+  if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
+  if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+  DeviceGuard g(h->device);
+  std::vector<const void*> dev;
+  onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev);
+  if (s) return s;
+  return do_compress(h, dev.data(), as_stream(stream));
+}
+
+onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t stream) {
+  if (!h) return ONEBIT_ERR_INVALID_ARG;
+  if (h->phase != ONEBIT_PHASE_WARMUP || h->t < 1) return ONEBIT_ERR_PHASE;
+  DeviceGuard g(h->device);
+  cudaStream_t st = as_stream(stream);
+  const int64_t groups = h->plan.Dp / 8;
+  const float bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)h->t));
+  float* v = h->at<float>(h->lay.v);
+  onebit_status_t s;
+  auto go = [&](auto kern) -> onebit_status_t {
+    TimedLaunch tl{ONEBIT_K_FREEZE, nullptr, nullptr};
+    if (h->timing) {
+      tl.start = take_event(h);
+      tl.stop = take_event(h);
+      if (tl.start) cudaEventRecord(tl.start, st);
+    }
+    const int grid = grid_for(h, (const void*)kern, kThreads, (groups + kThreads - 1) / kThreads);
+    kern<<<grid, kThreads, 0, st>>>(v, groups, bc2, h->cfg.eps);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(h, e, "freeze launch");
+    ++h->launches;
+    if (h->timing && tl.start && tl.stop) {
+      cudaEventRecord(tl.stop, st);
+      h->timed.push_back(tl);
+    }
+    return ONEBIT_OK;
+  };
+  s = h->cfg.bias_correction ? go(k_freeze<true>) : go(k_freeze<false>);
+  if (s) return s;
+  h->phase = ONEBIT_PHASE_COMPRESS;
+  h->m_dense = true;
+  h->werr_zero = true;
+  h->serr_zero = true;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_get_status(onebit_adam_t* h, onebit_stream_t stream) {
+  if (!h) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  unsigned int flag = 0;
+  cudaStream_t st = as_stream(stream);
+  ONEBIT_CUDA(h, cudaMemcpyAsync(&flag, h->ws + h->lay.status, sizeof flag, cudaMemcpyDeviceToHost, st));
+  ONEBIT_CUDA(h, cudaStreamSynchronize(st));
+  return flag ? ONEBIT_ERR_NONFINITE : ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_clear_status(onebit_adam_t* h, onebit_stream_t stream) {
+  if (!h) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  ONEBIT_CUDA(h, cudaMemsetAsync(h->ws + h->lay.status, 0, sizeof(unsigned int), as_stream(stream)));
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_get_step(const onebit_adam_t* h, int64_t* t, int32_t* phase) {
+  if (!h || !t || !phase) return ONEBIT_ERR_INVALID_ARG;
+  *t = h->t;
+  *phase = h->phase;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_set_step(onebit_adam_t* h, int64_t t, int32_t phase, onebit_stream_t stream) {
+  if (!h || t < 0) return ONEBIT_ERR_INVALID_ARG;
+  if (phase == ONEBIT_PHASE_WARMUP) {
+    if (t >= h->cfg.warmup_steps) return ONEBIT_ERR_INVALID_ARG;
+  } else if (phase == ONEBIT_PHASE_COMPRESS) {
+    if (t < 1) return ONEBIT_ERR_INVALID_ARG;
+    h->m_dense = true;
+    h->werr_zero = true;
+    h->serr_zero = true;
+  } else {
+    return ONEBIT_ERR_INVALID_ARG;
+  }
+  (void)stream;
+  h->t = t;
+  h->phase = phase;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_state_size(const onebit_adam_t* h, int32_t what, size_t* bytes) {
+  if (!h || !bytes) return ONEBIT_ERR_INVALID_ARG;
+  const Plan& P = h->plan;
+  switch (what) {
+    case ONEBIT_STATE_M:
+    case ONEBIT_STATE_V:
+    case ONEBIT_STATE_WORKER_ERROR:
+    case ONEBIT_STATE_SERVER_ERROR: *bytes = (size_t)P.D * 4; return ONEBIT_OK;
+    case ONEBIT_STATE_WORKER_BITS:
+    case ONEBIT_STATE_SERVER_BITS: *bytes = (size_t)P.Wp * 4; return ONEBIT_OK;
+    case ONEBIT_STATE_WORKER_SCALES:
+    case ONEBIT_STATE_SERVER_SCALES: *bytes = (size_t)P.n * P.T * 4; return ONEBIT_OK;
+    default: return ONEBIT_ERR_INVALID_ARG;
+  }
+}
+
+onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worker, void* dst, onebit_stream_t stream) {
+  if (!h || !dst) return ONEBIT_ERR_INVALID_ARG;
+  const Plan& P = h->plan;
+  const bool per_worker = what == ONEBIT_STATE_WORKER_ERROR || what == ONEBIT_STATE_WORKER_BITS;
+  if (per_worker && (worker < 0 || worker >= P.n)) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  cudaStream_t st = as_stream(stream);
+  float* out = static_cast<float*>(dst);
+  switch (what) {
+    case ONEBIT_STATE_M: return export_m(h, out, st);
+    case ONEBIT_STATE_V: return run_export(h, kExportCopy, h->at<float>(h->lay.v), nullptr, nullptr, 0, 0, out, st);
+    case ONEBIT_STATE_WORKER_ERROR:
+      if (h->phase != ONEBIT_PHASE_COMPRESS || h->werr_zero)
+        return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
+      return run_export(h, kExportSignedErr, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, nullptr,
+                        last_wscale(h) + (size_t)worker * P.T, 1, 0, out, st);
+    case ONEBIT_STATE_SERVER_ERROR:
+      if (h->phase != ONEBIT_PHASE_COMPRESS || h->serr_zero)
+        return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
+      return run_export(h, kExportSignedErr, h->at<float>(h->lay.a), nullptr, last_sscale(h), P.n, 1, out, st);
+    case ONEBIT_STATE_WORKER_BITS:
+      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.wbits) + (size_t)worker * P.Wp, P.Wp * 4,
+                                     cudaMemcpyDeviceToDevice, st));
+      return ONEBIT_OK;
+    case ONEBIT_STATE_SERVER_BITS:
+      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.sbits), P.Wp * 4, cudaMemcpyDeviceToDevice, st));
+      return ONEBIT_OK;
+    case ONEBIT_STATE_WORKER_SCALES:
+      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, last_wscale(h), (size_t)P.n * P.T * 4, cudaMemcpyDeviceToDevice, st));
+      return ONEBIT_OK;
+    case ONEBIT_STATE_SERVER_SCALES:
+      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, last_sscale(h), (size_t)P.n * P.T * 4, cudaMemcpyDeviceToDevice, st));
+      return ONEBIT_OK;
+    default: return ONEBIT_ERR_INVALID_ARG;
+  }
+}
+
+onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worker, const void* src, onebit_stream_t stream) {
+  if (!h || !src) return ONEBIT_ERR_INVALID_ARG;
+  const Plan& P = h->plan;
+  DeviceGuard g(h->device);
+  cudaStream_t st = as_stream(stream);
+  const float* in = static_cast<const float*>(src);
+  const size_t nt = (size_t)P.n * P.T;
+  onebit_status_t s;
+  switch (what) {
+    case ONEBIT_STATE_M:
+      if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.m), st))) return s;
+      h->m_dense = true;
+      return ONEBIT_OK;
+    case ONEBIT_STATE_V:
+      return run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.v), st);
+    case ONEBIT_STATE_WORKER_ERROR: {
+      if (worker < 0 || worker >= P.n) return ONEBIT_ERR_INVALID_ARG;
+      if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+      float* ws_prev = last_wscale(h);  // what the next step reads as the previous scales
+      if (h->werr_zero) {
+        ONEBIT_CUDA(h, cudaMemsetAsync(h->at<float>(h->lay.c), 0, (size_t)P.n * P.Dp * 4, st));
+        ONEBIT_CUDA(h, cudaMemsetAsync(ws_prev, 0, nt * 4, st));
+        h->werr_zero = false;
+      }
+      // store delta as c with a zero scale: the next step rebuilds c - 0*sign(c) = delta exactly
+      if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, st)))
+        return s;
+      ONEBIT_CUDA(h, cudaMemsetAsync(ws_prev + (size_t)worker * P.T, 0, (size_t)P.T * 4, st));
+      return ONEBIT_OK;
+    }
+    case ONEBIT_STATE_SERVER_ERROR: {
+      if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+      if (!h->m_dense) {  // m is carried by the server scales about to be zeroed: materialise it
+        if ((s = export_m(h, h->at<float>(h->lay.m), st))) return s;
+        h->m_dense = true;
+      }
+      // store eps as a with a zero scale: the next step rebuilds a - 0*sign(a) = eps exactly
+      if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.a), st))) return s;
+      ONEBIT_CUDA(h, cudaMemsetAsync(last_sscale(h), 0, nt * 4, st));
+      h->serr_zero = false;
+      return ONEBIT_OK;
+    }
+    default: return ONEBIT_ERR_INVALID_ARG;
+  }
+}
+
+onebit_status_t onebit_adam_comm_bytes(const onebit_adam_t* h, uint64_t* compressed, uint64_t* fp32_bytes) {
+  if (!h || !compressed || !fp32_bytes) return ONEBIT_ERR_INVALID_ARG;
+  uint64_t c = 0, f = 0;
+  for (int64_t L : h->plan.numel) {
+    c += (uint64_t)((L + 31) / 32) * 4 + 4;
+    f += (uint64_t)L * 4;
+  }
+  *compressed = c;
+  *fp32_bytes = f;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_set_timing(onebit_adam_t* h, int32_t enable) {
+  if (!h) return ONEBIT_ERR_INVALID_ARG;
+  h->timing = enable != 0;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_kernel_times(onebit_adam_t* h, double* ms, int64_t* launches) {
+  if (!h || !ms || !launches) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  for (int k = 0; k < ONEBIT_NUM_KERNELS; ++k) {
+    ms[k] = 0.0;
+    launches[k] = 0;
+  }
+  onebit_status_t rc = ONEBIT_OK;
+  for (auto& tl : h->timed) {
+    float t = 0.0f;
+    if (cudaEventSynchronize(tl.stop) != cudaSuccess || cudaEventElapsedTime(&t, tl.start, tl.stop) != cudaSuccess)
+      rc = cuda_fail(h, cudaGetLastError(), "kernel timing");
+    ms[tl.kernel] += t;
+    launches[tl.kernel] += 1;
+    h->event_pool.push_back(tl.start);
+    h->event_pool.push_back(tl.stop);
+  }
+  h->timed.clear();
+  return rc;
+}
+
+onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launches) {
+  if (!h || !launches) return ONEBIT_ERR_INVALID_ARG;
+  *launches = h->launches;
+  return ONEBIT_OK;
+}
+
+}  // extern "C"

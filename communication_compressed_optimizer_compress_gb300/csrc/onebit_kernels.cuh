@@ -1,0 +1,559 @@
+// onebit_kernels.cuh -- sm_103a kernels of the 1-bit Adam optimizer step.
+//
+// Method: "1-bit Adam: Communication Efficient Large-Scale Training with Adam's Convergence Speed"
+// (Tang et al.), Sec. 4.3 (1-bit sign + magnitude-preserving scale), Sec. 6 and Sec. 11 (workers
+// compress their momentum with error compensation, the server averages the messages and compresses
+// again, the result is broadcast), and the AIMech page "1-bit Adam (Two-Stage Preconditioner-Frozen
+// Error-Compensated Adam)" (v_t, m_t, V = diag(sqrt(v_Tw) + eps), x_t = x_{t-1} - gamma V^-1 m_hat).
+//
+// Data layout in HBM (one GPU simulates the n workers):
+//   every per-element state array uses a padded layout in which tensor k starts at element
+//   off_k = sum_{k'<k} roundup(L_k', 32); Dp = padded total, Wp = Dp / 32 sign words.
+//   m[Dp]        fp32 momentum (dense form: warm-up and the first compression step)
+//   v[Dp]        fp32 variance; after the freeze den = sqrt(v) + eps
+//   c[n][Dp]     fp32 compensated momentum c_i of the last step.  The worker error of that step is
+//                delta_i = c_i - s_i*sign(c_i), recomputed from c_i and the last scale s_i with the
+//                same single fp32 operation wherever it is needed, so it is never stored.
+//   a[Dp]        fp32 server input of the last step; server error eps = a - S*sign(a), likewise.
+//   wbits[n][Wp] worker sign words; sbits[Wp] server sign words (= the broadcast momentum's signs:
+//                after a compression step m = S*sign(a) is represented by sbits and S, 1/8 B/elem).
+//   scales       double-buffered by step parity: a step reads the previous step's scales (to rebuild
+//                the errors and m) and writes its own.
+//
+// Work decomposition: a host-built table of chunks (<= kChunk elements, never crossing a tensor or a
+// server-shard boundary, starting on a 32-element boundary).  Each lane owns 8 consecutive elements
+// (one byte of sign bits, one 256-bit load of fp32 state), so sign packing needs no cross-lane
+// exchange and every warp access is a contiguous 1 KB (fp32) or 512 B (16-bit) span.
+//
+// Arithmetic: fp32 with explicit round-to-nearest intrinsics (no contraction into FMA), in the
+// operation order of the method's formulas, so that the sign decisions match a plain CPU evaluation
+// bit for bit.  Sum-of-squares partials use short fp32 FMA runs (16 elements) promoted to fp64; the
+// per-chunk partials are reduced in a fixed order (deterministic, independent of the grid size).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace onebit {
+
+constexpr int kThreads = 256;          // threads per CTA of the streaming kernels
+constexpr int kChunk = 65536;          // maximum elements per work chunk (multiple of 256)
+constexpr int kMaxWorkers = 256;
+constexpr int kScaleThreads = 256;     // threads per CTA of the scale kernels
+
+struct Chunk {
+  int64_t off;    // element offset in the padded state layout (multiple of 32)
+  int64_t uoff;   // element offset in the unpadded concatenation of the tensors
+  int64_t start;  // element offset inside tensor `seg` (multiple of 32)
+  int32_t seg;    // tensor k
+  int32_t shard;  // server shard j of tensor k
+  int32_t len;    // elements, 1..kChunk
+  int32_t pad_;
+};
+
+struct Range {    // a contiguous run of chunks with its element count
+  int32_t first;
+  int32_t count;
+  int64_t len;
+};
+
+struct StepArgs {
+  const Chunk* chunks;
+  int32_t n_chunks;
+  int32_t n;      // workers
+  int32_t T;      // tensors
+  int32_t pow2;   // n is a power of two: x / n == x * (1/n) exactly
+  int64_t Dp;     // padded elements per row
+  int64_t Wp;     // sign words per row
+  const void* const* gptr;  // [n*T] gradient pointers, [worker][tensor]
+  float* const* pptr;       // [T] parameter pointers
+  float* m;
+  float* v;
+  float* c;
+  float* a;
+  uint32_t* wbits;
+  uint32_t* sbits;
+  const float* wscale_prev;  // [n*T]
+  float* wscale_cur;         // [n*T]
+  const float* sscale_prev;  // [T*n]
+  float* sscale_cur;         // [T*n]
+  double* wpart;             // [n*n_chunks]
+  double* spart;             // [n_chunks]
+  const Range* seg_ranges;   // [T]   chunks of each tensor
+  const Range* shard_ranges; // [T*n] chunks of each server shard
+  unsigned int* status;
+  float b1, omb1, b2, omb2, lr, eps, inv_n, nf, bc1, bc2;
+};
+
+// ------------------------------------------------------------------------------------------------
+// memory helpers (inline PTX): 256-bit accesses for fp32 state, 128-bit for 16-bit gradients.
+
+__device__ __forceinline__ void ld8_stream(const float* p, float (&r)[8]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7])
+               : "l"(p));
+}
+// coherent load for state the same kernel later overwrites in place
+__device__ __forceinline__ void ld8_state(const float* p, float (&r)[8]) {
+  asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st8(float* p, const float (&r)[8]) {
+  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(r[0]), "f"(r[1]), "f"(r[2]),
+               "f"(r[3]), "f"(r[4]), "f"(r[5]), "f"(r[6]), "f"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld16_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+template <typename GT> struct Grad;
+template <> struct Grad<float> {
+  static __device__ __forceinline__ void load8(const float* p, float (&g)[8]) { ld8_stream(p, g); }
+  static __device__ __forceinline__ float load1(const float* p) { return __ldg(p); }
+};
+template <> struct Grad<__half> {
+  static __device__ __forceinline__ void load8(const __half* p, float (&g)[8]) {
+    const uint4 u = ld16_stream(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+      g[2 * k] = f.x;
+      g[2 * k + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ float load1(const __half* p) { return __half2float(__ldg(p)); }
+};
+template <> struct Grad<__nv_bfloat16> {
+  static __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&g)[8]) {
+    const uint4 u = ld16_stream(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      g[2 * k] = __uint_as_float(w[k] << 16);
+      g[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  }
+  static __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(__ldg(p)); }
+};
+
+// ------------------------------------------------------------------------------------------------
+// fixed-order CTA reduction of one double per thread
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int NT>
+__device__ __forceinline__ double block_sum(double v, double* red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  double r = 0.0;
+  if (warp == 0) {
+    r = lane < NT / 32 ? red[lane] : 0.0;
+    r = warp_sum(r);
+  }
+  __syncthreads();
+  return r;  // valid in thread 0
+}
+
+// the fp32 operations of the method, in the oracle's order
+__device__ __forceinline__ float momentum(float b1, float omb1, float m, float g) {
+  return __fadd_rn(__fmul_rn(b1, m), __fmul_rn(omb1, g));
+}
+__device__ __forceinline__ float error_of(float c, float s) {  // c - s*sign(c), sign(0) = +1
+  return c >= 0.0f ? __fsub_rn(c, s) : __fadd_rn(c, s);
+}
+
+// ------------------------------------------------------------------------------------------------
+// K1: worker momentum + error feedback + 1-bit compression + norm partials.
+// One unit = (chunk, worker).  c_i = (b1*m + (1-b1)*g_i) + delta_i, delta_i rebuilt from the
+// previous c_i and s_i; writes c_i, its sign byte and the chunk's sum of c_i^2.
+
+template <typename GT, bool DENSE_M, bool HAS_ERR, bool VEC>
+__global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
+  __shared__ double red[kThreads / 32];
+  const int64_t n_units = (int64_t)A.n_chunks * A.n;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const int ci = (int)(u / A.n);
+    const int i = (int)(u - (int64_t)ci * A.n);
+    const Chunk ch = A.chunks[ci];
+    const GT* __restrict__ g = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start;
+    float* __restrict__ c = A.c + (int64_t)i * A.Dp + ch.off;
+    uint8_t* __restrict__ wb = reinterpret_cast<uint8_t*>(A.wbits + (int64_t)i * A.Wp) + (ch.off >> 3);
+    const uint8_t* __restrict__ sb = reinterpret_cast<const uint8_t*>(A.sbits) + (ch.off >> 3);
+    const float* __restrict__ md = A.m + ch.off;
+    const float sp = HAS_ERR ? A.wscale_prev[(int64_t)i * A.T + ch.seg] : 0.0f;
+    const float Sp = DENSE_M ? 0.0f : A.sscale_prev[(int64_t)ch.seg * A.n + ch.shard];
+    const float b1 = A.b1, omb1 = A.omb1;
+
+    // one group of 8 elements: loads first (so that two groups are in flight), then math + stores
+    struct In {
+      float g[8], cp[8], m[8];
+      uint32_t mb;
+    };
+    auto load = [&](In& r, int gi) {
+      const int64_t e = (int64_t)gi * 8;
+      if (VEC) {
+        Grad<GT>::load8(g + e, r.g);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) r.g[q] = Grad<GT>::load1(g + e + q);
+      }
+      if (HAS_ERR) ld8_state(c + e, r.cp);
+      if (DENSE_M) ld8_stream(md + e, r.m);
+      else r.mb = sb[gi];
+    };
+    auto work = [&](const In& r, int gi) -> float {
+      float out[8];
+      uint32_t byte = 0;
+      float sq = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float mq = DENSE_M ? r.m[q] : (((r.mb >> q) & 1u) ? Sp : -Sp);
+        const float mi = momentum(b1, omb1, mq, r.g[q]);
+        const float d = HAS_ERR ? error_of(r.cp[q], sp) : 0.0f;
+        const float cq = __fadd_rn(mi, d);
+        out[q] = cq;
+        byte |= (cq >= 0.0f ? 1u : 0u) << q;
+        sq = __fmaf_rn(cq, cq, sq);
+      }
+      st8(c + (int64_t)gi * 8, out);
+      wb[gi] = (uint8_t)byte;
+      return sq;
+    };
+
+    double acc = 0.0;
+    const int ng = ch.len >> 3;
+    int gi = threadIdx.x;
+    for (; gi + kThreads < ng; gi += 2 * kThreads) {
+      In r0, r1;
+      load(r0, gi);
+      load(r1, gi + kThreads);
+      const float s0 = work(r0, gi);
+      const float s1 = work(r1, gi + kThreads);
+      acc += (double)(s0 + s1);
+    }
+    if (gi < ng) {
+      In r0;
+      load(r0, gi);
+      acc += (double)work(r0, gi);
+    }
+    const int rem = ch.len & 7;
+    if (rem && threadIdx.x == (ng % kThreads)) {  // the ragged end of a tensor: scalar
+      const int64_t e0 = (int64_t)ng * 8;
+      uint32_t byte = 0;
+      float sq = 0.0f;
+      for (int q = 0; q < rem; ++q) {
+        const int64_t e = e0 + q;
+        const float mq = DENSE_M ? md[e] : (((sb[ng] >> q) & 1u) ? Sp : -Sp);
+        const float mi = momentum(b1, omb1, mq, Grad<GT>::load1(g + e));
+        const float d = HAS_ERR ? error_of(c[e], sp) : 0.0f;
+        const float cq = __fadd_rn(mi, d);
+        c[e] = cq;
+        byte |= (cq >= 0.0f ? 1u : 0u) << q;
+        sq = __fmaf_rn(cq, cq, sq);
+      }
+      wb[ng] = (uint8_t)byte;
+      acc += (double)sq;
+    }
+    const double tot = block_sum<kThreads>(acc, red);
+    if (threadIdx.x == 0) A.wpart[(int64_t)i * A.n_chunks + ci] = tot;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Scale kernels: one CTA per (worker, tensor) or (tensor, shard); fixed-order sum of the chunk
+// partials, then scale = sqrt(sum / len) in double, rounded once to fp32.
+
+__device__ __forceinline__ float finish_scale(const double* part, int64_t stride_unused, const Range r,
+                                              unsigned int* status, double* red) {
+  double acc = 0.0;
+  for (int c = threadIdx.x; c < r.count; c += kScaleThreads) acc += __ldcg(part + r.first + c);
+  const double tot = block_sum<kScaleThreads>(acc, red);
+  float s = 0.0f;
+  if (threadIdx.x == 0) {
+    s = r.len > 0 ? __double2float_rn(sqrt(tot / (double)r.len)) : 0.0f;
+    if (!isfinite(s)) atomicOr(status, 1u);
+  }
+  (void)stride_unused;
+  return s;
+}
+
+__global__ void __launch_bounds__(kScaleThreads) k_worker_scale(const StepArgs A) {
+  __shared__ double red[kScaleThreads / 32];
+  const int i = blockIdx.x / A.T, k = blockIdx.x % A.T;
+  const float s = finish_scale(A.wpart + (int64_t)i * A.n_chunks, 0, A.seg_ranges[k], A.status, red);
+  if (threadIdx.x == 0) A.wscale_cur[blockIdx.x] = s;
+}
+
+__global__ void __launch_bounds__(kScaleThreads) k_server_scale(const StepArgs A) {
+  __shared__ double red[kScaleThreads / 32];
+  const float s = finish_scale(A.spart, 0, A.shard_ranges[blockIdx.x], A.status, red);
+  if (threadIdx.x == 0) A.sscale_cur[blockIdx.x] = s;
+}
+
+// ------------------------------------------------------------------------------------------------
+// K2: server.  One unit = one chunk of one shard.  For every element the n decompressed worker
+// messages are summed in worker order in fp32, divided by n, the server error is added; the result
+// a is written with its sign byte and the chunk's sum of a^2.
+
+template <bool HAS_ERR>
+__global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
+  __shared__ float ssc[kMaxWorkers];
+  __shared__ double red[kThreads / 32];
+  const int n = A.n;
+  const int64_t wrow = A.Wp * 4;  // bytes per worker row of sign words
+  for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
+    const Chunk ch = A.chunks[u];
+    for (int i = threadIdx.x; i < n; i += kThreads) ssc[i] = A.wscale_cur[(int64_t)i * A.T + ch.seg];
+    __syncthreads();
+    const float Sp = HAS_ERR ? A.sscale_prev[(int64_t)ch.seg * n + ch.shard] : 0.0f;
+    float* __restrict__ a = A.a + ch.off;
+    const uint8_t* __restrict__ wb = reinterpret_cast<const uint8_t*>(A.wbits) + (ch.off >> 3);
+    uint8_t* __restrict__ sb = reinterpret_cast<uint8_t*>(A.sbits) + (ch.off >> 3);
+    double acc = 0.0;
+    const int ng = (ch.len + 7) >> 3;
+    for (int gi = threadIdx.x; gi < ng; gi += kThreads) {
+      const int cnt = min(8, ch.len - gi * 8);
+      const int64_t e = (int64_t)gi * 8;
+      float ap[8];
+      if (HAS_ERR) {
+        if (cnt == 8) ld8_state(a + e, ap);
+        else
+          for (int q = 0; q < 8; ++q) ap[q] = q < cnt ? a[e + q] : 0.0f;
+      }
+      float s[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) s[q] = 0.0f;
+      for (int i = 0; i < n; ++i) {
+        const uint32_t byte = __ldg(wb + (int64_t)i * wrow + gi);
+        const float si = ssc[i];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s[q] = __fadd_rn(s[q], ((byte >> q) & 1u) ? si : -si);
+      }
+      float out[8];
+      uint32_t byte = 0;
+      float sq = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float avg = A.pow2 ? __fmul_rn(s[q], A.inv_n) : __fdiv_rn(s[q], A.nf);
+        const float ep = HAS_ERR ? error_of(ap[q], Sp) : 0.0f;
+        const float aq = __fadd_rn(avg, ep);
+        out[q] = aq;
+        if (q < cnt) {
+          byte |= (aq >= 0.0f ? 1u : 0u) << q;
+          sq = __fmaf_rn(aq, aq, sq);
+        }
+      }
+      if (cnt == 8) st8(a + e, out);
+      else
+        for (int q = 0; q < cnt; ++q) a[e + q] = out[q];
+      sb[gi] = (uint8_t)byte;
+      acc += (double)sq;
+    }
+    const double tot = block_sum<kThreads>(acc, red);  // also orders the ssc reuse
+    if (threadIdx.x == 0) A.spart[u] = tot;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// K3: broadcast unpack + preconditioned update  x = x - lr * (m / den),  m = S_kj * sign(a).
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) k_update(const StepArgs A) {
+  const float lr = A.lr;
+  for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
+    const Chunk ch = A.chunks[u];
+    const float S = A.sscale_cur[(int64_t)ch.seg * A.n + ch.shard];
+    float* __restrict__ x = A.pptr[ch.seg] + ch.start;
+    const float* __restrict__ den = A.v + ch.off;
+    const uint8_t* __restrict__ sb = reinterpret_cast<const uint8_t*>(A.sbits) + (ch.off >> 3);
+    struct In {
+      float x[8], d[8];
+      uint32_t b;
+    };
+    auto load = [&](In& r, int gi) {
+      const int64_t e = (int64_t)gi * 8;
+      if (VEC) ld8_state(x + e, r.x);
+      else
+#pragma unroll
+        for (int q = 0; q < 8; ++q) r.x[q] = x[e + q];
+      ld8_stream(den + e, r.d);
+      r.b = sb[gi];
+    };
+    auto work = [&](In& r, int gi) {
+      const int64_t e = (int64_t)gi * 8;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float mq = ((r.b >> q) & 1u) ? S : -S;
+        r.x[q] = __fsub_rn(r.x[q], __fmul_rn(lr, __fdiv_rn(mq, r.d[q])));
+      }
+      if (VEC) st8(x + e, r.x);
+      else
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[e + q] = r.x[q];
+    };
+    const int ng = ch.len >> 3;
+    int gi = threadIdx.x;
+    for (; gi + kThreads < ng; gi += 2 * kThreads) {
+      In r0, r1;
+      load(r0, gi);
+      load(r1, gi + kThreads);
+      work(r0, gi);
+      work(r1, gi + kThreads);
+    }
+    if (gi < ng) {
+      In r0;
+      load(r0, gi);
+      work(r0, gi);
+    }
+    const int rem = ch.len & 7;
+    if (rem && threadIdx.x == (ng % kThreads)) {
+      const int64_t e0 = (int64_t)ng * 8;
+      for (int q = 0; q < rem; ++q) {
+        const float mq = ((sb[ng] >> q) & 1u) ? S : -S;
+        x[e0 + q] = __fsub_rn(x[e0 + q], __fmul_rn(lr, __fdiv_rn(mq, den[e0 + q])));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// K0: warm-up.  Mean of the n worker gradients (summed in worker order), then one Adam step.
+
+template <typename GT, bool BC, bool VEC>
+__global__ void __launch_bounds__(kThreads) k_warmup(const StepArgs A) {
+  for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
+    const Chunk ch = A.chunks[u];
+    float* __restrict__ x = A.pptr[ch.seg] + ch.start;
+    float* __restrict__ m = A.m + ch.off;
+    float* __restrict__ v = A.v + ch.off;
+    const int ng = (ch.len + 7) >> 3;
+    for (int gi = threadIdx.x; gi < ng; gi += kThreads) {
+      const int cnt = min(8, ch.len - gi * 8);
+      const int64_t e = (int64_t)gi * 8;
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+      for (int i = 0; i < A.n; ++i) {
+        const GT* gp = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start + e;
+        float gv[8];
+        if (VEC && cnt == 8) {
+          Grad<GT>::load8(gp, gv);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) gv[q] = q < cnt ? Grad<GT>::load1(gp + q) : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], gv[q]);
+      }
+      float mv[8], vv[8], xv[8];
+      if (cnt == 8) {
+        ld8_state(m + e, mv);
+        ld8_state(v + e, vv);
+      } else {
+        for (int q = 0; q < 8; ++q) {
+          mv[q] = q < cnt ? m[e + q] : 0.0f;
+          vv[q] = q < cnt ? v[e + q] : 0.0f;
+        }
+      }
+      if (VEC && cnt == 8) ld8_state(x + e, xv);
+      else
+        for (int q = 0; q < 8; ++q) xv[q] = q < cnt ? x[e + q] : 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float gbar = A.pow2 ? __fmul_rn(acc[q], A.inv_n) : __fdiv_rn(acc[q], A.nf);
+        mv[q] = momentum(A.b1, A.omb1, mv[q], gbar);
+        vv[q] = __fadd_rn(__fmul_rn(A.b2, vv[q]), __fmul_rn(A.omb2, __fmul_rn(gbar, gbar)));
+        const float mh = BC ? __fdiv_rn(mv[q], A.bc1) : mv[q];
+        const float vh = BC ? __fdiv_rn(vv[q], A.bc2) : vv[q];
+        xv[q] = __fsub_rn(xv[q], __fmul_rn(A.lr, __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), A.eps))));
+      }
+      if (cnt == 8) {
+        st8(m + e, mv);
+        st8(v + e, vv);
+      } else {
+        for (int q = 0; q < cnt; ++q) {
+          m[e + q] = mv[q];
+          v[e + q] = vv[q];
+        }
+      }
+      if (VEC && cnt == 8) st8(x + e, xv);
+      else
+        for (int q = 0; q < cnt; ++q) x[e + q] = xv[q];
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// KF: freeze  den = sqrt(v) + eps  (v / bc2 first with bias correction), in place over Dp.
+
+template <bool BC>
+__global__ void __launch_bounds__(kThreads) k_freeze(float* v, int64_t n_groups, float bc2, float eps) {
+  for (int64_t gi = blockIdx.x * (int64_t)kThreads + threadIdx.x; gi < n_groups;
+       gi += (int64_t)gridDim.x * kThreads) {
+    float r[8];
+    ld8_state(v + gi * 8, r);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) r[q] = __fadd_rn(__fsqrt_rn(BC ? __fdiv_rn(r[q], bc2) : r[q]), eps);
+    st8(v + gi * 8, r);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Export / import between the padded state layout and the caller's unpadded fp32 layout.
+
+enum ExportKind : int {
+  kExportCopy = 0,      // dst = src                        (m dense, v/den)
+  kExportSignedErr = 1, // dst = err(src, scale[seg...])    (worker / server error)
+  kExportBits = 2,      // dst = bit ? S : -S               (m from the broadcast)
+  kExportZero = 3,      // dst = 0
+  kImportCopy = 4       // padded dst = unpadded src
+};
+
+struct ExportArgs {
+  const Chunk* chunks;
+  int32_t n_chunks;
+  int32_t kind;
+  int32_t scale_stride;  // index of the scale: seg*scale_seg_mul + shard*scale_shard_mul
+  int32_t scale_seg_mul;
+  int32_t scale_shard_mul;
+  int32_t pad_;
+  const float* src;      // padded source (or unpadded source for import)
+  const uint32_t* bits;  // sign words for kExportBits
+  const float* scales;
+  float* dst;
+};
+
+__global__ void __launch_bounds__(kThreads) k_export(const ExportArgs X) {
+  for (int u = blockIdx.x; u < X.n_chunks; u += gridDim.x) {
+    const Chunk ch = X.chunks[u];
+    const float s = X.scales ? X.scales[(int64_t)ch.seg * X.scale_seg_mul + (int64_t)ch.shard * X.scale_shard_mul]
+                             : 0.0f;
+    for (int e = threadIdx.x; e < ch.len; e += kThreads) {
+      const int64_t p = ch.off + e, q = ch.uoff + e;
+      switch (X.kind) {
+        case kExportCopy: X.dst[q] = X.src[p]; break;
+        case kExportSignedErr: X.dst[q] = error_of(X.src[p], s); break;
+        case kExportBits: X.dst[q] = ((X.bits[p >> 5] >> (p & 31)) & 1u) ? s : -s; break;
+        case kExportZero: X.dst[q] = 0.0f; break;
+        case kImportCopy: X.dst[p] = X.src[q]; break;
+        default: break;
+      }
+    }
+  }
+}
+
+}  // namespace onebit

@@ -1,0 +1,192 @@
+/*
+ * onebit_adam.h -- C ABI of the GB300 (sm_103a) 1-bit Adam optimizer step.
+ *
+ * The method ("1-bit Adam: Communication Efficient Large-Scale Training with Adam's Convergence
+ * Speed", Tang et al. 2021) has two stages:
+ *   - warm-up: uncompressed Adam on the workers' averaged gradient (Sec. 4.3; AIMech page
+ *     "1-bit Adam (Two-Stage Preconditioner-Frozen Error-Compensated Adam)", summary formulas
+ *     m_t = b1 m_{t-1} + (1-b1) g_t, v_t = b2 v_{t-1} + (1-b2) g_t^2);
+ *   - compression: the variance is frozen as V = diag(sqrt(v_Tw) + eps) (Sec. 3.3 and 5: momentum
+ *     SGD with a coordinate-wise learning rate) and momentum is exchanged with error-compensated
+ *     1-bit compression through a gather-then-broadcast exchange (Sec. 6 and Sec. 11; AIMech
+ *     mechanism "custom compressed allreduce": worker error delta^(i), server error epsilon).
+ *
+ * All n data-parallel workers are simulated on ONE GPU: worker i's gradient is one of the n
+ * gradient buffers passed to a step, and the exchange is index arithmetic over the workers' packed
+ * messages in this GPU's memory.  Nothing here communicates across GPUs.
+ *
+ * Per compression step, for every tensor k of the parameter list:
+ *   worker i:   m_i = b1*m + (1-b1)*g_i;  c_i = m_i + delta_i;
+ *               s_ik = ||c_i||_2 / sqrt(L_k) (scale that preserves the magnitude, Sec. 4.3 and the
+ *               codewithpapers "1-bit Adam" page);  bits_i = [c_i >= 0];  delta_i = c_i - s_ik*sign(c_i)
+ *   server j:   over shard j of tensor k:  a = (sum_{i=0..n-1} s_ik*sign_i) / n + eps_srv;
+ *               S_kj = ||a||_2 / sqrt(len_kj);  bitsS = [a >= 0];  eps_srv = a - S_kj*sign(a)
+ *   broadcast:  m = S_kj*sign(a) becomes the shared momentum;  x = x - lr*(m / (sqrt(v_Tw)+eps)).
+ * The n-term server sum is taken in worker order 0..n-1 in fp32; all elementwise arithmetic is fp32
+ * with no fused multiply-add; norms are accumulated in double and rounded once to fp32.
+ *
+ * Conventions used by every entry point:
+ *   - Errors: every call returns a status and never aborts.  Argument and phase checks happen on
+ *     the host before anything is enqueued; a failed check changes no state.  CUDA launch or copy
+ *     failures return ONEBIT_ERR_CUDA (onebit_adam_last_error() gives the CUDA message).  A
+ *     non-finite scale found on the device sets a sticky flag read by onebit_adam_get_status().
+ *   - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Calls enqueue work and
+ *     return without synchronising, except where stated.  All calls on one handle must be ordered
+ *     on one stream (or synchronised by the caller): the handle's state is updated in stream order.
+ *   - Memory: parameters and gradients are caller-owned device memory.  Gradients are only read
+ *     and must stay valid until the enqueued work completes.  Parameters are updated in place.
+ *     All optimizer state lives in the workspace (caller-provided or library-allocated).
+ *   - Layout: a parameter list has T tensors of numel L_k (one flat buffer is T = 1).  State
+ *     exported or imported per element is the concatenation of the tensors, without padding
+ *     (D = sum L_k).  Packed sign words: tensor k owns ceil(L_k/32) uint32 words, concatenated;
+ *     bit b of word w of tensor k is element 32w+b; a set bit means the value is >= 0 (+0 and -0
+ *     give 1, NaN gives 0); bits past L_k are 0.  Server shards of tensor k: S_k = 32*ceil(L_k/(32n)),
+ *     shard j = [j*S_k, min((j+1)*S_k, L_k)), possibly short or empty (an empty shard has scale 0).
+ */
+#ifndef ONEBIT_ADAM_H
+#define ONEBIT_ADAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct onebit_adam onebit_adam_t; /* opaque, owned by the library */
+typedef void* onebit_stream_t;            /* a cudaStream_t */
+
+typedef enum {
+  ONEBIT_OK = 0,
+  ONEBIT_ERR_INVALID_ARG = 1, /* a NULL or out-of-range argument, or an inconsistent config */
+  ONEBIT_ERR_PHASE = 2,       /* the call is not legal in the handle's current phase */
+  ONEBIT_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+  ONEBIT_ERR_NOMEM = 4,       /* a library allocation failed */
+  ONEBIT_ERR_WORKSPACE = 5,   /* the caller's workspace is too small or misaligned */
+  ONEBIT_ERR_NONFINITE = 6,   /* a worker or server scale was NaN or infinite */
+  ONEBIT_ERR_UNSUPPORTED = 7  /* a valid request this build does not support */
+} onebit_status_t;
+
+typedef enum { ONEBIT_F32 = 0, ONEBIT_F16 = 1, ONEBIT_BF16 = 2 } onebit_dtype_t;
+
+typedef enum { ONEBIT_PHASE_WARMUP = 0, ONEBIT_PHASE_COMPRESS = 1 } onebit_phase_t;
+
+/* What export/import/state_size address. */
+typedef enum {
+  ONEBIT_STATE_M = 0,             /* shared momentum m: D fp32 */
+  ONEBIT_STATE_V = 1,             /* warm-up: v; after the freeze: den = sqrt(v_Tw)+eps.  D fp32 */
+  ONEBIT_STATE_WORKER_ERROR = 2,  /* delta_i of one worker: D fp32 */
+  ONEBIT_STATE_SERVER_ERROR = 3,  /* eps_srv: D fp32 */
+  ONEBIT_STATE_WORKER_BITS = 4,   /* last message of one worker: W uint32 (export only) */
+  ONEBIT_STATE_SERVER_BITS = 5,   /* last broadcast: W uint32 (export only) */
+  ONEBIT_STATE_WORKER_SCALES = 6, /* last worker scales: n*T fp32, [worker][tensor] (export only) */
+  ONEBIT_STATE_SERVER_SCALES = 7  /* last server scales: T*n fp32, [tensor][shard] (export only) */
+} onebit_state_t;
+
+/* The kernels, for onebit_adam_kernel_times(). */
+typedef enum {
+  ONEBIT_K_WARMUP = 0,         /* fused worker-average + Adam */
+  ONEBIT_K_FREEZE = 1,         /* den = sqrt(v)+eps */
+  ONEBIT_K_WORKER = 2,         /* momentum + error + sign pack + norm partials, all workers */
+  ONEBIT_K_WORKER_SCALE = 3,   /* worker scales from the partials */
+  ONEBIT_K_SERVER = 4,         /* unpack + ordered average + server error + sign pack + partials */
+  ONEBIT_K_SERVER_SCALE = 5,   /* server shard scales from the partials */
+  ONEBIT_K_UPDATE = 6,         /* unpack broadcast + preconditioned update */
+  ONEBIT_K_EXPORT = 7,         /* state export / import */
+  ONEBIT_NUM_KERNELS = 8
+} onebit_kernel_t;
+
+typedef struct {
+  float beta1;             /* b1, 0 <= b1 < 1 */
+  float beta2;             /* b2, 0 <= b2 < 1 */
+  float eps;               /* epsilon of V = diag(sqrt(v) + eps), >= 0 */
+  float lr;                /* gamma */
+  int64_t warmup_steps;    /* T_w >= 1: warm-up steps before the variance is frozen */
+  int32_t n_workers;       /* n, 1 <= n <= 256 */
+  int32_t n_tensors;       /* T >= 1 (1 = one flat buffer) */
+  const int64_t* numel;    /* host array [T], L_k >= 0, sum L_k >= 1 */
+  int32_t grad_dtype;      /* onebit_dtype_t */
+  int32_t bias_correction; /* 0: the pages' formulas (default); 1: Kingma-Ba bias correction */
+} onebit_adam_config_t;
+
+/* Bytes of device workspace a config needs (256-byte aligned pieces included). */
+onebit_status_t onebit_adam_workspace_size(const onebit_adam_config_t* cfg, size_t* bytes);
+
+/* Create a handle.  params: host array [T] of device pointers to the fp32 parameters, kept for the
+ * handle's lifetime.  workspace: device memory of at least onebit_adam_workspace_size() bytes,
+ * 256-byte aligned, caller-owned; or NULL for a library cudaMalloc freed by onebit_adam_free().
+ * The state is zeroed on `stream` (m = v = 0, t = 0, phase WARMUP). */
+onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* params, void* workspace,
+                                 size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out);
+
+/* One warm-up Adam step (legal while phase == WARMUP and t < T_w).  grads: host array [n*T] of
+ * device pointers, ordered [worker][tensor], each L_k values of grad_dtype.  t += 1. */
+onebit_status_t onebit_adam_warmup_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream);
+
+/* Freeze the variance: den = sqrt(v) + eps (v / (1 - b2^t) first with bias correction).  Legal in
+ * phase WARMUP after at least one warm-up step; the phase becomes COMPRESS, worker and server
+ * errors start at 0 and the first compression step reads the fp32 warm-up momentum. */
+onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t stream);
+
+/* One compression-stage step (legal in phase COMPRESS).  grads as for warmup_step.  t += 1. */
+onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream);
+
+/* The same two steps with HOST gradient buffers ([n*T] host pointers, pinned or pageable): the
+ * library copies them into a device staging area it owns (allocated on first use, n*D*grad bytes),
+ * with cudaMemcpyAsync on `stream`, then runs the step.  Pageable sources are copied before the
+ * call returns; pinned sources must stay valid until the copy completes on `stream`. */
+onebit_status_t onebit_adam_warmup_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream);
+onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream);
+
+/* Release the handle (synchronises its device; frees library allocations only). */
+onebit_status_t onebit_adam_free(onebit_adam_t* h);
+
+/* Synchronise `stream` and report the sticky device flag: ONEBIT_OK or ONEBIT_ERR_NONFINITE. */
+onebit_status_t onebit_adam_get_status(onebit_adam_t* h, onebit_stream_t stream);
+/* Clear the sticky device flag (enqueued on `stream`). */
+onebit_status_t onebit_adam_clear_status(onebit_adam_t* h, onebit_stream_t stream);
+
+/* Current step count t and phase (host-side state, no synchronisation). */
+onebit_status_t onebit_adam_get_step(const onebit_adam_t* h, int64_t* t, int32_t* phase);
+/* Set t and the phase, for resuming from a checkpoint.  Moving to COMPRESS marks the errors zero
+ * and the momentum as the fp32 buffer (import them afterwards); the V buffer must then hold den. */
+onebit_status_t onebit_adam_set_step(onebit_adam_t* h, int64_t t, int32_t phase, onebit_stream_t stream);
+
+/* Bytes of one export/import buffer for `what` (see onebit_state_t). */
+onebit_status_t onebit_adam_state_size(const onebit_adam_t* h, int32_t what, size_t* bytes);
+
+/* Copy state `what` (worker index for per-worker items, else ignored) into device memory `dst`
+ * (onebit_adam_state_size() bytes) on `stream`.  Errors and the momentum are materialised in fp32. */
+onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worker, void* dst, onebit_stream_t stream);
+
+/* Load state `what` (M, V, WORKER_ERROR, SERVER_ERROR) from device memory `src` on `stream`.
+ * Importing an error in phase COMPRESS makes the next step use it exactly; importing M makes the
+ * next compression step read this fp32 momentum. */
+onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worker, const void* src, onebit_stream_t stream);
+
+/* Bytes one worker sends per compression step (sign words + one fp32 scale per tensor) and the
+ * bytes the same vector takes in fp32. */
+onebit_status_t onebit_adam_comm_bytes(const onebit_adam_t* h, uint64_t* compressed, uint64_t* fp32_bytes);
+
+/* Per-kernel timing with CUDA events recorded around every launch on the launch stream.
+ * kernel_times synchronises the recorded events, writes the total milliseconds and launch counts
+ * accumulated since the previous call (arrays of ONEBIT_NUM_KERNELS), and resets them. */
+onebit_status_t onebit_adam_set_timing(onebit_adam_t* h, int32_t enable);
+onebit_status_t onebit_adam_kernel_times(onebit_adam_t* h, double* ms, int64_t* launches);
+/* Kernel launches enqueued by this handle since init. */
+onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launches);
+
+/* The work chunks the kernels use for a config (host only, no GPU needed): up to `cap` rows of
+ * five int64 {tensor, shard, start element within the tensor, length, padded state offset}.
+ * *count receives the total number of chunks. */
+onebit_status_t onebit_adam_plan_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap, int64_t* count);
+
+/* Static description of a status code. */
+const char* onebit_adam_error_string(onebit_status_t status);
+/* Message of the last CUDA failure seen by this handle ("" if none). */
+const char* onebit_adam_last_error(const onebit_adam_t* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ONEBIT_ADAM_H */

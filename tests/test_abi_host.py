@@ -1,0 +1,110 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, validates configs and
+plans its chunk table (the multi-tensor launcher) correctly.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import communication_compressed_optimizer_compress_gb300 as ob
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from communication_compressed_optimizer_compress_gb300 import _build
+
+    _build.build()
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(onebit_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert len(names) >= 20, names
+    L = ctypes.CDLL(ob.LIB_PATH)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_error_strings():
+    for s in range(8):
+        assert ob.error_string(s)
+    assert "unknown" in ob.error_string(99)
+
+
+@pytest.mark.parametrize("kw,bad", [
+    (dict(numel=[0]), "empty"), (dict(numel=[-1, 5]), "negative"), (dict(n_workers=0), "n=0"),
+    (dict(n_workers=257), "n too large"), (dict(beta1=1.0), "beta1"), (dict(beta2=-0.1), "beta2"),
+    (dict(eps=-1.0), "eps"), (dict(warmup_steps=0), "T_w"), (dict(grad_dtype=3), "dtype"),
+])
+def test_config_validation(kw, bad):
+    base = dict(numel=[100], n_workers=2, warmup_steps=1)
+    base.update(kw)
+    cfg = ob.make_config(**base)
+    with pytest.raises(ob.OneBitError) as e:
+        ob.workspace_size(cfg)
+    assert e.value.status == ob.ERR_INVALID_ARG
+
+
+def test_null_arguments_return_status():
+    L = ob.lib()
+    assert L.onebit_adam_workspace_size(None, None) == ob.ERR_INVALID_ARG
+    assert L.onebit_adam_free(None) == ob.ERR_INVALID_ARG
+    assert L.onebit_adam_compress_step(None, None, None) == ob.ERR_INVALID_ARG
+    assert L.onebit_adam_get_status(None, None) == ob.ERR_INVALID_ARG
+    cfg = ob.make_config([10], 2)
+    assert L.onebit_adam_init(ctypes.byref(cfg), None, None, 0, None, None) == ob.ERR_INVALID_ARG
+
+
+SHAPES = [[1], [5, 0, 33, 200], [65536 * 3 + 17], [1 << 20], [1000] * 7, [110_000_000], [1, 1, 1]]
+
+
+@pytest.mark.parametrize("numel", SHAPES, ids=lambda v: f"T{len(v)}_{sum(v)}")
+@pytest.mark.parametrize("n", [1, 3, 8, 16])
+def test_chunk_plan(numel, n):
+    """Chunks tile every tensor exactly once, never cross a server shard (the oracle's shard rule),
+    start on a 32-element boundary, hold at most 65536 elements, and the padded offsets keep every
+    tensor 32-element aligned."""
+    rows = ob.plan_chunks(ob.make_config(numel, n))
+    by_tensor = {k: [] for k in range(len(numel))}
+    for (k, j, start, length, off) in rows:
+        by_tensor[k].append((j, start, length, off))
+        assert 1 <= length <= 65536 and start % 32 == 0 and off % 32 == 0
+    pad_off = 0
+    for k, L in enumerate(numel):
+        ch = by_tensor[k]
+        pos = 0
+        for (j, start, length, off) in ch:
+            assert start == pos
+            lo, hi = oracle.shard(L, n, j)
+            assert lo <= start and start + length <= hi
+            assert off == pad_off + start
+            pos += length
+        assert pos == L
+        pad_off += (L + 31) // 32 * 32
+
+
+def test_workspace_size_scales_with_workers():
+    a = ob.workspace_size(ob.make_config([1 << 20], 2))
+    b = ob.workspace_size(ob.make_config([1 << 20], 4))
+    # two more workers: two compensated-momentum rows (4 B/elem) and two sign rows (1/8 B/elem)
+    assert b - a >= 2 * (1 << 20) * 4 + 2 * (1 << 20) // 8
+
+
+def test_comm_bytes_volume_reduction_closed_form():
+    """The message of one worker is ceil(L/32) words + one scale per tensor: 1/32 of fp32."""
+    numel = [340_000_000]
+    compressed = sum(((L + 31) // 32) * 4 + 4 for L in numel)
+    assert abs(compressed / (4 * numel[0]) - 1 / 32) < 1e-6

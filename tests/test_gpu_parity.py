@@ -1,0 +1,262 @@
+"""CUDA path vs the oracle, element by element, on seeded inputs (free-running; see parity_util)."""
+import numpy as np
+import pytest
+import torch
+
+import communication_compressed_optimizer_compress_gb300 as ob
+from communication_compressed_optimizer_compress_gb300 import workloads as W
+from parity_util import Pair, _close
+
+pytestmark = pytest.mark.gpu
+
+
+def _tiny(**kw):
+    return W.WORKLOADS["tiny"].with_(**kw)
+
+
+def test_tiny_schedule():
+    """The Tiny workload: 2^20 fp32, n=4, 5 warm-up Adam steps then 5 compression steps, compared
+    after every step; the warm-up is bit-exact."""
+    p = Pair(_tiny())
+    for _ in range(5):
+        p.warmup(check=False)
+        p.check_warmup(exact=True)
+    p.freeze()
+    for _ in range(5):
+        p.compress()
+    st = p.stats
+    assert st.excluded_server / st.coords <= 1e-6, st
+    assert st.scales_exact >= 0.9 * st.scales, st
+    p.close()
+
+
+ODD = [
+    ([1], 1), ([31], 2), ([33], 3), ([32 * 4 - 1], 4), ([32 * 4 + 1], 4), ([(1 << 20) + 7], 8),
+    ([1, 5, 32, 33], 3), ([5, 0, 33, 200], 4), ([65536 * 2 + 100, 7], 16), ([1000], 16),
+]
+
+
+@pytest.mark.parametrize("numel,n", ODD, ids=[f"{'-'.join(map(str, a))}_n{b}" for a, b in ODD])
+@pytest.mark.parametrize("dtype", [W.F32, W.F16, W.BF16], ids=["f32", "f16", "bf16"])
+def test_odd_sizes(numel, n, dtype):
+    """Ragged tensors, tails that are not a multiple of 8 or 32, empty tensors and shards, several
+    chunks per shard, worker counts that are not powers of two, all gradient dtypes."""
+    w = _tiny(numel=tuple(numel), n_workers=n, grad_dtype=dtype, warmup_steps=2, compress_steps=3,
+              seed=7 + n + len(numel))
+    p = Pair(w)
+    st = p.run()
+    assert st.excluded_server <= max(2, 1e-5 * st.coords), st
+    p.close()
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.F16, W.BF16], ids=["f32", "f16", "bf16"])
+def test_misaligned_pointers(dtype):
+    """Parameters and gradients that start 4 or 2 bytes into an allocation take the scalar path."""
+    w = _tiny(numel=(5000, 77), n_workers=3, grad_dtype=dtype, warmup_steps=2, compress_steps=3, seed=21)
+    p = Pair(w, misalign=True)
+    p.run()
+    p.close()
+
+
+def test_bias_correction():
+    w = _tiny(numel=(4099,), n_workers=2, warmup_steps=4, compress_steps=3, seed=31)
+    p = Pair(w, bias_correction=True)
+    for _ in range(4):
+        p.warmup(check=False)
+        p.check_warmup(exact=True)
+    p.freeze()
+    for _ in range(3):
+        p.compress()
+    p.close()
+
+
+def test_heavy_tail_bf16():
+    """GPT-2-like gradient law (1% of coordinates x100) in bf16, n=4."""
+    w = W.WORKLOADS["gpt2_1p5b"].with_(numel=(300_001,), warmup_steps=3, compress_steps=4)
+    p = Pair(w)
+    p.run()
+    p.close()
+
+
+def test_block_sigma_f16():
+    """BERT-Large-like gradient law (log-uniform per-block sigma) in fp16, n=16, several blocks."""
+    w = W.WORKLOADS["bert_large"].with_(numel=(3 * (1 << 20) + 333,), warmup_steps=3, compress_steps=3)
+    p = Pair(w)
+    p.run()
+    p.close()
+
+
+def _state(opt, n):
+    out = {"m": opt.export_state(ob.STATE_M), "v": opt.export_state(ob.STATE_V),
+           "eps": opt.export_state(ob.STATE_SERVER_ERROR), "sb": opt.export_state(ob.STATE_SERVER_BITS),
+           "ws": opt.export_state(ob.STATE_WORKER_SCALES), "ss": opt.export_state(ob.STATE_SERVER_SCALES)}
+    for i in range(n):
+        out[f"d{i}"] = opt.export_state(ob.STATE_WORKER_ERROR, i)
+        out[f"b{i}"] = opt.export_state(ob.STATE_WORKER_BITS, i)
+    return {k: v.cpu().numpy().copy() for k, v in out.items()}
+
+
+def test_determinism():
+    """Two runs on the same inputs give bitwise-identical state (fixed-order reductions)."""
+    w = _tiny(numel=(200_003, 4096), n_workers=5, warmup_steps=2, compress_steps=3, seed=41)
+    res = []
+    for _ in range(2):
+        p = Pair(w)
+        for _ in range(2):
+            p.warmup(check=False)
+        p.freeze(check=False)
+        for _ in range(3):
+            p.compress(check=False)
+        torch.cuda.synchronize()
+        s = _state(p.gpu, w.n_workers)
+        s["x"] = p.x()
+        res.append(s)
+        p.close()
+    for k in res[0]:
+        assert np.array_equal(res[0][k].view(np.uint8), res[1][k].view(np.uint8)), k
+
+
+def test_checkpoint_resume():
+    """Export the state after some steps, import it into a fresh handle, continue: the result is
+    identical to the uninterrupted run."""
+    w = _tiny(numel=(70_001, 33), n_workers=3, warmup_steps=2, compress_steps=4, seed=51)
+    ref = Pair(w)
+    for _ in range(2):
+        ref.warmup(check=False)
+    ref.freeze(check=False)
+    for _ in range(2):
+        ref.compress(check=False)
+    torch.cuda.synchronize()
+    snap = {k: torch.from_numpy(v).cuda() for k, v in _state(ref.gpu, w.n_workers).items()}
+    x_snap = [p.detach().clone() for p in ref.params]
+    for _ in range(2):
+        ref.compress(check=False)
+    torch.cuda.synchronize()
+    want = _state(ref.gpu, w.n_workers)
+    want_x = ref.x()
+
+    params = [x.clone() for x in x_snap]
+    opt = ob.OneBitAdam(params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr)
+    opt.set_step(2 + 2, ob.PHASE_COMPRESS)
+    opt.import_state(ob.STATE_V, snap["v"])
+    opt.import_state(ob.STATE_M, snap["m"])
+    opt.import_state(ob.STATE_SERVER_ERROR, snap["eps"])
+    for i in range(w.n_workers):
+        opt.import_state(ob.STATE_WORKER_ERROR, snap[f"d{i}"], i)
+    src = W.GradSource(w, "cpu")
+    for step in (4, 5):
+        opt.compress_step([g.cuda() for g in src.grads(step)])
+    torch.cuda.synchronize()
+    got = _state(opt, w.n_workers)
+    got_x = torch.cat([p.cpu() for p in params]).numpy()
+    assert np.array_equal(got_x.view(np.uint32), want_x.view(np.uint32))
+    for k in want:
+        assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
+    opt.free()
+    ref.close()
+
+
+def test_host_gradient_entry_points():
+    """warmup_step_host / compress_step_host (host buffers copied by the library) equal the
+    device-pointer entry points."""
+    w = _tiny(numel=(10_007, 64), n_workers=2, grad_dtype=W.F16, warmup_steps=2, compress_steps=2, seed=61)
+    a, b = Pair(w), Pair(w)
+    for step in range(4):
+        g = a.grads()
+        b.grads()
+        host = [t.pin_memory() for t in g]
+        dev = [t.cuda() for t in g]
+        if step < 2:
+            a.gpu.warmup_step(dev)
+            b.gpu.warmup_step_host(host)
+        else:
+            if step == 2:
+                a.gpu.freeze_variance()
+                b.gpu.freeze_variance()
+            a.gpu.compress_step(dev)
+            b.gpu.compress_step_host(host)
+    torch.cuda.synchronize()
+    assert np.array_equal(a.x().view(np.uint32), b.x().view(np.uint32))
+    sa, sb = _state(a.gpu, 2), _state(b.gpu, 2)
+    for k in sa:
+        assert np.array_equal(sa[k].view(np.uint8), sb[k].view(np.uint8)), k
+    a.close()
+    b.close()
+
+
+def test_phase_errors_and_status():
+    w = _tiny(numel=(1000,), n_workers=2, warmup_steps=2)
+    p = Pair(w)
+    g = [t.cuda() for t in p.src.grads(0)]
+    with pytest.raises(ob.OneBitError) as e:
+        p.gpu.compress_step(g)
+    assert e.value.status == ob.ERR_PHASE
+    with pytest.raises(ob.OneBitError) as e:
+        p.gpu.freeze_variance()  # before any warm-up step
+    assert e.value.status == ob.ERR_PHASE
+    p.gpu.warmup_step(g)
+    p.gpu.warmup_step(g)
+    with pytest.raises(ob.OneBitError) as e:
+        p.gpu.warmup_step(g)  # T_w reached
+    assert e.value.status == ob.ERR_PHASE
+    p.gpu.freeze_variance()
+    with pytest.raises(ob.OneBitError) as e:
+        p.gpu.warmup_step(g)
+    assert e.value.status == ob.ERR_PHASE
+    p.gpu.compress_step(g)
+    assert p.gpu.get_status() == ob.OK
+    assert p.gpu.get_step() == (3, ob.PHASE_COMPRESS)
+    # a NaN gradient makes that worker's scale non-finite: the sticky flag reports it
+    bad = [t.clone() for t in g]
+    bad[1][17] = float("nan")
+    p.gpu.compress_step(bad)
+    assert p.gpu.get_status() == ob.ERR_NONFINITE
+    p.gpu.clear_status()
+    assert p.gpu.get_status() == ob.OK
+    p.close()
+
+
+def test_timing_and_launch_counts():
+    w = _tiny(numel=(50_000,), n_workers=4, warmup_steps=1)
+    p = Pair(w)
+    p.gpu.set_timing(True)
+    p.warmup(check=False)
+    p.freeze(check=False)
+    p.compress(check=False)
+    t = p.gpu.kernel_times()
+    assert t["warmup"][1] == 1 and t["freeze"][1] == 1
+    for k in ("worker", "worker_scale", "server", "server_scale", "update"):
+        assert t[k][1] == 1 and t[k][0] > 0.0, (k, t[k])
+    n0 = p.gpu.launch_count()
+    p.compress(check=False)
+    assert p.gpu.launch_count() - n0 == 5
+    p.close()
+
+
+def test_workspace_caller_owned():
+    """A caller-provided workspace (torch uint8 tensor) gives the same results as a library one."""
+    w = _tiny(numel=(12_345,), n_workers=3, warmup_steps=2, compress_steps=2, seed=71)
+    ws_bytes = ob.workspace_size(ob.make_config(list(w.numel), w.n_workers, w.warmup_steps))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    a = Pair(w)
+    params = [torch.cat([x.clone() for x in W.params(w, "cpu")]).cuda()]
+    opt = ob.OneBitAdam(params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr, workspace=ws)
+    src = W.GradSource(w, "cpu")
+    for step in range(4):
+        g = [t.cuda() for t in src.grads(step)]
+        if step < 2:
+            opt.warmup_step(g)
+            a.warmup(check=False)
+        else:
+            if step == 2:
+                opt.freeze_variance()
+                a.freeze(check=False)
+            opt.compress_step(g)
+            a.compress(check=False)
+    torch.cuda.synchronize()
+    assert np.array_equal(params[0].cpu().numpy().view(np.uint32), a.x().view(np.uint32))
+    with pytest.raises(ob.OneBitError) as e:
+        ob.OneBitAdam(params, w.n_workers, w.warmup_steps, workspace=ws[: ws_bytes // 2])
+    assert e.value.status == ob.ERR_WORKSPACE
+    opt.free()
+    a.close()
