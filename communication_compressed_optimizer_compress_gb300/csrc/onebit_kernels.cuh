@@ -27,8 +27,9 @@
 //
 // Arithmetic: fp32 with explicit round-to-nearest intrinsics (no contraction into FMA), in the
 // operation order of the method's formulas, so that the sign decisions match a plain CPU evaluation
-// bit for bit.  Sum-of-squares partials use short fp32 FMA runs (16 elements) promoted to fp64; the
-// per-chunk partials are reduced in a fixed order (deterministic, independent of the grid size).
+// bit for bit.  Sums of squares are exact per element (double-float accumulation, promoted to fp64
+// once per unit); the per-chunk partials are reduced in a fixed order (deterministic, independent
+// of the grid size).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -168,6 +169,39 @@ __device__ __forceinline__ double block_sum(double v, double* red) {
   return r;  // valid in thread 0
 }
 
+// Sum of squares without rounding error at the element level: c*c = p + pe exactly (FMA), p is
+// added to the running fp32 sum with an exact two-sum, and the two error terms are collected in a
+// second fp32 word.  (hi, lo) carries ~44 bits; it is promoted to double once per work unit.  This
+// keeps the scales equal to a double-precision evaluation (1 ulp at most, almost always 0) without
+// using the GPU's slow fp64 pipe per element.
+__device__ __forceinline__ void add_square(float& hi, float& lo, float c) {
+  const float p = __fmul_rn(c, c);
+  const float pe = __fmaf_rn(c, c, -p);
+  const float s = __fadd_rn(hi, p);
+  const float bb = __fsub_rn(s, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(err, pe));
+}
+
+// Transpose of an 8x8 bit matrix held in a 64-bit word (bit 8r+c -> bit 8c+r), by three rounds of
+// masked bit swaps (the classic recursive block transpose).
+__device__ __forceinline__ uint64_t transpose8x8(uint64_t x) {
+  uint64_t t;
+  t = (x ^ (x >> 7)) & 0x00AA00AA00AA00AAull;
+  x = x ^ t ^ (t << 7);
+  t = (x ^ (x >> 14)) & 0x0000CCCC0000CCCCull;
+  x = x ^ t ^ (t << 14);
+  t = (x ^ (x >> 28)) & 0x00000000F0F0F0F0ull;
+  x = x ^ t ^ (t << 28);
+  return x;
+}
+
+// +s when the bit is set, -s otherwise (flip of the sign bit)
+__device__ __forceinline__ float signed_scale(float s, uint32_t byte, int q) {
+  return __int_as_float(__float_as_int(s) ^ ((~byte << (31 - q)) & 0x80000000u));
+}
+
 // the fp32 operations of the method, in the oracle's order
 __device__ __forceinline__ float momentum(float b1, float omb1, float m, float g) {
   return __fadd_rn(__fmul_rn(b1, m), __fmul_rn(omb1, g));
@@ -215,10 +249,10 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       if (DENSE_M) ld8_stream(md + e, r.m);
       else r.mb = sb[gi];
     };
-    auto work = [&](const In& r, int gi) -> float {
+    float hi = 0.0f, lo = 0.0f;  // this thread's sum of c^2 over the unit
+    auto work = [&](const In& r, int gi) {
       float out[8];
       uint32_t byte = 0;
-      float sq = 0.0f;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float mq = DENSE_M ? r.m[q] : (((r.mb >> q) & 1u) ? Sp : -Sp);
@@ -227,34 +261,30 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
         const float cq = __fadd_rn(mi, d);
         out[q] = cq;
         byte |= (cq >= 0.0f ? 1u : 0u) << q;
-        sq = __fmaf_rn(cq, cq, sq);
+        add_square(hi, lo, cq);
       }
       st8(c + (int64_t)gi * 8, out);
       wb[gi] = (uint8_t)byte;
-      return sq;
     };
 
-    double acc = 0.0;
     const int ng = ch.len >> 3;
     int gi = threadIdx.x;
     for (; gi + kThreads < ng; gi += 2 * kThreads) {
       In r0, r1;
       load(r0, gi);
       load(r1, gi + kThreads);
-      const float s0 = work(r0, gi);
-      const float s1 = work(r1, gi + kThreads);
-      acc += (double)(s0 + s1);
+      work(r0, gi);
+      work(r1, gi + kThreads);
     }
     if (gi < ng) {
       In r0;
       load(r0, gi);
-      acc += (double)work(r0, gi);
+      work(r0, gi);
     }
     const int rem = ch.len & 7;
     if (rem && threadIdx.x == (ng % kThreads)) {  // the ragged end of a tensor: scalar
       const int64_t e0 = (int64_t)ng * 8;
       uint32_t byte = 0;
-      float sq = 0.0f;
       for (int q = 0; q < rem; ++q) {
         const int64_t e = e0 + q;
         const float mq = DENSE_M ? md[e] : (((sb[ng] >> q) & 1u) ? Sp : -Sp);
@@ -263,12 +293,11 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
         const float cq = __fadd_rn(mi, d);
         c[e] = cq;
         byte |= (cq >= 0.0f ? 1u : 0u) << q;
-        sq = __fmaf_rn(cq, cq, sq);
+        add_square(hi, lo, cq);
       }
       wb[ng] = (uint8_t)byte;
-      acc += (double)sq;
     }
-    const double tot = block_sum<kThreads>(acc, red);
+    const double tot = block_sum<kThreads>((double)hi + (double)lo, red);
     if (threadIdx.x == 0) A.wpart[(int64_t)i * A.n_chunks + ci] = tot;
   }
 }
@@ -277,8 +306,8 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
 // Scale kernels: one CTA per (worker, tensor) or (tensor, shard); fixed-order sum of the chunk
 // partials, then scale = sqrt(sum / len) in double, rounded once to fp32.
 
-__device__ __forceinline__ float finish_scale(const double* part, int64_t stride_unused, const Range r,
-                                              unsigned int* status, double* red) {
+__device__ __forceinline__ float finish_scale(const double* part, const Range r, unsigned int* status,
+                                              double* red) {
   double acc = 0.0;
   for (int c = threadIdx.x; c < r.count; c += kScaleThreads) acc += __ldcg(part + r.first + c);
   const double tot = block_sum<kScaleThreads>(acc, red);
@@ -287,43 +316,60 @@ __device__ __forceinline__ float finish_scale(const double* part, int64_t stride
     s = r.len > 0 ? __double2float_rn(sqrt(tot / (double)r.len)) : 0.0f;
     if (!isfinite(s)) atomicOr(status, 1u);
   }
-  (void)stride_unused;
   return s;
 }
 
 __global__ void __launch_bounds__(kScaleThreads) k_worker_scale(const StepArgs A) {
   __shared__ double red[kScaleThreads / 32];
   const int i = blockIdx.x / A.T, k = blockIdx.x % A.T;
-  const float s = finish_scale(A.wpart + (int64_t)i * A.n_chunks, 0, A.seg_ranges[k], A.status, red);
+  const float s = finish_scale(A.wpart + (int64_t)i * A.n_chunks, A.seg_ranges[k], A.status, red);
   if (threadIdx.x == 0) A.wscale_cur[blockIdx.x] = s;
 }
 
 __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const StepArgs A) {
   __shared__ double red[kScaleThreads / 32];
-  const float s = finish_scale(A.spart, 0, A.shard_ranges[blockIdx.x], A.status, red);
+  const float s = finish_scale(A.spart, A.shard_ranges[blockIdx.x], A.status, red);
   if (threadIdx.x == 0) A.sscale_cur[blockIdx.x] = s;
 }
 
 // ------------------------------------------------------------------------------------------------
 // K2: server.  One unit = one chunk of one shard.  For every element the n decompressed worker
-// messages are summed in worker order in fp32, divided by n, the server error is added; the result
-// a is written with its sign byte and the chunk's sum of a^2.
+// messages are summed in worker order in fp32, divided by n, and the server error is added; the
+// result a is written with its sign byte, and the chunk's sum of a^2 is kept.
+//
+// The ordered sum over the first min(n, 8) workers depends only on their 8 sign bits, so it is read
+// from a 256-entry table built per tensor with exactly those fp32 additions; an 8x8 bit transpose
+// turns the 8 workers' sign bytes into the 8 elements' table indices.  Workers 8.. are then added
+// one by one in order, so the result is the same fp32 value as the plain left-to-right sum.
 
 template <bool HAS_ERR>
 __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
   __shared__ float ssc[kMaxWorkers];
+  __shared__ float lut[256];
   __shared__ double red[kThreads / 32];
   const int n = A.n;
+  const int nl = n < 8 ? n : 8;
   const int64_t wrow = A.Wp * 4;  // bytes per worker row of sign words
+  int cur_seg = -1;
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
     const Chunk ch = A.chunks[u];
-    for (int i = threadIdx.x; i < n; i += kThreads) ssc[i] = A.wscale_cur[(int64_t)i * A.T + ch.seg];
-    __syncthreads();
+    if (ch.seg != cur_seg) {  // block-uniform
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += kThreads) ssc[i] = A.wscale_cur[(int64_t)i * A.T + ch.seg];
+      __syncthreads();
+      if (threadIdx.x < (1 << nl)) {
+        float acc = 0.0f;
+        for (int i = 0; i < nl; ++i) acc = __fadd_rn(acc, ((threadIdx.x >> i) & 1) ? ssc[i] : -ssc[i]);
+        lut[threadIdx.x] = acc;
+      }
+      __syncthreads();
+      cur_seg = ch.seg;
+    }
     const float Sp = HAS_ERR ? A.sscale_prev[(int64_t)ch.seg * n + ch.shard] : 0.0f;
     float* __restrict__ a = A.a + ch.off;
     const uint8_t* __restrict__ wb = reinterpret_cast<const uint8_t*>(A.wbits) + (ch.off >> 3);
     uint8_t* __restrict__ sb = reinterpret_cast<uint8_t*>(A.sbits) + (ch.off >> 3);
-    double acc = 0.0;
+    float hi = 0.0f, lo = 0.0f;
     const int ng = (ch.len + 7) >> 3;
     for (int gi = threadIdx.x; gi < ng; gi += kThreads) {
       const int cnt = min(8, ch.len - gi * 8);
@@ -334,18 +380,20 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
         else
           for (int q = 0; q < 8; ++q) ap[q] = q < cnt ? a[e + q] : 0.0f;
       }
+      uint64_t x = 0;
+      for (int i = 0; i < nl; ++i) x |= (uint64_t)__ldg(wb + (int64_t)i * wrow + gi) << (8 * i);
+      x = transpose8x8(x);
       float s[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) s[q] = 0.0f;
-      for (int i = 0; i < n; ++i) {
+      for (int q = 0; q < 8; ++q) s[q] = lut[(uint32_t)(x >> (8 * q)) & 0xffu];
+      for (int i = nl; i < n; ++i) {
         const uint32_t byte = __ldg(wb + (int64_t)i * wrow + gi);
         const float si = ssc[i];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) s[q] = __fadd_rn(s[q], ((byte >> q) & 1u) ? si : -si);
+        for (int q = 0; q < 8; ++q) s[q] = __fadd_rn(s[q], signed_scale(si, byte, q));
       }
       float out[8];
       uint32_t byte = 0;
-      float sq = 0.0f;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float avg = A.pow2 ? __fmul_rn(s[q], A.inv_n) : __fdiv_rn(s[q], A.nf);
@@ -354,16 +402,15 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
         out[q] = aq;
         if (q < cnt) {
           byte |= (aq >= 0.0f ? 1u : 0u) << q;
-          sq = __fmaf_rn(aq, aq, sq);
+          add_square(hi, lo, aq);
         }
       }
       if (cnt == 8) st8(a + e, out);
       else
         for (int q = 0; q < cnt; ++q) a[e + q] = out[q];
       sb[gi] = (uint8_t)byte;
-      acc += (double)sq;
     }
-    const double tot = block_sum<kThreads>(acc, red);  // also orders the ssc reuse
+    const double tot = block_sum<kThreads>((double)hi + (double)lo, red);
     if (threadIdx.x == 0) A.spart[u] = tot;
   }
 }
