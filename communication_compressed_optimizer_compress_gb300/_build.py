@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libonebit_adam.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
-SOURCES = ["onebit_adam.cu"]
+SOURCES = ["onebit_adam.cu", "onebit_noalloc.cu"]
 HEADERS = ["onebit_kernels.cuh", os.path.join("..", "..", "include", "onebit_adam.h")]
 
 NVCC_FLAGS = [

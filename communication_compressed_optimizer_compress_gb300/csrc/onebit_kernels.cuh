@@ -319,14 +319,14 @@ __device__ __forceinline__ float finish_scale(const double* part, const Range r,
   return s;
 }
 
-__global__ void __launch_bounds__(kScaleThreads) k_worker_scale(const StepArgs A) {
+static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale(const StepArgs A) {
   __shared__ double red[kScaleThreads / 32];
   const int i = blockIdx.x / A.T, k = blockIdx.x % A.T;
   const float s = finish_scale(A.wpart + (int64_t)i * A.n_chunks, A.seg_ranges[k], A.status, red);
   if (threadIdx.x == 0) A.wscale_cur[blockIdx.x] = s;
 }
 
-__global__ void __launch_bounds__(kScaleThreads) k_server_scale(const StepArgs A) {
+static __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const StepArgs A) {
   __shared__ double red[kScaleThreads / 32];
   const float s = finish_scale(A.spart, A.shard_ranges[blockIdx.x], A.status, red);
   if (threadIdx.x == 0) A.sscale_cur[blockIdx.x] = s;
@@ -584,7 +584,7 @@ struct ExportArgs {
   float* dst;
 };
 
-__global__ void __launch_bounds__(kThreads) k_export(const ExportArgs X) {
+static __global__ void __launch_bounds__(kThreads) k_export(const ExportArgs X) {
   for (int u = blockIdx.x; u < X.n_chunks; u += gridDim.x) {
     const Chunk ch = X.chunks[u];
     const float s = X.scales ? X.scales[(int64_t)ch.seg * X.scale_seg_mul + (int64_t)ch.shard * X.scale_shard_mul]

@@ -181,6 +181,37 @@ onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launch
  * *count receives the total number of chunks. */
 onebit_status_t onebit_adam_plan_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap, int64_t* count);
 
+/* Largest vector onebit_worker_compress_noalloc() accepts (elements). */
+#define ONEBIT_NOALLOC_MAX_LEN 268435456
+
+/* Worker compression of one vector, for callers that may not allocate device memory.
+ *
+ * No counterpart on the method's pages: it is a service of this library.  Code that runs under a
+ * framework whose caching allocator owns every device byte, in a latency-critical loop where
+ * cudaMalloc's implicit device-wide synchronisation is not acceptable, or in a plug-in that is handed
+ * buffers but no right to allocate, cannot obtain scratch memory.  This call needs none from the
+ * caller and allocates none itself (no cudaMalloc, cudaFree or allocating library routine): its
+ * scratch (per-chunk sum-of-squares partials and the scale, 32 KB) is a file-scope __device__ array
+ * that every GPU loading this library holds until the process exits.
+ *
+ * Computes, in the worker kernel's fp32 operation order:
+ *   c = (beta1*m + (1-beta1)*g) + err_in;   scale = ||c||_2 / sqrt(len);
+ *   bits = [c >= 0] packed (bit b of word w = element 32w+b, padding bits 0);
+ *   err_out = c - scale*sign(c).
+ * m: len fp32, device.  grad: len values of grad_dtype, device.  err_in: len fp32, device, or NULL
+ * for a zero error; it may be the same buffer as err_out but may not partly overlap it.
+ * bits_out: ceil(len/32) uint32, device.  scale_out: one fp32, device.  err_out: len fp32, device.
+ * 1 <= len <= ONEBIT_NOALLOC_MAX_LEN, otherwise ONEBIT_ERR_INVALID_ARG (nothing is enqueued).
+ *
+ * The first call on a device looks up the scratch array's device address (once per device, with
+ * that device current); make that first call before any stream capture.  Every call on a device
+ * shares the one scratch array and leaves the last call's contents in it; nothing in it needs
+ * clearing because each call writes every slot it reads.  Calls that overlap on the GPU (issued to
+ * different streams without ordering between them) race on the array and give wrong results. */
+onebit_status_t onebit_worker_compress_noalloc(const float* m, const void* grad, int32_t grad_dtype,
+                                               const float* err_in, float beta1, int64_t len, uint32_t* bits_out,
+                                               float* scale_out, float* err_out, onebit_stream_t stream);
+
 /* Static description of a status code. */
 const char* onebit_adam_error_string(onebit_status_t status);
 /* Message of the last CUDA failure seen by this handle ("" if none). */
