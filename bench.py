@@ -51,12 +51,27 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_from_profiles(name: str):
-    """DRAM bytes per element of a kernel from the committed ncu summary, if one exists."""
+def _kernel_source_hash(marker: str):
+    """Hash of one kernel's source region (from its heading comment to the next separator)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "communication_compressed_optimizer_compress_gb300", "csrc", "onebit_kernels.cuh")
+    src = open(path).read()
+    i = src.index(marker)
+    j = src.index("// ------", i)
+    return hashlib.sha256(src[i:j].encode()).hexdigest()[:16]
+
+
+def traffic_from_profiles(name: str, marker: str, elems: int):
+    """DRAM bytes per launch of a kernel from its committed ncu summary (bytes per element there x
+    the elements of this launch), or None when the kernel's source changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(name)
+            rec = json.load(f)[name]
+        if rec["source_sha256_16"] != _kernel_source_hash(marker):
+            return None
+        return rec["dram_bytes_per_elem"] * elems
     except Exception:
         return None
 
@@ -358,7 +373,8 @@ def main():
             "bytes_per_elem": ab["step"],
             "roofline": {"bound": "hbm", "kernel": "k_worker (momentum + error + sign pack + norm partials)",
                          "achieved": k1_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": k1_gbs / peak, "traffic": traffic_from_profiles("k_worker"),
+                         "frac": k1_gbs / peak,
+                         "traffic": traffic_from_profiles("k_worker", "// K1: worker momentum", w.d),
                          "bytes_per_elem": ab["worker"], "elems_per_launch": w.d},
             "kernels": per_kernel,
             "warmup_adam_ms_per_step": warm_ms,

@@ -184,6 +184,31 @@ __device__ __forceinline__ void add_square(float& hi, float& lo, float c) {
   lo = __fadd_rn(lo, __fadd_rn(err, pe));
 }
 
+// The same exact-square accumulation for two elements at once with Blackwell's packed fp32x2
+// arithmetic: (hi, lo) hold two independent (hi, lo) accumulators, one per half.
+__device__ __forceinline__ void add_square2(unsigned long long& hi, unsigned long long& lo, float c0, float c1) {
+  asm("{\n\t.reg .b64 c, p, np, pe, s, bb, t, u, e;\n\t"
+      "mov.b64 c, {%2, %3};\n\t"
+      "mul.rn.f32x2 p, c, c;\n\t"
+      "xor.b64 np, p, 0x8000000080000000;\n\t"
+      "fma.rn.f32x2 pe, c, c, np;\n\t"
+      "add.rn.f32x2 s, %0, p;\n\t"
+      "sub.rn.f32x2 bb, s, %0;\n\t"
+      "sub.rn.f32x2 t, s, bb;\n\t"
+      "sub.rn.f32x2 t, %0, t;\n\t"
+      "sub.rn.f32x2 u, p, bb;\n\t"
+      "add.rn.f32x2 e, t, u;\n\t"
+      "add.rn.f32x2 e, e, pe;\n\t"
+      "add.rn.f32x2 %1, %1, e;\n\t"
+      "mov.b64 %0, s;\n\t}"
+      : "+l"(hi), "+l"(lo)
+      : "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ double square_total(unsigned long long hi, unsigned long long lo) {
+  return ((double)__uint_as_float((uint32_t)hi) + (double)__uint_as_float((uint32_t)(hi >> 32))) +
+         ((double)__uint_as_float((uint32_t)lo) + (double)__uint_as_float((uint32_t)(lo >> 32)));
+}
+
 // Transpose of an 8x8 bit matrix held in a 64-bit word (bit 8r+c -> bit 8c+r), by three rounds of
 // masked bit swaps (the classic recursive block transpose).
 __device__ __forceinline__ uint64_t transpose8x8(uint64_t x) {
@@ -249,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       if (DENSE_M) ld8_stream(md + e, r.m);
       else r.mb = sb[gi];
     };
-    float hi = 0.0f, lo = 0.0f;  // this thread's sum of c^2 over the unit
+    unsigned long long hi = 0, lo = 0;  // this thread's sum of c^2 over the unit (two lanes)
     auto work = [&](const In& r, int gi) {
       float out[8];
       uint32_t byte = 0;
@@ -261,8 +286,9 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
         const float cq = __fadd_rn(mi, d);
         out[q] = cq;
         byte |= (cq >= 0.0f ? 1u : 0u) << q;
-        add_square(hi, lo, cq);
       }
+#pragma unroll
+      for (int q = 0; q < 8; q += 2) add_square2(hi, lo, out[q], out[q + 1]);
       st8(c + (int64_t)gi * 8, out);
       wb[gi] = (uint8_t)byte;
     };
@@ -293,11 +319,11 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
         const float cq = __fadd_rn(mi, d);
         c[e] = cq;
         byte |= (cq >= 0.0f ? 1u : 0u) << q;
-        add_square(hi, lo, cq);
+        add_square2(hi, lo, cq, 0.0f);
       }
       wb[ng] = (uint8_t)byte;
     }
-    const double tot = block_sum<kThreads>((double)hi + (double)lo, red);
+    const double tot = block_sum<kThreads>(square_total(hi, lo), red);
     if (threadIdx.x == 0) A.wpart[(int64_t)i * A.n_chunks + ci] = tot;
   }
 }
@@ -337,56 +363,86 @@ static __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const Ste
 // messages are summed in worker order in fp32, divided by n, and the server error is added; the
 // result a is written with its sign byte, and the chunk's sum of a^2 is kept.
 //
-// The ordered sum over the first min(n, 8) workers depends only on their 8 sign bits, so it is read
-// from a 256-entry table built per tensor with exactly those fp32 additions; an 8x8 bit transpose
-// turns the 8 workers' sign bytes into the 8 elements' table indices.  Workers 8.. are then added
-// one by one in order, so the result is the same fp32 value as the plain left-to-right sum.
+// The ordered sum over the first min(n, 12) workers depends only on their 12 sign bits, so it is read
+// from a 4096-entry shared-memory table built per tensor with exactly those fp32 additions
+// (level k: T_k[p] = T_{k-1}[p mod 2^k] + (bit k of p ? s_k : -s_k), starting from 0 + x_0).
+// Two 8x8 bit transposes turn the workers' sign bytes into the 8 elements' table indices.  Workers
+// 12.. are then added one by one in order, so the result is the same fp32 value as the plain
+// left-to-right sum.
+
+constexpr int kLutBits = 12;  // workers folded into the server's sum table
 
 template <bool HAS_ERR>
 __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
   __shared__ float ssc[kMaxWorkers];
-  __shared__ float lut[256];
+  __shared__ float lut[1 << kLutBits];
   __shared__ double red[kThreads / 32];
   const int n = A.n;
-  const int nl = n < 8 ? n : 8;
+  const int nl = n < kLutBits ? n : kLutBits;
   const int64_t wrow = A.Wp * 4;  // bytes per worker row of sign words
   int cur_seg = -1;
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
     const Chunk ch = A.chunks[u];
-    if (ch.seg != cur_seg) {  // block-uniform
+    if (ch.seg != cur_seg) {  // block-uniform: rebuild the table for this tensor's worker scales
       __syncthreads();
       for (int i = threadIdx.x; i < n; i += kThreads) ssc[i] = A.wscale_cur[(int64_t)i * A.T + ch.seg];
       __syncthreads();
-      if (threadIdx.x < (1 << nl)) {
-        float acc = 0.0f;
-        for (int i = 0; i < nl; ++i) acc = __fadd_rn(acc, ((threadIdx.x >> i) & 1) ? ssc[i] : -ssc[i]);
-        lut[threadIdx.x] = acc;
+      if (threadIdx.x == 0) {
+        lut[0] = __fadd_rn(0.0f, -ssc[0]);
+        lut[1] = __fadd_rn(0.0f, ssc[0]);
       }
       __syncthreads();
+      for (int k = 1; k < nl; ++k) {
+        const float sk = ssc[k];
+        for (int p = threadIdx.x; p < (1 << k); p += kThreads) {
+          const float old = lut[p];
+          lut[p] = __fadd_rn(old, -sk);
+          lut[p + (1 << k)] = __fadd_rn(old, sk);
+        }
+        __syncthreads();
+      }
       cur_seg = ch.seg;
     }
     const float Sp = HAS_ERR ? A.sscale_prev[(int64_t)ch.seg * n + ch.shard] : 0.0f;
     float* __restrict__ a = A.a + ch.off;
     const uint8_t* __restrict__ wb = reinterpret_cast<const uint8_t*>(A.wbits) + (ch.off >> 3);
     uint8_t* __restrict__ sb = reinterpret_cast<uint8_t*>(A.sbits) + (ch.off >> 3);
-    float hi = 0.0f, lo = 0.0f;
+    unsigned long long hi = 0, lo = 0;
     const int ng = (ch.len + 7) >> 3;
     for (int gi = threadIdx.x; gi < ng; gi += kThreads) {
-      const int cnt = min(8, ch.len - gi * 8);
       const int64_t e = (int64_t)gi * 8;
+      const int cnt = ch.len - gi * 8;  // >= 8 except in a tensor's last group
+      // all sign bytes of this group first (one memory latency for the whole group)
+      uint32_t b[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) b[i] = i < n ? (uint32_t)__ldg(wb + (int64_t)i * wrow + gi) : 0u;
       float ap[8];
       if (HAS_ERR) {
-        if (cnt == 8) ld8_state(a + e, ap);
-        else
+        if (cnt >= 8) {
+          ld8_state(a + e, ap);
+        } else {
+#pragma unroll
           for (int q = 0; q < 8; ++q) ap[q] = q < cnt ? a[e + q] : 0.0f;
+        }
       }
-      uint64_t x = 0;
-      for (int i = 0; i < nl; ++i) x |= (uint64_t)__ldg(wb + (int64_t)i * wrow + gi) << (8 * i);
-      x = transpose8x8(x);
+      const uint32_t w0 = __byte_perm(b[0] | (b[1] << 8), b[2] | (b[3] << 8), 0x5410);
+      const uint32_t w1 = __byte_perm(b[4] | (b[5] << 8), b[6] | (b[7] << 8), 0x5410);
+      const uint64_t t0 = transpose8x8(((uint64_t)w1 << 32) | w0);
+      uint64_t t1 = 0;
+      if (nl > 8) t1 = transpose8x8((uint64_t)__byte_perm(b[8] | (b[9] << 8), b[10] | (b[11] << 8), 0x5410));
       float s[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) s[q] = lut[(uint32_t)(x >> (8 * q)) & 0xffu];
-      for (int i = nl; i < n; ++i) {
+      for (int q = 0; q < 8; ++q)
+        s[q] = lut[((uint32_t)(t0 >> (8 * q)) & 0xffu) | (((uint32_t)(t1 >> (8 * q)) & 0x0fu) << 8)];
+#pragma unroll
+      for (int i = kLutBits; i < 16; ++i) {
+        if (i < n) {
+          const float si = ssc[i];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) s[q] = __fadd_rn(s[q], signed_scale(si, b[i], q));
+        }
+      }
+      for (int i = 16; i < n; ++i) {
         const uint32_t byte = __ldg(wb + (int64_t)i * wrow + gi);
         const float si = ssc[i];
 #pragma unroll
@@ -398,19 +454,26 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
       for (int q = 0; q < 8; ++q) {
         const float avg = A.pow2 ? __fmul_rn(s[q], A.inv_n) : __fdiv_rn(s[q], A.nf);
         const float ep = HAS_ERR ? error_of(ap[q], Sp) : 0.0f;
-        const float aq = __fadd_rn(avg, ep);
-        out[q] = aq;
-        if (q < cnt) {
-          byte |= (aq >= 0.0f ? 1u : 0u) << q;
-          add_square(hi, lo, aq);
+        out[q] = __fadd_rn(avg, ep);
+        byte |= (out[q] >= 0.0f ? 1u : 0u) << q;
+      }
+      if (cnt >= 8) {
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) add_square2(hi, lo, out[q], out[q + 1]);
+        st8(a + e, out);
+      } else {
+        byte &= (1u << cnt) - 1u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q < cnt) {
+            a[e + q] = out[q];
+            add_square2(hi, lo, out[q], 0.0f);
+          }
         }
       }
-      if (cnt == 8) st8(a + e, out);
-      else
-        for (int q = 0; q < cnt; ++q) a[e + q] = out[q];
       sb[gi] = (uint8_t)byte;
     }
-    const double tot = block_sum<kThreads>((double)hi + (double)lo, red);
+    const double tot = block_sum<kThreads>(square_total(hi, lo), red);
     if (threadIdx.x == 0) A.spart[u] = tot;
   }
 }

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads) k_vec_worker(const float* __restrict
         }
       }
     };
-    float hi = 0.0f, lo = 0.0f;
+    unsigned long long hi = 0, lo = 0;
     auto work = [&](const In& r, int gi) {
       float out[8];
       uint32_t byte = 0;
@@ -74,8 +74,9 @@ __global__ void __launch_bounds__(kThreads) k_vec_worker(const float* __restrict
         const float cq = __fadd_rn(mi, HAS_ERR ? r.e[q] : 0.0f);
         out[q] = cq;
         byte |= (cq >= 0.0f ? 1u : 0u) << q;
-        add_square(hi, lo, cq);
       }
+#pragma unroll
+      for (int q = 0; q < 8; q += 2) add_square2(hi, lo, out[q], out[q + 1]);
       if (VEC) {
         st8(cc + (int64_t)gi * 8, out);
       } else {
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) k_vec_worker(const float* __restrict
         const float cq = __fadd_rn(mi, HAS_ERR ? ec[e] : 0.0f);
         cc[e] = cq;
         byte |= (cq >= 0.0f ? 1u : 0u) << q;
-        add_square(hi, lo, cq);
+        add_square2(hi, lo, cq, 0.0f);
       }
       bc[ng] = (uint8_t)byte;
     }
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) k_vec_worker(const float* __restrict
       const int64_t used = (len + 7) >> 3, words = (len + 31) >> 5;
       for (int64_t b = used; b < words * 4; ++b) bits[b] = 0;
     }
-    const double tot = block_sum<kThreads>((double)hi + (double)lo, red);
+    const double tot = block_sum<kThreads>(square_total(hi, lo), red);
     if (threadIdx.x == 0) part[ci] = tot;
   }
 }
