@@ -367,8 +367,10 @@ static __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const Ste
 // from a 4096-entry shared-memory table built per tensor with exactly those fp32 additions
 // (level k: T_k[p] = T_{k-1}[p mod 2^k] + (bit k of p ? s_k : -s_k), starting from 0 + x_0).
 // Two 8x8 bit transposes turn the workers' sign bytes into the 8 elements' table indices.  Workers
-// 12.. are then added one by one in order, so the result is the same fp32 value as the plain
-// left-to-right sum.
+// 12..15 are then added one by one in order; their four signed scales come as one float4 from a
+// 16-entry table indexed by their 4 sign bits (one copy per lane, so the lookups never conflict).
+// Workers 16.. (if any) are added from their sign bytes.  The result is the same fp32 value as the
+// plain left-to-right sum.
 
 constexpr int kLutBits = 12;  // workers folded into the server's sum table
 
@@ -376,9 +378,11 @@ template <bool HAS_ERR>
 __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
   __shared__ float ssc[kMaxWorkers];
   __shared__ float lut[1 << kLutBits];
+  __shared__ float4 quad[16 * 32];  // [pattern of workers 12..15][lane]
   __shared__ double red[kThreads / 32];
   const int n = A.n;
   const int nl = n < kLutBits ? n : kLutBits;
+  const int lane = threadIdx.x & 31;
   const int64_t wrow = A.Wp * 4;  // bytes per worker row of sign words
   int cur_seg = -1;
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
@@ -398,6 +402,19 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
           const float old = lut[p];
           lut[p] = __fadd_rn(old, -sk);
           lut[p + (1 << k)] = __fadd_rn(old, sk);
+        }
+        __syncthreads();
+      }
+      if (n > kLutBits) {
+        for (int p = threadIdx.x; p < 16 * 32; p += kThreads) {
+          const int pat = p >> 5;
+          float v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float sj = kLutBits + j < n ? ssc[kLutBits + j] : 0.0f;
+            v[j] = ((pat >> j) & 1) ? sj : -sj;
+          }
+          quad[p] = make_float4(v[0], v[1], v[2], v[3]);
         }
         __syncthreads();
       }
@@ -429,17 +446,22 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
       const uint32_t w1 = __byte_perm(b[4] | (b[5] << 8), b[6] | (b[7] << 8), 0x5410);
       const uint64_t t0 = transpose8x8(((uint64_t)w1 << 32) | w0);
       uint64_t t1 = 0;
-      if (nl > 8) t1 = transpose8x8((uint64_t)__byte_perm(b[8] | (b[9] << 8), b[10] | (b[11] << 8), 0x5410));
+      if (nl > 8) {
+        const uint32_t w2 = __byte_perm(b[8] | (b[9] << 8), b[10] | (b[11] << 8), 0x5410);
+        const uint32_t w3 = __byte_perm(b[12] | (b[13] << 8), b[14] | (b[15] << 8), 0x5410);
+        t1 = transpose8x8(((uint64_t)w3 << 32) | w2);
+      }
       float s[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        s[q] = lut[((uint32_t)(t0 >> (8 * q)) & 0xffu) | (((uint32_t)(t1 >> (8 * q)) & 0x0fu) << 8)];
-#pragma unroll
-      for (int i = kLutBits; i < 16; ++i) {
-        if (i < n) {
-          const float si = ssc[i];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) s[q] = __fadd_rn(s[q], signed_scale(si, b[i], q));
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t hi8 = (uint32_t)(t1 >> (8 * q)) & 0xffu;
+        s[q] = lut[((uint32_t)(t0 >> (8 * q)) & 0xffu) | ((hi8 & 0x0fu) << 8)];
+        if (n > kLutBits) {  // workers 12..15, in order
+          const float4 qv = quad[(hi8 >> 4) * 32 + lane];
+          s[q] = __fadd_rn(s[q], qv.x);
+          if (n > kLutBits + 1) s[q] = __fadd_rn(s[q], qv.y);
+          if (n > kLutBits + 2) s[q] = __fadd_rn(s[q], qv.z);
+          if (n > kLutBits + 3) s[q] = __fadd_rn(s[q], qv.w);
         }
       }
       for (int i = 16; i < n; ++i) {
@@ -542,11 +564,42 @@ __global__ void __launch_bounds__(kThreads) k_update(const StepArgs A) {
 
 // ------------------------------------------------------------------------------------------------
 // K0: warm-up.  Mean of the n worker gradients (summed in worker order), then one Adam step.
+// The gradients are fetched in batches (8 workers for 16-bit, 4 for fp32 gradients) whose loads are
+// all issued before the batch is added in order, so one memory latency covers a whole batch.
+
+template <typename GT> struct RawGrad;  // one 8-element gradient group as loaded
+template <> struct RawGrad<float> {
+  float v[8];
+  __device__ __forceinline__ void load(const float* p) { ld8_stream(p, v); }
+  __device__ __forceinline__ float get(int q) const { return v[q]; }
+};
+template <> struct RawGrad<__half> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __half* p) { u = ld16_stream(p); }
+  __device__ __forceinline__ float get(int q) const {
+    const uint32_t w = q < 2 ? u.x : q < 4 ? u.y : q < 6 ? u.z : u.w;
+    return __half2float(__ushort_as_half((unsigned short)((q & 1) ? (w >> 16) : (w & 0xffffu))));
+  }
+};
+template <> struct RawGrad<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = ld16_stream(p); }
+  __device__ __forceinline__ float get(int q) const {
+    const uint32_t w = q < 2 ? u.x : q < 4 ? u.y : q < 6 ? u.z : u.w;
+    return __uint_as_float((q & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+};
 
 template <typename GT, bool BC, bool VEC>
 __global__ void __launch_bounds__(kThreads) k_warmup(const StepArgs A) {
+  constexpr int B = sizeof(GT) == 4 ? 4 : 8;
+  __shared__ const GT* gsm[kMaxWorkers];
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
     const Chunk ch = A.chunks[u];
+    __syncthreads();
+    for (int i = threadIdx.x; i < A.n; i += kThreads)
+      gsm[i] = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start;
+    __syncthreads();
     float* __restrict__ x = A.pptr[ch.seg] + ch.start;
     float* __restrict__ m = A.m + ch.off;
     float* __restrict__ v = A.v + ch.off;
@@ -554,34 +607,46 @@ __global__ void __launch_bounds__(kThreads) k_warmup(const StepArgs A) {
     for (int gi = threadIdx.x; gi < ng; gi += kThreads) {
       const int cnt = min(8, ch.len - gi * 8);
       const int64_t e = (int64_t)gi * 8;
-      float acc[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-      for (int i = 0; i < A.n; ++i) {
-        const GT* gp = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start + e;
-        float gv[8];
-        if (VEC && cnt == 8) {
-          Grad<GT>::load8(gp, gv);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) gv[q] = q < cnt ? Grad<GT>::load1(gp + q) : 0.0f;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], gv[q]);
-      }
+      const bool vec = VEC && cnt == 8;
       float mv[8], vv[8], xv[8];
       if (cnt == 8) {
         ld8_state(m + e, mv);
         ld8_state(v + e, vv);
       } else {
+#pragma unroll
         for (int q = 0; q < 8; ++q) {
           mv[q] = q < cnt ? m[e + q] : 0.0f;
           vv[q] = q < cnt ? v[e + q] : 0.0f;
         }
       }
-      if (VEC && cnt == 8) ld8_state(x + e, xv);
-      else
+      if (vec) {
+        ld8_state(x + e, xv);
+      } else {
+#pragma unroll
         for (int q = 0; q < 8; ++q) xv[q] = q < cnt ? x[e + q] : 0.0f;
+      }
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+      for (int i0 = 0; i0 < A.n; i0 += B) {
+        if (vec) {
+          RawGrad<GT> r[B];
+#pragma unroll
+          for (int j = 0; j < B; ++j)
+            if (i0 + j < A.n) r[j].load(gsm[i0 + j] + e);
+#pragma unroll
+          for (int j = 0; j < B; ++j)
+            if (i0 + j < A.n)
+#pragma unroll
+              for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], r[j].get(q));
+        } else {
+          for (int j = 0; j < B && i0 + j < A.n; ++j) {
+            const GT* gp = gsm[i0 + j] + e;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], q < cnt ? Grad<GT>::load1(gp + q) : 0.0f);
+          }
+        }
+      }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float gbar = A.pow2 ? __fmul_rn(acc[q], A.inv_n) : __fdiv_rn(acc[q], A.nf);
@@ -595,14 +660,20 @@ __global__ void __launch_bounds__(kThreads) k_warmup(const StepArgs A) {
         st8(m + e, mv);
         st8(v + e, vv);
       } else {
-        for (int q = 0; q < cnt; ++q) {
-          m[e + q] = mv[q];
-          v[e + q] = vv[q];
-        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < cnt) {
+            m[e + q] = mv[q];
+            v[e + q] = vv[q];
+          }
       }
-      if (VEC && cnt == 8) st8(x + e, xv);
-      else
-        for (int q = 0; q < cnt; ++q) x[e + q] = xv[q];
+      if (vec) {
+        st8(x + e, xv);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < cnt) x[e + q] = xv[q];
+      }
     }
   }
 }
