@@ -18,6 +18,7 @@ F32, F16, BF16 = 0, 1, 2
 PHASE_WARMUP, PHASE_COMPRESS = 0, 1
 (STATE_M, STATE_V, STATE_WORKER_ERROR, STATE_SERVER_ERROR, STATE_WORKER_BITS, STATE_SERVER_BITS,
  STATE_WORKER_SCALES, STATE_SERVER_SCALES) = range(8)
+FAULT_NONE, FAULT_STALL_COPIES = 0, 1
 KERNEL_NAMES = ["warmup", "freeze", "worker", "worker_scale", "server", "server_scale", "update", "export"]
 NUM_KERNELS = len(KERNEL_NAMES)
 
@@ -82,6 +83,7 @@ def lib() -> ctypes.CDLL:
             "onebit_adam_kernel_times": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)],
             "onebit_adam_launch_count": [vp, ctypes.POINTER(i64)],
             "onebit_adam_plan_chunks": [cfgp, ctypes.POINTER(i64), i64, ctypes.POINTER(i64)],
+            "onebit_adam_set_fault_injection": [vp, i32, i64],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -262,6 +264,10 @@ class OneBitAdam:
         cnt = (ctypes.c_int64 * NUM_KERNELS)()
         _check(lib().onebit_adam_kernel_times(self.h, ms, cnt), "onebit_adam_kernel_times", self.h)
         return {KERNEL_NAMES[k]: (ms[k], cnt[k]) for k in range(NUM_KERNELS)}
+
+    def set_fault_injection(self, kind: int, value: int = 0):
+        _check(lib().onebit_adam_set_fault_injection(self.h, int(kind), int(value)),
+               "onebit_adam_set_fault_injection")
 
     def launch_count(self) -> int:
         out = ctypes.c_int64()

@@ -33,7 +33,7 @@ struct Plan {
   std::vector<int64_t> numel;
   std::vector<int64_t> seg_off;   // padded offsets
   std::vector<int64_t> seg_uoff;  // unpadded offsets
-  int64_t Dp = 0, D = 0, Wp = 0;
+  int64_t Dp = 0, D = 0, Wp = 0, Wr = 0;  // Wr: worker sign-row stride in words (multiple of 4)
   std::vector<Chunk> chunks;
   std::vector<Range> seg_ranges;    // [T]
   std::vector<Range> shard_ranges;  // [T*n]
@@ -108,6 +108,7 @@ onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
   P->Dp = off;
   P->D = uoff;
   P->Wp = off / 32;
+  P->Wr = (P->Wp + 3) / 4 * 4;
   return ONEBIT_OK;
 }
 
@@ -129,7 +130,7 @@ Layout make_layout(const Plan& P) {
   L.v = take(P.Dp * 4);
   L.a = take(P.Dp * 4);
   L.c = take(n * P.Dp * 4);
-  L.wbits = take(n * P.Wp * 4);
+  L.wbits = take(n * P.Wr * 4);
   L.sbits = take(P.Wp * 4);
   L.wscale = take(2 * n * T * 4);
   L.sscale = take(2 * n * T * 4);
@@ -180,6 +181,8 @@ struct onebit_adam {
   std::vector<cudaEvent_t> event_pool;
   int64_t launches = 0;
   std::unordered_map<const void*, int> occupancy;
+  bool smem_configured[2] = {false, false};
+  uint32_t stall_tx = 0;  // fault injection (see onebit_adam_set_fault_injection)
   std::string last_error;
 
   template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
@@ -213,11 +216,11 @@ onebit_status_t cuda_fail(onebit_adam* h, cudaError_t e, const char* where) {
 
 cudaStream_t as_stream(onebit_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
-int grid_for(onebit_adam* h, const void* fn, int threads, int64_t units) {
+int grid_for(onebit_adam* h, const void* fn, int threads, int64_t units, size_t dyn_smem = 0) {
   auto it = h->occupancy.find(fn);
   int per_sm;
   if (it == h->occupancy.end()) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, dyn_smem) != cudaSuccess || per_sm < 1)
       per_sm = 1;
     h->occupancy[fn] = per_sm;
   } else {
@@ -241,14 +244,14 @@ cudaEvent_t take_event(onebit_adam* h) {
 // Launch one kernel on `stream`, bracketed by timing events when timing is on.
 template <typename Kern, typename Arg>
 onebit_status_t launch(onebit_adam* h, int kid, Kern kern, int grid, int threads, cudaStream_t stream,
-                       const Arg& arg) {
+                       const Arg& arg, size_t dyn_smem = 0) {
   TimedLaunch tl{kid, nullptr, nullptr};
   if (h->timing) {
     tl.start = take_event(h);
     tl.stop = take_event(h);
     if (tl.start) cudaEventRecord(tl.start, stream);
   }
-  kern<<<grid, threads, 0, stream>>>(arg);
+  kern<<<grid, threads, dyn_smem, stream>>>(arg);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
   ++h->launches;
@@ -270,6 +273,7 @@ StepArgs base_args(onebit_adam* h) {
   A.pow2 = (P.n & (P.n - 1)) == 0;
   A.Dp = P.Dp;
   A.Wp = P.Wp;
+  A.Wr = P.Wr;
   A.pptr = h->at<float*>(L.pptr);
   A.m = h->at<float>(L.m);
   A.v = h->at<float>(L.v);
@@ -299,6 +303,7 @@ StepArgs base_args(onebit_adam* h) {
   A.inv_n = 1.0f / (float)P.n;
   A.bc1 = 1.0f;
   A.bc2 = 1.0f;
+  A.stall_tx = h->stall_tx;
   return A;
 }
 
@@ -362,6 +367,29 @@ onebit_status_t run_worker(onebit_adam* h, const StepArgs& A, bool vec, cudaStre
   return run_worker_v<GT, false, false>(h, A, vec, st);
 }
 
+template <bool HE>
+onebit_status_t run_server_v(onebit_adam* h, const StepArgs& A, cudaStream_t st) {
+  if (A.n <= kStageMaxWorkers) {
+    // shared-memory staged variant: the tiles of a and the n sign rows arrive by bulk copies
+    auto k = k_server_staged<HE>;
+    const size_t dyn = server_dyn_smem(A.n);
+    if (!h->smem_configured[HE ? 1 : 0]) {
+      cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)server_dyn_smem(kStageMaxWorkers));
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute");
+      h->smem_configured[HE ? 1 : 0] = true;
+    }
+    return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kStagedThreads, A.n_chunks, dyn), kStagedThreads,
+                  st, A, dyn);
+  }
+  auto k = k_server<HE>;
+  return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+}
+
+onebit_status_t run_server(onebit_adam* h, const StepArgs& A, cudaStream_t st) {
+  return h->serr_zero ? run_server_v<false>(h, A, st) : run_server_v<true>(h, A, st);
+}
+
 onebit_status_t do_warmup(onebit_adam* h, const void* const* grads, cudaStream_t st) {
   if (h->phase != ONEBIT_PHASE_WARMUP) return ONEBIT_ERR_PHASE;
   if (h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
@@ -397,14 +425,7 @@ onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream
   if (s) return s;
   const int nt = h->plan.n * h->plan.T;
   if ((s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale, nt, kScaleThreads, st, A))) return s;
-  if (h->serr_zero) {
-    auto k = k_server<false>;
-    s = launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
-  } else {
-    auto k = k_server<true>;
-    s = launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
-  }
-  if (s) return s;
+  if ((s = run_server(h, A, st))) return s;
   if ((s = launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale, nt, kScaleThreads, st, A))) return s;
   if (h->params_aligned) {
     auto k = k_update<true>;
@@ -689,6 +710,10 @@ onebit_status_t onebit_adam_get_status(onebit_adam_t* h, onebit_stream_t stream)
   cudaStream_t st = as_stream(stream);
   ONEBIT_CUDA(h, cudaMemcpyAsync(&flag, h->ws + h->lay.status, sizeof flag, cudaMemcpyDeviceToHost, st));
   ONEBIT_CUDA(h, cudaStreamSynchronize(st));
+  if (flag & 2u) {
+    h->last_error = "a kernel's wait for its asynchronous copies timed out";
+    return ONEBIT_ERR_CUDA;
+  }
   return flag ? ONEBIT_ERR_NONFINITE : ONEBIT_OK;
 }
 
@@ -761,7 +786,7 @@ onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worke
         return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
       return run_export(h, kExportSignedErr, h->at<float>(h->lay.a), nullptr, last_sscale(h), P.n, 1, out, st);
     case ONEBIT_STATE_WORKER_BITS:
-      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.wbits) + (size_t)worker * P.Wp, P.Wp * 4,
+      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.wbits) + (size_t)worker * P.Wr, P.Wp * 4,
                                      cudaMemcpyDeviceToDevice, st));
       return ONEBIT_OK;
     case ONEBIT_STATE_SERVER_BITS:
@@ -860,6 +885,18 @@ onebit_status_t onebit_adam_kernel_times(onebit_adam_t* h, double* ms, int64_t* 
   }
   h->timed.clear();
   return rc;
+}
+
+onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, int64_t value) {
+  if (!h) return ONEBIT_ERR_INVALID_ARG;
+  switch (kind) {
+    case ONEBIT_FAULT_NONE: h->stall_tx = 0; return ONEBIT_OK;
+    case ONEBIT_FAULT_STALL_COPIES:
+      if (value < 1 || value > (1 << 20)) return ONEBIT_ERR_INVALID_ARG;
+      h->stall_tx = (uint32_t)value;
+      return ONEBIT_OK;
+    default: return ONEBIT_ERR_INVALID_ARG;
+  }
 }
 
 onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launches) {

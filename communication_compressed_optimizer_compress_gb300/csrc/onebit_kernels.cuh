@@ -8,14 +8,15 @@
 //
 // Data layout in HBM (one GPU simulates the n workers):
 //   every per-element state array uses a padded layout in which tensor k starts at element
-//   off_k = sum_{k'<k} roundup(L_k', 32); Dp = padded total, Wp = Dp / 32 sign words.
+//   off_k = sum_{k'<k} roundup(L_k', 32); Dp = padded total, Wp = Dp / 32 sign words; worker sign
+//   rows are Wr = roundup(Wp, 4) words apart, so every row starts on a 16-byte boundary.
 //   m[Dp]        fp32 momentum (dense form: warm-up and the first compression step)
 //   v[Dp]        fp32 variance; after the freeze den = sqrt(v) + eps
 //   c[n][Dp]     fp32 compensated momentum c_i of the last step.  The worker error of that step is
 //                delta_i = c_i - s_i*sign(c_i), recomputed from c_i and the last scale s_i with the
 //                same single fp32 operation wherever it is needed, so it is never stored.
 //   a[Dp]        fp32 server input of the last step; server error eps = a - S*sign(a), likewise.
-//   wbits[n][Wp] worker sign words; sbits[Wp] server sign words (= the broadcast momentum's signs:
+//   wbits[n][Wr] worker sign words; sbits[Wp] server sign words (= the broadcast momentum's signs:
 //                after a compression step m = S*sign(a) is represented by sbits and S, 1/8 B/elem).
 //   scales       double-buffered by step parity: a step reads the previous step's scales (to rebuild
 //                the errors and m) and writes its own.
@@ -67,6 +68,7 @@ struct StepArgs {
   int32_t pow2;   // n is a power of two: x / n == x * (1/n) exactly
   int64_t Dp;     // padded elements per row
   int64_t Wp;     // sign words per row
+  int64_t Wr;     // worker sign-row stride in words (multiple of 4)
   const void* const* gptr;  // [n*T] gradient pointers, [worker][tensor]
   float* const* pptr;       // [T] parameter pointers
   float* m;
@@ -85,6 +87,7 @@ struct StepArgs {
   const Range* shard_ranges; // [T*n] chunks of each server shard
   unsigned int* status;
   float b1, omb1, b2, omb2, lr, eps, inv_n, nf, bc1, bc2;
+  uint32_t stall_tx;  // test hook: extra bytes the staged kernels' copy barriers wait for (normally 0)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
     const Chunk ch = A.chunks[ci];
     const GT* __restrict__ g = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start;
     float* __restrict__ c = A.c + (int64_t)i * A.Dp + ch.off;
-    uint8_t* __restrict__ wb = reinterpret_cast<uint8_t*>(A.wbits + (int64_t)i * A.Wp) + (ch.off >> 3);
+    uint8_t* __restrict__ wb = reinterpret_cast<uint8_t*>(A.wbits + (int64_t)i * A.Wr) + (ch.off >> 3);
     const uint8_t* __restrict__ sb = reinterpret_cast<const uint8_t*>(A.sbits) + (ch.off >> 3);
     const float* __restrict__ md = A.m + ch.off;
     const float sp = HAS_ERR ? A.wscale_prev[(int64_t)i * A.T + ch.seg] : 0.0f;
@@ -359,9 +362,9 @@ static __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const Ste
 }
 
 // ------------------------------------------------------------------------------------------------
-// K2: server.  One unit = one chunk of one shard.  For every element the n decompressed worker
-// messages are summed in worker order in fp32, divided by n, and the server error is added; the
-// result a is written with its sign byte, and the chunk's sum of a^2 is kept.
+// K2: server.  For every element the n decompressed worker messages are summed in worker order in
+// fp32, divided by n, and the server error is added; the result a is written with its sign byte, and
+// each chunk's sum of a^2 is kept.
 //
 // The ordered sum over the first min(n, 12) workers depends only on their 12 sign bits, so it is read
 // from a 4096-entry shared-memory table built per tensor with exactly those fp32 additions
@@ -374,50 +377,126 @@ static __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const Ste
 
 constexpr int kLutBits = 12;  // workers folded into the server's sum table
 
+struct ServerTables {
+  float ssc[kMaxWorkers];
+  float lut[1 << kLutBits];
+  float4 quad[16 * 32];  // [pattern of workers 12..15][lane]
+  double red[kThreads / 32];
+};
+
+// Rebuild the tables for tensor `seg` (block-wide; every thread calls it).
+__device__ __forceinline__ void build_server_tables(ServerTables& S, const StepArgs& A, int seg) {
+  const int n = A.n, nl = n < kLutBits ? n : kLutBits;
+  __syncthreads();  // everyone is done with the previous tables
+  for (int i = threadIdx.x; i < n; i += kThreads) S.ssc[i] = A.wscale_cur[(int64_t)i * A.T + seg];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    S.lut[0] = __fadd_rn(0.0f, -S.ssc[0]);
+    S.lut[1] = __fadd_rn(0.0f, S.ssc[0]);
+  }
+  __syncthreads();
+  for (int k = 1; k < nl; ++k) {
+    const float sk = S.ssc[k];
+    for (int p = threadIdx.x; p < (1 << k); p += kThreads) {
+      const float old = S.lut[p];
+      S.lut[p] = __fadd_rn(old, -sk);
+      S.lut[p + (1 << k)] = __fadd_rn(old, sk);
+    }
+    __syncthreads();
+  }
+  if (n > kLutBits) {
+    for (int p = threadIdx.x; p < 16 * 32; p += kThreads) {
+      const int pat = p >> 5;
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float sj = kLutBits + j < n ? S.ssc[kLutBits + j] : 0.0f;
+        v[j] = ((pat >> j) & 1) ? sj : -sj;
+      }
+      S.quad[p] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncthreads();
+  }
+}
+
+// Ordered sum of the first min(n, 16) workers' decompressed messages for 8 elements, from their sign
+// bytes b[0..15] (bytes of absent workers are 0).
+__device__ __forceinline__ void server_sum16(const ServerTables& S, int n, const uint32_t (&b)[16], float (&s)[8]) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t w0 = __byte_perm(b[0] | (b[1] << 8), b[2] | (b[3] << 8), 0x5410);
+  const uint32_t w1 = __byte_perm(b[4] | (b[5] << 8), b[6] | (b[7] << 8), 0x5410);
+  const uint64_t t0 = transpose8x8(((uint64_t)w1 << 32) | w0);
+  uint64_t t1 = 0;
+  if (n > 8) {
+    const uint32_t w2 = __byte_perm(b[8] | (b[9] << 8), b[10] | (b[11] << 8), 0x5410);
+    const uint32_t w3 = __byte_perm(b[12] | (b[13] << 8), b[14] | (b[15] << 8), 0x5410);
+    t1 = transpose8x8(((uint64_t)w3 << 32) | w2);
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t hi8 = (uint32_t)(t1 >> (8 * q)) & 0xffu;
+    s[q] = S.lut[((uint32_t)(t0 >> (8 * q)) & 0xffu) | ((hi8 & 0x0fu) << 8)];
+    if (n > kLutBits) {  // workers 12..15, in order
+      const float4 qv = S.quad[(hi8 >> 4) * 32 + lane];
+      s[q] = __fadd_rn(s[q], qv.x);
+      if (n > kLutBits + 1) s[q] = __fadd_rn(s[q], qv.y);
+      if (n > kLutBits + 2) s[q] = __fadd_rn(s[q], qv.z);
+      if (n > kLutBits + 3) s[q] = __fadd_rn(s[q], qv.w);
+    }
+  }
+}
+
+__device__ __forceinline__ void server_add_worker(float (&s)[8], float si, uint32_t byte) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) s[q] = __fadd_rn(s[q], signed_scale(si, byte, q));
+}
+
+// a = sum / n + eps_prev, its sign byte (bits past `cnt` cleared) and the squares of the first cnt.
+template <bool HAS_ERR>
+__device__ __forceinline__ uint32_t server_finish(const StepArgs& A, const float (&s)[8], const float (&ap)[8],
+                                                  float Sp, int cnt, float (&out)[8], unsigned long long& hi,
+                                                  unsigned long long& lo) {
+  uint32_t byte = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float avg = A.pow2 ? __fmul_rn(s[q], A.inv_n) : __fdiv_rn(s[q], A.nf);
+    const float ep = HAS_ERR ? error_of(ap[q], Sp) : 0.0f;
+    out[q] = __fadd_rn(avg, ep);
+    byte |= (out[q] >= 0.0f ? 1u : 0u) << q;
+  }
+  if (cnt >= 8) {
+#pragma unroll
+    for (int q = 0; q < 8; q += 2) add_square2(hi, lo, out[q], out[q + 1]);
+  } else {
+    byte &= (1u << cnt) - 1u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < cnt) add_square2(hi, lo, out[q], 0.0f);
+  }
+  return byte;
+}
+
+__device__ __forceinline__ void store_a(float* a, int64_t e, int cnt, const float (&out)[8]) {
+  if (cnt >= 8) {
+    st8(a + e, out);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < cnt) a[e + q] = out[q];
+  }
+}
+
+// K2, register variant (any n): every thread loads its group's sign bytes and a directly.
 template <bool HAS_ERR>
 __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
-  __shared__ float ssc[kMaxWorkers];
-  __shared__ float lut[1 << kLutBits];
-  __shared__ float4 quad[16 * 32];  // [pattern of workers 12..15][lane]
-  __shared__ double red[kThreads / 32];
+  __shared__ ServerTables S;
   const int n = A.n;
-  const int nl = n < kLutBits ? n : kLutBits;
-  const int lane = threadIdx.x & 31;
-  const int64_t wrow = A.Wp * 4;  // bytes per worker row of sign words
+  const int64_t wrow = A.Wr * 4;  // bytes per worker row of sign words
   int cur_seg = -1;
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
     const Chunk ch = A.chunks[u];
-    if (ch.seg != cur_seg) {  // block-uniform: rebuild the table for this tensor's worker scales
-      __syncthreads();
-      for (int i = threadIdx.x; i < n; i += kThreads) ssc[i] = A.wscale_cur[(int64_t)i * A.T + ch.seg];
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        lut[0] = __fadd_rn(0.0f, -ssc[0]);
-        lut[1] = __fadd_rn(0.0f, ssc[0]);
-      }
-      __syncthreads();
-      for (int k = 1; k < nl; ++k) {
-        const float sk = ssc[k];
-        for (int p = threadIdx.x; p < (1 << k); p += kThreads) {
-          const float old = lut[p];
-          lut[p] = __fadd_rn(old, -sk);
-          lut[p + (1 << k)] = __fadd_rn(old, sk);
-        }
-        __syncthreads();
-      }
-      if (n > kLutBits) {
-        for (int p = threadIdx.x; p < 16 * 32; p += kThreads) {
-          const int pat = p >> 5;
-          float v[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float sj = kLutBits + j < n ? ssc[kLutBits + j] : 0.0f;
-            v[j] = ((pat >> j) & 1) ? sj : -sj;
-          }
-          quad[p] = make_float4(v[0], v[1], v[2], v[3]);
-        }
-        __syncthreads();
-      }
+    if (ch.seg != cur_seg) {  // block-uniform
+      build_server_tables(S, A, ch.seg);
       cur_seg = ch.seg;
     }
     const float Sp = HAS_ERR ? A.sscale_prev[(int64_t)ch.seg * n + ch.shard] : 0.0f;
@@ -429,7 +508,6 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
     for (int gi = threadIdx.x; gi < ng; gi += kThreads) {
       const int64_t e = (int64_t)gi * 8;
       const int cnt = ch.len - gi * 8;  // >= 8 except in a tensor's last group
-      // all sign bytes of this group first (one memory latency for the whole group)
       uint32_t b[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) b[i] = i < n ? (uint32_t)__ldg(wb + (int64_t)i * wrow + gi) : 0u;
@@ -442,61 +520,256 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
           for (int q = 0; q < 8; ++q) ap[q] = q < cnt ? a[e + q] : 0.0f;
         }
       }
-      const uint32_t w0 = __byte_perm(b[0] | (b[1] << 8), b[2] | (b[3] << 8), 0x5410);
-      const uint32_t w1 = __byte_perm(b[4] | (b[5] << 8), b[6] | (b[7] << 8), 0x5410);
-      const uint64_t t0 = transpose8x8(((uint64_t)w1 << 32) | w0);
-      uint64_t t1 = 0;
-      if (nl > 8) {
-        const uint32_t w2 = __byte_perm(b[8] | (b[9] << 8), b[10] | (b[11] << 8), 0x5410);
-        const uint32_t w3 = __byte_perm(b[12] | (b[13] << 8), b[14] | (b[15] << 8), 0x5410);
-        t1 = transpose8x8(((uint64_t)w3 << 32) | w2);
-      }
-      float s[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t hi8 = (uint32_t)(t1 >> (8 * q)) & 0xffu;
-        s[q] = lut[((uint32_t)(t0 >> (8 * q)) & 0xffu) | ((hi8 & 0x0fu) << 8)];
-        if (n > kLutBits) {  // workers 12..15, in order
-          const float4 qv = quad[(hi8 >> 4) * 32 + lane];
-          s[q] = __fadd_rn(s[q], qv.x);
-          if (n > kLutBits + 1) s[q] = __fadd_rn(s[q], qv.y);
-          if (n > kLutBits + 2) s[q] = __fadd_rn(s[q], qv.z);
-          if (n > kLutBits + 3) s[q] = __fadd_rn(s[q], qv.w);
-        }
-      }
-      for (int i = 16; i < n; ++i) {
-        const uint32_t byte = __ldg(wb + (int64_t)i * wrow + gi);
-        const float si = ssc[i];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) s[q] = __fadd_rn(s[q], signed_scale(si, byte, q));
-      }
+      float sum[8];
+      server_sum16(S, n, b, sum);
+      for (int i = 16; i < n; ++i) server_add_worker(sum, S.ssc[i], __ldg(wb + (int64_t)i * wrow + gi));
       float out[8];
-      uint32_t byte = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float avg = A.pow2 ? __fmul_rn(s[q], A.inv_n) : __fdiv_rn(s[q], A.nf);
-        const float ep = HAS_ERR ? error_of(ap[q], Sp) : 0.0f;
-        out[q] = __fadd_rn(avg, ep);
-        byte |= (out[q] >= 0.0f ? 1u : 0u) << q;
-      }
-      if (cnt >= 8) {
-#pragma unroll
-        for (int q = 0; q < 8; q += 2) add_square2(hi, lo, out[q], out[q + 1]);
-        st8(a + e, out);
-      } else {
-        byte &= (1u << cnt) - 1u;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (q < cnt) {
-            a[e + q] = out[q];
-            add_square2(hi, lo, out[q], 0.0f);
-          }
-        }
-      }
+      const uint32_t byte = server_finish<HAS_ERR>(A, sum, ap, Sp, cnt, out, hi, lo);
+      store_a(a, e, cnt, out);
       sb[gi] = (uint8_t)byte;
     }
-    const double tot = block_sum<kThreads>(square_total(hi, lo), red);
+    const double tot = block_sum<kThreads>(square_total(hi, lo), S.red);
     if (threadIdx.x == 0) A.spart[u] = tot;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// K2, staged variant (n <= kStageMaxWorkers), warp-specialised.  A ring of kStages shared-memory
+// stages each holds one tile of kTile elements of a and the n workers' sign bytes for it.  One
+// producer warp keeps the ring full with bulk asynchronous copies (cp.async.bulk; completion counted
+// on a "full" mbarrier per stage); kConsumerWarps consumer warps compute from shared memory and
+// release a stage by arriving on its "empty" mbarrier.  Consumers synchronise with each other only
+// through a named barrier, when the tables are rebuilt and at the end of each chunk.
+//
+// Every wait is bounded (kWaitCycles, about one second).  A wait that runs out sets status bit 2 and
+// the block-wide abort flag; from then on every thread skips its waits and its work but keeps
+// stepping through the same sequence, so that the named barriers still meet, and the producer drains
+// its own copies still in flight (bounded again) before the block ends.
+
+constexpr int kTile = 4096;                 // elements per tile (two groups per consumer thread)
+constexpr int kStages = 3;
+constexpr int kStageMaxWorkers = 32;
+constexpr int kRowBytes = kTile / 8 + 32;   // a 16-byte aligned window around the tile's sign bytes
+constexpr int kConsumerWarps = kThreads / 32;
+constexpr int kStagedThreads = kThreads + 32;      // consumers + one producer warp
+constexpr long long kWaitCycles = 2000000000LL;    // ~1 s at the maximum SM clock
+
+__host__ __device__ constexpr size_t server_stage_bytes(int n) { return (size_t)kTile * 4 + (size_t)n * kRowBytes; }
+__host__ __device__ constexpr size_t server_dyn_smem(int n) { return kStages * server_stage_bytes(n) + 2 * kStages * 8; }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// bounded wait: false if the phase did not complete within kWaitCycles
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory"); }
+
+struct TileCursor {  // position in this block's sequence of (unit, tile)
+  int u, t;
+};
+
+__device__ __forceinline__ int tiles_of(const Chunk& ch) { return (ch.len + kTile - 1) / kTile; }
+
+// table rebuild among the consumer threads only (same arithmetic as build_server_tables)
+__device__ __forceinline__ void build_server_tables_consumers(ServerTables& S, const StepArgs& A, int seg) {
+  const int n = A.n, nl = n < kLutBits ? n : kLutBits;
+  consumers_sync();
+  for (int i = threadIdx.x; i < n; i += kThreads) S.ssc[i] = A.wscale_cur[(int64_t)i * A.T + seg];
+  consumers_sync();
+  if (threadIdx.x == 0) {
+    S.lut[0] = __fadd_rn(0.0f, -S.ssc[0]);
+    S.lut[1] = __fadd_rn(0.0f, S.ssc[0]);
+  }
+  consumers_sync();
+  for (int k = 1; k < nl; ++k) {
+    const float sk = S.ssc[k];
+    for (int p = threadIdx.x; p < (1 << k); p += kThreads) {
+      const float old = S.lut[p];
+      S.lut[p] = __fadd_rn(old, -sk);
+      S.lut[p + (1 << k)] = __fadd_rn(old, sk);
+    }
+    consumers_sync();
+  }
+  if (n > kLutBits) {
+    for (int p = threadIdx.x; p < 16 * 32; p += kThreads) {
+      const int pat = p >> 5;
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float sj = kLutBits + j < n ? S.ssc[kLutBits + j] : 0.0f;
+        v[j] = ((pat >> j) & 1) ? sj : -sj;
+      }
+      S.quad[p] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    consumers_sync();
+  }
+}
+
+template <bool HAS_ERR>
+__global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs A) {
+  __shared__ ServerTables S;
+  __shared__ volatile int abort_flag;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  const int n = A.n;
+  const size_t stage_bytes = server_stage_bytes(n);
+  uint64_t* full = reinterpret_cast<uint64_t*>(dyn + kStages * stage_bytes);
+  uint64_t* empty = full + kStages;
+  const uint64_t wrow = (uint64_t)A.Wr * 4;  // a multiple of 16: one window offset for all workers
+  const uint8_t* wbase = reinterpret_cast<const uint8_t*>(A.wbits);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  auto advance = [&](TileCursor& c) {
+    if (++c.t >= tiles_of(A.chunks[c.u])) {
+      c.t = 0;
+      c.u += gridDim.x;
+    }
+  };
+
+  if (threadIdx.x >= kThreads) {
+    // ---------------- producer warp (one elected lane issues the copies)
+    if (threadIdx.x != kThreads) return;
+    TileCursor c{(int)blockIdx.x, 0};
+    int j = 0;
+    for (; c.u < A.n_chunks; ++j, advance(c)) {
+      const int st = j % kStages;
+      if (j >= kStages && !abort_flag && !mbar_wait(&empty[st], (uint32_t)((j / kStages - 1) & 1))) {
+        atomicOr(A.status, 2u);
+        abort_flag = 1;
+      }
+      if (abort_flag) break;
+      const Chunk ch = A.chunks[c.u];
+      const int e0 = c.t * kTile;
+      const int tlen = min(kTile, ch.len - e0);
+      unsigned char* sbase = dyn + (size_t)st * stage_bytes;
+      const uint32_t abytes = (uint32_t)(((tlen + 31) / 32) * 32 * 4);  // the padded layout keeps this in bounds
+      const uint64_t byte0 = (uint64_t)(ch.off + e0) >> 3;
+      const uint32_t nb = (uint32_t)((tlen + 7) / 8);
+      // every worker's sign bytes for the tile, widened to the same 16-byte aligned window
+      const uint64_t wlo = byte0 & ~(uint64_t)15;
+      const uint32_t wlen = (uint32_t)(((byte0 & 15) + nb + 15) & ~(uint64_t)15);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_expect_tx(&full[st], (HAS_ERR ? abytes : 0u) + (uint32_t)n * wlen + A.stall_tx);
+      if (HAS_ERR) bulk_copy_g2s(sbase, A.a + ch.off + e0, abytes, &full[st]);
+      for (int i = 0; i < n; ++i)
+        bulk_copy_g2s(sbase + (size_t)kTile * 4 + (size_t)i * kRowBytes, wbase + (uint64_t)i * wrow + wlo, wlen,
+                      &full[st]);
+    }
+    if (abort_flag) {
+      // drain this block's copies still in flight before the shared memory is released; a second
+      // expired wait ends the drain (the copies behind it are as stuck as the first)
+      for (int q = j - kStages; q < j; ++q)
+        if (q >= 0 && !mbar_wait(&full[q % kStages], (uint32_t)((q / kStages) & 1))) break;
+    }
+    return;
+  }
+
+  // ---------------- consumer warps
+  const int lane = threadIdx.x & 31;
+  TileCursor cons{(int)blockIdx.x, 0};
+  int k = 0;
+  int cur_seg = -1;
+  unsigned long long hi = 0, lo = 0;
+  while (cons.u < A.n_chunks) {
+    const Chunk ch = A.chunks[cons.u];
+    if (cons.t == 0 && ch.seg != cur_seg) {
+      build_server_tables_consumers(S, A, ch.seg);
+      cur_seg = ch.seg;
+    }
+    const int st = k % kStages;
+    if (!abort_flag && !mbar_wait(&full[st], (uint32_t)((k / kStages) & 1))) {
+      atomicOr(A.status, 2u);
+      abort_flag = 1;
+    }
+    if (!abort_flag) {
+      const unsigned char* sbase = dyn + (size_t)st * stage_bytes;
+      const float* as = reinterpret_cast<const float*>(sbase);
+      const unsigned char* bs = sbase + (size_t)kTile * 4;
+      const int e0 = cons.t * kTile;
+      const int tlen = min(kTile, ch.len - e0);
+      const int boff = (int)(((uint64_t)(ch.off + e0) >> 3) & 15);  // the tile's first byte in each window
+      const float Sp = HAS_ERR ? A.sscale_prev[(int64_t)ch.seg * n + ch.shard] : 0.0f;
+#pragma unroll
+      for (int h = 0; h < kTile / 8 / kThreads; ++h) {
+        const int gl = threadIdx.x + h * kThreads;
+        if (gl * 8 < tlen) {
+          const int cnt = tlen - gl * 8;
+          uint32_t b[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) b[i] = i < n ? (uint32_t)bs[i * kRowBytes + boff + gl] : 0u;
+          float ap[8];
+          if (HAS_ERR) {
+            const float4 v0 = *reinterpret_cast<const float4*>(as + gl * 8);
+            const float4 v1 = *reinterpret_cast<const float4*>(as + gl * 8 + 4);
+            ap[0] = v0.x; ap[1] = v0.y; ap[2] = v0.z; ap[3] = v0.w;
+            ap[4] = v1.x; ap[5] = v1.y; ap[6] = v1.z; ap[7] = v1.w;
+          }
+          float sum[8];
+          server_sum16(S, n, b, sum);
+          for (int i = 16; i < n; ++i) server_add_worker(sum, S.ssc[i], bs[i * kRowBytes + boff + gl]);
+          float out[8];
+          const uint32_t byte = server_finish<HAS_ERR>(A, sum, ap, Sp, cnt, out, hi, lo);
+          const int64_t e = (int64_t)ch.off + e0 + gl * 8;
+          store_a(A.a, e, cnt, out);
+          reinterpret_cast<uint8_t*>(A.sbits)[e >> 3] = (uint8_t)byte;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with stage st
+    }
+    ++k;
+    const bool last_tile = cons.t == tiles_of(ch) - 1;
+    const int u_done = cons.u;
+    advance(cons);
+    if (last_tile) {  // chunk total among the consumers (fixed order)
+      double v = warp_sum(square_total(hi, lo));
+      if (lane == 0) S.red[threadIdx.x >> 5] = v;
+      consumers_sync();
+      if (threadIdx.x < 32) {
+        double r = lane < kConsumerWarps ? S.red[lane] : 0.0;
+        r = warp_sum(r);
+        if (threadIdx.x == 0 && !abort_flag) A.spart[u_done] = r;
+      }
+      consumers_sync();
+      hi = lo = 0;
+    }
   }
 }
 

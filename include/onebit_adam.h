@@ -141,7 +141,9 @@ onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* con
 /* Release the handle (synchronises its device; frees library allocations only). */
 onebit_status_t onebit_adam_free(onebit_adam_t* h);
 
-/* Synchronise `stream` and report the sticky device flag: ONEBIT_OK or ONEBIT_ERR_NONFINITE. */
+/* Synchronise `stream` and report the sticky device flags: ONEBIT_OK, ONEBIT_ERR_NONFINITE (a scale
+ * was NaN or infinite), or ONEBIT_ERR_CUDA when a kernel gave up waiting (about one second) for its
+ * own asynchronous copies and stopped early (onebit_adam_last_error() says so). */
 onebit_status_t onebit_adam_get_status(onebit_adam_t* h, onebit_stream_t stream);
 /* Clear the sticky device flag (enqueued on `stream`). */
 onebit_status_t onebit_adam_clear_status(onebit_adam_t* h, onebit_stream_t stream);
@@ -175,6 +177,14 @@ onebit_status_t onebit_adam_set_timing(onebit_adam_t* h, int32_t enable);
 onebit_status_t onebit_adam_kernel_times(onebit_adam_t* h, double* ms, int64_t* launches);
 /* Kernel launches enqueued by this handle since init. */
 onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launches);
+
+/* Failure-detection test hook.  ONEBIT_FAULT_STALL_COPIES makes the next steps' shared-memory staged
+ * kernels wait for `value` bytes (1..2^20) that no copy delivers, so that their bounded waits run out
+ * (about one second): the kernel stops early, the sticky flag is set and onebit_adam_get_status()
+ * returns ONEBIT_ERR_CUDA, with the CUDA context still usable.  The state of that step is not
+ * meaningful.  ONEBIT_FAULT_NONE turns it off. */
+typedef enum { ONEBIT_FAULT_NONE = 0, ONEBIT_FAULT_STALL_COPIES = 1 } onebit_fault_t;
+onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, int64_t value);
 
 /* The work chunks the kernels use for a config (host only, no GPU needed): up to `cap` rows of
  * five int64 {tensor, shard, start element within the tensor, length, padded state offset}.

@@ -33,6 +33,7 @@ def test_tiny_schedule():
 ODD = [
     ([1], 1), ([31], 2), ([33], 3), ([32 * 4 - 1], 4), ([32 * 4 + 1], 4), ([(1 << 20) + 7], 8),
     ([1, 5, 32, 33], 3), ([5, 0, 33, 200], 4), ([65536 * 2 + 100, 7], 16), ([1000], 16),
+    ([5000, 37], 20), ([3000, 2049], 33),
 ]
 
 
@@ -214,6 +215,25 @@ def test_phase_errors_and_status():
     p.gpu.clear_status()
     assert p.gpu.get_status() == ob.OK
     p.close()
+
+
+def test_stalled_copies_are_reported_not_hung():
+    """Failure detection without a GPU fault: the staged server kernel is made to wait for bytes
+    that never arrive; its bounded wait runs out, the status reports it, and the context still
+    works (a later step on a fresh handle is correct)."""
+    w = _tiny(numel=(20_000,), n_workers=4, warmup_steps=1, compress_steps=2, seed=81)
+    p = Pair(w)
+    p.warmup(check=False)
+    p.freeze(check=False)
+    p.gpu.set_fault_injection(ob.FAULT_STALL_COPIES, 64)
+    p.gpu.compress_step([t.cuda() for t in p.src.grads(5)])
+    assert p.gpu.get_status() == ob.ERR_CUDA
+    assert "timed out" in ob.lib().onebit_adam_last_error(p.gpu.h).decode()
+    p.gpu.set_fault_injection(ob.FAULT_NONE)
+    p.close()
+    q = Pair(w)  # the CUDA context is still usable: a full schedule matches the oracle
+    q.run()
+    q.close()
 
 
 def test_timing_and_launch_counts():
