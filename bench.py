@@ -340,7 +340,7 @@ def main():
             host.append(hb)
         h2d = sum(t.numel() * t.element_size() for t in host)
         out = torch.empty(w.n_tensors * w.n_workers, dtype=torch.float32).pin_memory()
-        e2e_steps = max(1, min(args.steps, 5))
+        e2e_steps = max(2, min(args.steps, 10))
         opt.compress_step_host(host)  # first call allocates the library's staging buffer
         torch.cuda.synchronize()
         barrier()

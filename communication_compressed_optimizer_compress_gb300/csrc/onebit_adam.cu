@@ -24,6 +24,8 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int kPtrRing = 4;
+constexpr int kCopyStreams = 4;               // host-gradient copies run on this many internal streams
+constexpr size_t kCopyPiece = size_t(64) << 20;  // and are cut into pieces of at most this size
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t round32(int64_t v) { return (v + 31) / 32 * 32; }
@@ -173,8 +175,14 @@ struct onebit_adam {
   // gradient pointer table ring
   std::vector<std::vector<const void*>> ring;
   int ring_next = 0;
-  // host-gradient staging
-  uint8_t* staging = nullptr;
+  // host-gradient staging: two device buffers used alternately, so that one step's copies can run
+  // while the previous step's kernels still read the other buffer
+  uint8_t* staging[2] = {nullptr, nullptr};
+  int stage_next = 0;
+  cudaStream_t copy_st[kCopyStreams] = {};
+  cudaEvent_t ev_copied[kCopyStreams] = {};
+  cudaEvent_t ev_free[2] = {};  // recorded after the last step that read staging[i]
+  bool ev_free_recorded[2] = {false, false};
   // timing
   bool timing = false;
   std::vector<TimedLaunch> timed;
@@ -474,31 +482,66 @@ onebit_status_t export_m(onebit_adam* h, float* dst, cudaStream_t st) {
   return run_export(h, kExportBits, nullptr, h->at<uint32_t>(h->lay.sbits), last_sscale(h), h->plan.n, 1, dst, st);
 }
 
-onebit_status_t stage_copy(onebit_adam* h, const void* const* host_grads, cudaStream_t st, std::vector<const void*>* dev) {
+// Copy the host gradients of one step into a staging buffer; returns the device pointers and the
+// buffer index (to be marked free once the step that reads it is enqueued: release_stage()).
+onebit_status_t stage_copy(onebit_adam* h, const void* const* host_grads, cudaStream_t st,
+                           std::vector<const void*>* dev, int* idx_out) {
   const int n = h->plan.n, T = h->plan.T;
   const size_t gb = h->cfg.grad_dtype == ONEBIT_F32 ? 4 : 2;
   if (!host_grads) return ONEBIT_ERR_INVALID_ARG;
-  if (!h->staging) {
+  for (int i = 0; i < n; ++i)
+    for (int k = 0; k < T; ++k)
+      if (h->plan.numel[k] > 0 && !host_grads[(size_t)i * T + k]) return ONEBIT_ERR_INVALID_ARG;
+  if (!h->staging[0]) {
     size_t bytes = 0;
     for (int i = 0; i < n; ++i)
       for (int k = 0; k < T; ++k) bytes += align_up(h->plan.numel[k] * gb, kAlign);
-    if (cudaMalloc(&h->staging, std::max<size_t>(bytes, 1)) != cudaSuccess) {
-      cudaGetLastError();
-      h->staging = nullptr;
-      return ONEBIT_ERR_NOMEM;
+    for (int b = 0; b < 2; ++b) {
+      if (cudaMalloc(&h->staging[b], std::max<size_t>(bytes, 1)) != cudaSuccess) {
+        cudaGetLastError();
+        if (b == 1) cudaFree(h->staging[0]);
+        h->staging[0] = h->staging[1] = nullptr;
+        return ONEBIT_ERR_NOMEM;
+      }
     }
+    for (int c = 0; c < kCopyStreams; ++c) {
+      ONEBIT_CUDA(h, cudaStreamCreateWithFlags(&h->copy_st[c], cudaStreamNonBlocking));
+      ONEBIT_CUDA(h, cudaEventCreateWithFlags(&h->ev_copied[c], cudaEventDisableTiming));
+    }
+    for (int b = 0; b < 2; ++b) ONEBIT_CUDA(h, cudaEventCreateWithFlags(&h->ev_free[b], cudaEventDisableTiming));
   }
+  const int idx = h->stage_next;
+  h->stage_next ^= 1;
+  uint8_t* base = h->staging[idx];
+  for (int c = 0; c < kCopyStreams; ++c)
+    if (h->ev_free_recorded[idx]) ONEBIT_CUDA(h, cudaStreamWaitEvent(h->copy_st[c], h->ev_free[idx], 0));
   dev->resize((size_t)n * T);
   size_t off = 0;
+  int r = 0;
   for (int i = 0; i < n; ++i)
     for (int k = 0; k < T; ++k) {
       const size_t bytes = h->plan.numel[k] * gb;
       const size_t q = (size_t)i * T + k;
-      if (bytes && !host_grads[q]) return ONEBIT_ERR_INVALID_ARG;
-      (*dev)[q] = h->staging + off;
-      if (bytes) ONEBIT_CUDA(h, cudaMemcpyAsync(h->staging + off, host_grads[q], bytes, cudaMemcpyHostToDevice, st));
+      (*dev)[q] = base + off;
+      const uint8_t* src = static_cast<const uint8_t*>(host_grads[q]);
+      for (size_t p = 0; p < bytes; p += kCopyPiece, ++r) {
+        const size_t len = std::min(kCopyPiece, bytes - p);
+        ONEBIT_CUDA(h, cudaMemcpyAsync(base + off + p, src + p, len, cudaMemcpyHostToDevice,
+                                       h->copy_st[r % kCopyStreams]));
+      }
       off += align_up(bytes, kAlign);
     }
+  for (int c = 0; c < kCopyStreams; ++c) {
+    ONEBIT_CUDA(h, cudaEventRecord(h->ev_copied[c], h->copy_st[c]));
+    ONEBIT_CUDA(h, cudaStreamWaitEvent(st, h->ev_copied[c], 0));
+  }
+  *idx_out = idx;
+  return ONEBIT_OK;
+}
+
+onebit_status_t release_stage(onebit_adam* h, int idx, cudaStream_t st) {
+  ONEBIT_CUDA(h, cudaEventRecord(h->ev_free[idx], st));
+  h->ev_free_recorded[idx] = true;
   return ONEBIT_OK;
 }
 
@@ -630,7 +673,14 @@ onebit_status_t onebit_adam_free(onebit_adam_t* h) {
   }
   for (auto e : h->event_pool) cudaEventDestroy(e);
   if (h->ws_owned && h->ws) cudaFree(h->ws);
-  if (h->staging) cudaFree(h->staging);
+  for (int b = 0; b < 2; ++b) {
+    if (h->staging[b]) cudaFree(h->staging[b]);
+    if (h->ev_free[b]) cudaEventDestroy(h->ev_free[b]);
+  }
+  for (int c = 0; c < kCopyStreams; ++c) {
+    if (h->copy_st[c]) cudaStreamDestroy(h->copy_st[c]);
+    if (h->ev_copied[c]) cudaEventDestroy(h->ev_copied[c]);
+  }
   delete h;
   return ONEBIT_OK;
 }
@@ -652,9 +702,12 @@ onebit_status_t onebit_adam_warmup_step_host(onebit_adam_t* h, const void* const
   if (h->phase != ONEBIT_PHASE_WARMUP || h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
   DeviceGuard g(h->device);
   std::vector<const void*> dev;
-  onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev);
+  int idx = 0;
+  onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev, &idx);
   if (s) return s;
-  return do_warmup(h, dev.data(), as_stream(stream));
+  s = do_warmup(h, dev.data(), as_stream(stream));
+  const onebit_status_t r = release_stage(h, idx, as_stream(stream));
+  return s ? s : r;
 }
 
 onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream) {
@@ -662,9 +715,12 @@ onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* con
   if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
   DeviceGuard g(h->device);
   std::vector<const void*> dev;
-  onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev);
+  int idx = 0;
+  onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev, &idx);
   if (s) return s;
-  return do_compress(h, dev.data(), as_stream(stream));
+  s = do_compress(h, dev.data(), as_stream(stream));
+  const onebit_status_t r = release_stage(h, idx, as_stream(stream));
+  return s ? s : r;
 }
 
 onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t stream) {

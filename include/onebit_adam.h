@@ -132,9 +132,13 @@ onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t st
 onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream);
 
 /* The same two steps with HOST gradient buffers ([n*T] host pointers, pinned or pageable): the
- * library copies them into a device staging area it owns (allocated on first use, n*D*grad bytes),
- * with cudaMemcpyAsync on `stream`, then runs the step.  Pageable sources are copied before the
- * call returns; pinned sources must stay valid until the copy completes on `stream`. */
+ * library copies them into one of two device staging buffers it owns (allocated on first use,
+ * 2 x n*D*grad bytes, used alternately) on internal copy streams, and `stream` waits for those
+ * copies before the step's kernels.  The copies wait only until their staging buffer is free again,
+ * not for earlier work on `stream`, so that one step's copies overlap the previous step's kernels:
+ * the host buffers must already hold this step's gradients when the call is made.  Pageable sources
+ * are copied before the call returns; pinned sources must stay valid until `stream` has passed this
+ * step. */
 onebit_status_t onebit_adam_warmup_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream);
 onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream);
 
