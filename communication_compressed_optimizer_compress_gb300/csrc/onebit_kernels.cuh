@@ -43,6 +43,7 @@ constexpr int kThreads = 256;          // threads per CTA of the streaming kerne
 constexpr int kChunk = 65536;          // maximum elements per work chunk (multiple of 256)
 constexpr int kMaxWorkers = 256;
 constexpr int kScaleThreads = 256;     // threads per CTA of the scale kernels
+constexpr int kWorkerUnroll = 3;       // 8-element groups whose loads a worker-kernel thread issues together
 
 struct Chunk {
   int64_t off;    // element offset in the padded state layout (multiple of 32)
@@ -298,14 +299,14 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
 
     const int ng = ch.len >> 3;
     int gi = threadIdx.x;
-    for (; gi + kThreads < ng; gi += 2 * kThreads) {
-      In r0, r1;
-      load(r0, gi);
-      load(r1, gi + kThreads);
-      work(r0, gi);
-      work(r1, gi + kThreads);
+    for (; gi + (kWorkerUnroll - 1) * kThreads < ng; gi += kWorkerUnroll * kThreads) {
+      In r[kWorkerUnroll];  // all loads of kWorkerUnroll groups in flight, then the math
+#pragma unroll
+      for (int j = 0; j < kWorkerUnroll; ++j) load(r[j], gi + j * kThreads);
+#pragma unroll
+      for (int j = 0; j < kWorkerUnroll; ++j) work(r[j], gi + j * kThreads);
     }
-    if (gi < ng) {
+    for (; gi < ng; gi += kThreads) {
       In r0;
       load(r0, gi);
       work(r0, gi);
@@ -421,23 +422,24 @@ __device__ __forceinline__ void build_server_tables(ServerTables& S, const StepA
 
 // Ordered sum of the first min(n, 16) workers' decompressed messages for 8 elements, from their sign
 // bytes b[0..15] (bytes of absent workers are 0).
+__device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);  // b0 | b1<<8 | ...
+}
+
 __device__ __forceinline__ void server_sum16(const ServerTables& S, int n, const uint32_t (&b)[16], float (&s)[8]) {
   const int lane = threadIdx.x & 31;
-  const uint32_t w0 = __byte_perm(b[0] | (b[1] << 8), b[2] | (b[3] << 8), 0x5410);
-  const uint32_t w1 = __byte_perm(b[4] | (b[5] << 8), b[6] | (b[7] << 8), 0x5410);
-  const uint64_t t0 = transpose8x8(((uint64_t)w1 << 32) | w0);
+  const uint64_t t0 = transpose8x8(((uint64_t)pack4(b[4], b[5], b[6], b[7]) << 32) | pack4(b[0], b[1], b[2], b[3]));
   uint64_t t1 = 0;
-  if (n > 8) {
-    const uint32_t w2 = __byte_perm(b[8] | (b[9] << 8), b[10] | (b[11] << 8), 0x5410);
-    const uint32_t w3 = __byte_perm(b[12] | (b[13] << 8), b[14] | (b[15] << 8), 0x5410);
-    t1 = transpose8x8(((uint64_t)w3 << 32) | w2);
-  }
+  if (n > 8) t1 = transpose8x8(((uint64_t)pack4(b[12], b[13], b[14], b[15]) << 32) | pack4(b[8], b[9], b[10], b[11]));
+  const uint32_t t0w[2] = {(uint32_t)t0, (uint32_t)(t0 >> 32)};
+  const uint32_t t1w[2] = {(uint32_t)t1, (uint32_t)(t1 >> 32)};
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const uint32_t hi8 = (uint32_t)(t1 >> (8 * q)) & 0xffu;
-    s[q] = S.lut[((uint32_t)(t0 >> (8 * q)) & 0xffu) | ((hi8 & 0x0fu) << 8)];
+    // bits 0..7: workers 0..7 of element q; bits 8..15: workers 8..15
+    const uint32_t x = __byte_perm(t0w[q >> 2], t1w[q >> 2], (q & 3) | (((q & 3) + 4) << 4));
+    s[q] = S.lut[x & 0x0fffu];
     if (n > kLutBits) {  // workers 12..15, in order
-      const float4 qv = S.quad[(hi8 >> 4) * 32 + lane];
+      const float4 qv = S.quad[((x >> 12) & 0x0fu) * 32 + lane];
       s[q] = __fadd_rn(s[q], qv.x);
       if (n > kLutBits + 1) s[q] = __fadd_rn(s[q], qv.y);
       if (n > kLutBits + 2) s[q] = __fadd_rn(s[q], qv.z);
