@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
             "onebit_adam_launch_count": [vp, ctypes.POINTER(i64)],
             "onebit_adam_plan_chunks": [cfgp, ctypes.POINTER(i64), i64, ctypes.POINTER(i64)],
             "onebit_adam_set_fault_injection": [vp, i32, i64],
+            "onebit_adam_set_variance_monitor": [vp, i32],
+            "onebit_adam_variance_norm": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -264,6 +266,36 @@ class OneBitAdam:
         cnt = (ctypes.c_int64 * NUM_KERNELS)()
         _check(lib().onebit_adam_kernel_times(self.h, ms, cnt), "onebit_adam_kernel_times", self.h)
         return {KERNEL_NAMES[k]: (ms[k], cnt[k]) for k in range(NUM_KERNELS)}
+
+    def set_variance_monitor(self, enable: bool):
+        _check(lib().onebit_adam_set_variance_monitor(self.h, int(bool(enable))), "onebit_adam_set_variance_monitor")
+
+    def variance_norm(self):
+        """(||v_t||_2, t) of the last monitored warm-up step (waits for it)."""
+        v, t = ctypes.c_double(), ctypes.c_int64()
+        _check(lib().onebit_adam_variance_norm(self.h, ctypes.byref(v), ctypes.byref(t)), "onebit_adam_variance_norm",
+               self.h)
+        return v.value, t.value
+
+    def warmup_until_stable(self, grads_fn, tol: float, max_steps: int | None = None, stream=None):
+        """Warm-up steps until the variance norm's relative change per step falls to `tol` or below
+        (|n_t - n_{t-1}| <= tol * n_{t-1}), or until the configured T_w; then freeze the variance.
+        grads_fn(t) returns the gradients of warm-up step t (0-based).  Returns the steps taken."""
+        self.set_variance_monitor(True)
+        t0, _ = self.get_step()
+        limit = int(self.cfg.warmup_steps) if max_steps is None else min(int(max_steps), int(self.cfg.warmup_steps))
+        prev = None
+        taken = 0
+        while t0 + taken < limit:
+            self.warmup_step(grads_fn(t0 + taken), stream)
+            taken += 1
+            cur, _ = self.variance_norm()
+            if prev is not None and abs(cur - prev) <= tol * prev:
+                break
+            prev = cur
+        self.set_variance_monitor(False)
+        self.freeze_variance(stream)
+        return taken
 
     def set_fault_injection(self, kind: int, value: int = 0):
         _check(lib().onebit_adam_set_fault_injection(self.h, int(kind), int(value)),

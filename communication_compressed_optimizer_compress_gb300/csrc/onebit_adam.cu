@@ -191,6 +191,11 @@ struct onebit_adam {
   std::unordered_map<const void*, int> occupancy;
   bool smem_configured[2] = {false, false};
   uint32_t stall_tx = 0;  // fault injection (see onebit_adam_set_fault_injection)
+  // variance-norm monitor (warm-up)
+  bool vmon = false;
+  double* vnorm_host = nullptr;  // pinned
+  cudaEvent_t ev_vnorm = nullptr;
+  int64_t vnorm_step = 0;
   std::string last_error;
 
   template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
@@ -346,13 +351,18 @@ onebit_status_t bind_grads(onebit_adam* h, const void* const* grads, cudaStream_
   return ONEBIT_OK;
 }
 
-template <typename GT>
-onebit_status_t run_warmup(onebit_adam* h, StepArgs A, bool vec, cudaStream_t st) {
+template <typename GT, bool MON>
+onebit_status_t run_warmup_m(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
   const int C = A.n_chunks;
   const bool bc = h->cfg.bias_correction != 0;
   auto pick = [&](auto kern) { return launch(h, ONEBIT_K_WARMUP, kern, grid_for(h, (const void*)kern, kThreads, C), kThreads, st, A); };
-  if (bc) return vec ? pick(k_warmup<GT, true, true>) : pick(k_warmup<GT, true, false>);
-  return vec ? pick(k_warmup<GT, false, true>) : pick(k_warmup<GT, false, false>);
+  if (bc) return vec ? pick(k_warmup<GT, true, true, MON>) : pick(k_warmup<GT, true, false, MON>);
+  return vec ? pick(k_warmup<GT, false, true, MON>) : pick(k_warmup<GT, false, false, MON>);
+}
+
+template <typename GT>
+onebit_status_t run_warmup(onebit_adam* h, StepArgs A, bool vec, cudaStream_t st) {
+  return h->vmon ? run_warmup_m<GT, true>(h, A, vec, st) : run_warmup_m<GT, false>(h, A, vec, st);
 }
 
 template <typename GT, bool DM, bool HE>
@@ -416,6 +426,16 @@ onebit_status_t do_warmup(onebit_adam* h, const void* const* grads, cudaStream_t
   }
   if (s) return s;
   h->t = t;
+  if (h->vmon) {  // ||v_t|| from the chunk partials, then to the pinned host slot
+    double* slot = reinterpret_cast<double*>(h->ws + h->lay.status + 64);
+    k_variance_norm<<<1, kScaleThreads, 0, st>>>(h->at<double>(h->lay.spart), A.n_chunks, slot);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(h, e, "variance norm launch");
+    ++h->launches;
+    ONEBIT_CUDA(h, cudaMemcpyAsync(h->vnorm_host, slot, sizeof(double), cudaMemcpyDeviceToHost, st));
+    ONEBIT_CUDA(h, cudaEventRecord(h->ev_vnorm, st));
+    h->vnorm_step = t;
+  }
   return ONEBIT_OK;
 }
 
@@ -673,6 +693,8 @@ onebit_status_t onebit_adam_free(onebit_adam_t* h) {
   }
   for (auto e : h->event_pool) cudaEventDestroy(e);
   if (h->ws_owned && h->ws) cudaFree(h->ws);
+  if (h->vnorm_host) cudaFreeHost(h->vnorm_host);
+  if (h->ev_vnorm) cudaEventDestroy(h->ev_vnorm);
   for (int b = 0; b < 2; ++b) {
     if (h->staging[b]) cudaFree(h->staging[b]);
     if (h->ev_free[b]) cudaEventDestroy(h->ev_free[b]);
@@ -941,6 +963,32 @@ onebit_status_t onebit_adam_kernel_times(onebit_adam_t* h, double* ms, int64_t* 
   }
   h->timed.clear();
   return rc;
+}
+
+onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enable) {
+  if (!h) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  if (enable && !h->vnorm_host) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&h->vnorm_host), sizeof(double), cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      h->vnorm_host = nullptr;
+      return ONEBIT_ERR_NOMEM;
+    }
+    *h->vnorm_host = 0.0;
+    ONEBIT_CUDA(h, cudaEventCreateWithFlags(&h->ev_vnorm, cudaEventDisableTiming));
+  }
+  h->vmon = enable != 0;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_variance_norm(onebit_adam_t* h, double* norm, int64_t* step) {
+  if (!h || !norm || !step) return ONEBIT_ERR_INVALID_ARG;
+  if (h->vnorm_step == 0) return ONEBIT_ERR_PHASE;  // no monitored warm-up step yet
+  DeviceGuard g(h->device);
+  ONEBIT_CUDA(h, cudaEventSynchronize(h->ev_vnorm));
+  *norm = *h->vnorm_host;
+  *step = h->vnorm_step;
+  return ONEBIT_OK;
 }
 
 onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, int64_t value) {

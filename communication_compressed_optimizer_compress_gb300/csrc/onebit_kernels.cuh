@@ -865,11 +865,15 @@ template <> struct RawGrad<__nv_bfloat16> {
   }
 };
 
-template <typename GT, bool BC, bool VEC>
+// With MON the kernel also writes each chunk's exact sum of the new v^2 to A.spart (the "fused
+// variance norm" monitor; k_variance_norm reduces it).
+template <typename GT, bool BC, bool VEC, bool MON>
 __global__ void __launch_bounds__(kThreads) k_warmup(const StepArgs A) {
   constexpr int B = sizeof(GT) == 4 ? 4 : 8;
   __shared__ const GT* gsm[kMaxWorkers];
+  __shared__ double red[kThreads / 32];
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
+    unsigned long long vhi = 0, vlo = 0;
     const Chunk ch = A.chunks[u];
     __syncthreads();
     for (int i = threadIdx.x; i < A.n; i += kThreads)
@@ -931,6 +935,10 @@ __global__ void __launch_bounds__(kThreads) k_warmup(const StepArgs A) {
         const float vh = BC ? __fdiv_rn(vv[q], A.bc2) : vv[q];
         xv[q] = __fsub_rn(xv[q], __fmul_rn(A.lr, __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), A.eps))));
       }
+      if (MON) {
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) add_square2(vhi, vlo, q < cnt ? vv[q] : 0.0f, q + 1 < cnt ? vv[q + 1] : 0.0f);
+      }
       if (cnt == 8) {
         st8(m + e, mv);
         st8(v + e, vv);
@@ -950,7 +958,20 @@ __global__ void __launch_bounds__(kThreads) k_warmup(const StepArgs A) {
           if (q < cnt) x[e + q] = xv[q];
       }
     }
+    if (MON) {
+      const double tot = block_sum<kThreads>(square_total(vhi, vlo), red);
+      if (threadIdx.x == 0) A.spart[u] = tot;
+    }
   }
+}
+
+// ||v||_2 after a monitored warm-up step: one CTA, fixed-order sum of the chunk partials.
+static __global__ void __launch_bounds__(kScaleThreads) k_variance_norm(const double* part, int n_chunks, double* out) {
+  __shared__ double red[kScaleThreads / 32];
+  double acc = 0.0;
+  for (int c = threadIdx.x; c < n_chunks; c += kScaleThreads) acc += __ldcg(part + c);
+  const double tot = block_sum<kScaleThreads>(acc, red);
+  if (threadIdx.x == 0) *out = sqrt(tot);
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -182,6 +182,15 @@ onebit_status_t onebit_adam_kernel_times(onebit_adam_t* h, double* ms, int64_t* 
 /* Kernel launches enqueued by this handle since init. */
 onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launches);
 
+/* Variance-norm monitor ("1-bit Adam ...", Sec. 3.3: the fused variance norm stabilises early in
+ * training, which is why the variance can be frozen).  While enabled, every warm-up step also
+ * computes ||v_t||_2 over the whole parameter list (exact squares, double accumulation) and copies
+ * it to a pinned host slot (enabling allocates that slot).  variance_norm() waits for the last
+ * monitored step's value and returns it with its step index t; ONEBIT_ERR_PHASE if no monitored
+ * warm-up step has run. */
+onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enable);
+onebit_status_t onebit_adam_variance_norm(onebit_adam_t* h, double* norm, int64_t* step);
+
 /* Failure-detection test hook.  ONEBIT_FAULT_STALL_COPIES makes the next steps' shared-memory staged
  * kernels wait for `value` bytes (1..2^20) that no copy delivers, so that their bounded waits run out
  * (about one second): the kernel stops early, the sticky flag is set and onebit_adam_get_status()

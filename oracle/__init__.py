@@ -73,6 +73,8 @@ class OracleLib:
         L.ora_shard.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i64p, _i64p]
         L.ora_rms.restype = ctypes.c_float
         L.ora_rms.argtypes = [_f32p, ctypes.c_int64]
+        L.ora_norm2.restype = ctypes.c_double
+        L.ora_norm2.argtypes = [_f32p, ctypes.c_int64]
         L.ora_pack_signs.restype = None
         L.ora_pack_signs.argtypes = [_f32p, ctypes.c_int64, _u32p]
         L.ora_unpack_signs.restype = None
@@ -108,6 +110,12 @@ class OracleLib:
     def rms(self, v: np.ndarray) -> np.float32:
         v = np.ascontiguousarray(v, dtype=np.float32)
         return np.float32(self.c.ora_rms(_fp(v), v.size))
+
+    def norm2(self, v: np.ndarray) -> float:
+        v = np.ascontiguousarray(v, dtype=np.float32)
+        if v.size == 0:
+            return 0.0
+        return float(self.c.ora_norm2(_fp(v), v.size))
 
     def pack_signs(self, v: np.ndarray) -> np.ndarray:
         v = np.ascontiguousarray(v, dtype=np.float32)
@@ -174,6 +182,10 @@ def shard(length, n, j):
 
 def rms(v):
     return lib().rms(v)
+
+
+def norm2(v):
+    return lib().norm2(v)
 
 
 def pack_signs(v):

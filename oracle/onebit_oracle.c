@@ -71,6 +71,20 @@ float ora_rms(const float* v, int64_t len) {
   return (float)sqrt((sum + comp) / (double)len);
 }
 
+double ora_norm2(const float* v, int64_t len) {
+  double sum = 0.0, comp = 0.0;
+  for (int64_t e = 0; e < len; ++e) {
+    double sq = (double)v[e] * (double)v[e];
+    double t = sum + sq;
+    if (fabs(sum) >= fabs(sq))
+      comp += (sum - t) + sq;
+    else
+      comp += (sq - t) + sum;
+    sum = t;
+  }
+  return sqrt(sum + comp);
+}
+
 void ora_pack_signs(const float* v, int64_t len, uint32_t* words) {
   int64_t nw = ora_words(len);
   for (int64_t w = 0; w < nw; ++w) words[w] = 0u;

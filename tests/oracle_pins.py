@@ -268,6 +268,22 @@ def pin_warmup_mean_of_workers(ora):
         assert np.array_equal(a.view(k), b.view(k)), k
 
 
+def pin_variance_norm(ora):
+    """||v||_2 of the warm-up variance: a 3-4-12-84 vector has norm 85 exactly; with a constant
+    gradient g, ||v_t|| = (1 - b2^t) ||g^2|| (closed form of the summary formula for v_t)."""
+    assert ora.norm2(np.array([3.0, 4.0, 12.0, 84.0], np.float32)) == 85.0
+    assert ora.norm2(np.zeros(0, np.float32)) == 0.0
+    rng = np.random.default_rng(16)
+    d, T = 333, 9
+    g = (rng.standard_normal(d) * 1e-2).astype(np.float32)
+    o = ora.optimizer([d], 2, np.zeros(d, np.float32))
+    B2 = float(np.float32(0.999))
+    for t in range(1, T + 1):
+        o.warmup_step([g, g])
+        want = (1 - B2 ** t) * float(np.linalg.norm(g.astype(np.float64) ** 2))
+        assert abs(ora.norm2(o.view("v")) - want) <= 1e-5 * want, t
+
+
 def pin_freeze_closed_form(ora):
     """V = diag(sqrt(v_Tw) + eps); with bias correction v is divided by (1 - b2^Tw) first."""
     rng = np.random.default_rng(8)

@@ -280,3 +280,38 @@ def test_workspace_caller_owned():
     assert e.value.status == ob.ERR_WORKSPACE
     opt.free()
     a.close()
+
+
+def test_variance_norm_monitor_matches_oracle():
+    """||v_t||_2 reported during warm-up equals the oracle's norm of its own v after every step."""
+    import oracle
+
+    w = _tiny(numel=(70_001, 333, 5), n_workers=3, grad_dtype=W.F16, warmup_steps=4, seed=101)
+    p = Pair(w)
+    p.gpu.set_variance_monitor(True)
+    for t in range(1, 5):
+        p.warmup()
+        got, step = p.gpu.variance_norm()
+        want = oracle.norm2(p.ora.view("v"))
+        assert step == t
+        assert abs(got - want) <= 1e-12 * want, (t, got, want)
+    p.close()
+
+
+def test_warmup_until_stable_stops_where_the_closed_form_says():
+    """Constant gradient: ||v_t|| = (1 - b2^t) ||g^2||, so the relative change per step is
+    b2^(t-1) (1 - b2) / (1 - b2^(t-1)); the helper must freeze at the first step where it drops to
+    the tolerance."""
+    import math
+
+    w = _tiny(numel=(50_000,), n_workers=2, warmup_steps=100, seed=111)
+    p = Pair(w)
+    g = [t.cuda() for t in p.src.grads(0)]
+    b2 = float(np.float32(w.beta2))
+    r = {t: b2 ** (t - 1) * (1 - b2) / (1 - b2 ** (t - 1)) for t in range(2, 101)}
+    t_star = 21
+    tol = math.sqrt(r[t_star] * r[t_star - 1])  # between two consecutive steps' changes
+    steps = p.gpu.warmup_until_stable(lambda t: g, tol)
+    assert steps == t_star, (steps, t_star)
+    assert p.gpu.get_step() == (t_star, ob.PHASE_COMPRESS)
+    p.close()

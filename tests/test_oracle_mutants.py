@@ -50,6 +50,7 @@ MUTANTS = {
     "worker_scale_index_transposed": ("const float s = wscale[(int64_t)i * T + k];",
                                       "const float s = wscale[(int64_t)k * n + i];"),
     "warmup_sum_not_averaged": ("const float g = acc / (float)n;", "const float g = acc;"),
+    "norm2_without_sqrt": ("  return sqrt(sum + comp);\n}", "  return sum + comp;\n}"),
     "warmup_reads_one_worker": ("acc = acc + ora_grad_value(grads[(int64_t)i * T + k], cfg->grad_dtype, e);",
                                 "acc = acc + ora_grad_value(grads[k], cfg->grad_dtype, e);"),
 }
