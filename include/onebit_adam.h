@@ -64,7 +64,7 @@ typedef enum {
   ONEBIT_ERR_NOMEM = 4,       /* a library allocation failed */
   ONEBIT_ERR_WORKSPACE = 5,   /* the caller's workspace is too small or misaligned */
   ONEBIT_ERR_NONFINITE = 6,   /* a worker or server scale was NaN or infinite */
-  ONEBIT_ERR_UNSUPPORTED = 7  /* a valid request this build does not support */
+  ONEBIT_ERR_UNSUPPORTED = 7  /* a valid request the library does not support */
 } onebit_status_t;
 
 typedef enum { ONEBIT_F32 = 0, ONEBIT_F16 = 1, ONEBIT_BF16 = 2 } onebit_dtype_t;
