@@ -33,11 +33,18 @@ HBM_NOMINAL_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def algorithmic_bytes(n: int, gb: int) -> dict:
-    """Bytes per element each kernel must move in a steady-state compression step (m carried as
-    the broadcast's sign bits + one scale per shard; errors rebuilt from the stored c and a)."""
-    k1 = n * (gb + 4 + 4 + 1 / 8) + 1 / 8      # g_i, c_i read, c_i write, worker bits; server bits
+def algorithmic_bytes(n: int, gb: int, step: str = "compress") -> dict:
+    """Bytes per element each kernel must move in a steady-state step (compression stage: m carried
+    as the broadcast's sign bits + one scale per shard; errors rebuilt from the stored c and a)."""
+    if step == "warmup":
+        k0 = n * gb + 24                        # n gradients; m, v, x read + write
+        return {"warmup": k0, "step": k0}
     k2 = n / 8 + 4 + 4 + 1 / 8                  # n worker bit rows; a read + write; server bits
+    if step == "ec_adam":
+        k1 = n * (gb + 4 + 4 + 1 / 8)           # g_i, c_i read, c_i write, worker bits (no momentum)
+        k3 = 1 / 8 + 8 + 8 + 8                  # server bits; m, v, x read + write
+        return {"worker": k1, "server": k2, "ec_update": k3, "step": k1 + k2 + k3}
+    k1 = n * (gb + 4 + 4 + 1 / 8) + 1 / 8      # g_i, c_i read, c_i write, worker bits; server bits
     k3 = 1 / 8 + 4 + 4 + 4                      # server bits; den; x read + write
     return {"worker": k1, "server": k2, "update": k3, "step": k1 + k2 + k3}
 
@@ -225,6 +232,10 @@ def run_reference(args, w):
 
 
 METRIC = "compression-stage optimizer step params/s and HBM GB/s (% of 8 TB/s) at 1 GB300"
+STEP_METRIC = {
+    "warmup": "warm-up (uncompressed) Adam step params/s and HBM GB/s at 1 GB300",
+    "ec_adam": "gradient-compression baseline step (1-bit EC on gradients + Adam) params/s and HBM GB/s at 1 GB300",
+}
 
 
 def workload_config(w, args):
@@ -250,6 +261,9 @@ def main():
     ap.add_argument("--tw", type=int, default=-1, help="override the number of warm-up Adam steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--step", default="compress", choices=["compress", "warmup", "ec_adam"],
+                    help="what one timed step is: the compression-stage step (default), an uncompressed "
+                         "warm-up Adam step, or the gradient-compression baseline step")
     args = ap.parse_args()
 
     from communication_compressed_optimizer_compress_gb300 import workloads as W
@@ -279,20 +293,29 @@ def main():
     params = [p.to(dev) for p in W.params(w, dev)]
     src = W.GradSource(w, dev)
     gsets = [src.grads(s) for s in range(2)]
-    opt = ob.OneBitAdam(params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr,
+    # a timed warm-up step needs room for the untimed and timed warm-up steps before T_w
+    tw_handle = w.warmup_steps if args.step == "compress" else args.warmup + args.steps + 1
+    opt = ob.OneBitAdam(params, w.n_workers, tw_handle, w.beta1, w.beta2, w.eps, w.lr,
                         grad_dtype=W.TORCH_DTYPE[w.grad_dtype])
     stream = torch.cuda.current_stream()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for s in range(w.warmup_steps):
-        opt.warmup_step(gsets[s % 2])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    warm_ms = t0.elapsed_time(t1) / max(1, w.warmup_steps)
-    opt.freeze_variance()
+    warm_ms = None
+    if args.step == "compress":
+        t0.record(stream)
+        for s in range(w.warmup_steps):
+            opt.warmup_step(gsets[s % 2])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        warm_ms = t0.elapsed_time(t1) / max(1, w.warmup_steps)
+        opt.freeze_variance()
+        step_fn = opt.compress_step
+    elif args.step == "warmup":
+        step_fn = opt.warmup_step
+    else:
+        step_fn = opt.ec_adam_step
     for s in range(max(3, args.warmup)):
-        opt.compress_step(gsets[s % 2])
+        step_fn(gsets[s % 2])
     assert opt.get_status() == ob.OK, "non-finite state after warm-up"
 
     # ---- timed region
@@ -304,7 +327,7 @@ def main():
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         t0.record(stream)
         for s in range(args.steps):
-            opt.compress_step(gsets[s % 2])
+            step_fn(gsets[s % 2])
         t1.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -315,16 +338,19 @@ def main():
     max_ms = dist_max(elapsed_ms, dev)
     status = opt.get_status()
 
-    ab = algorithmic_bytes(w.n_workers, W.GRAD_BYTES[w.grad_dtype])
+    ab = algorithmic_bytes(w.n_workers, W.GRAD_BYTES[w.grad_dtype], args.step)
     ms_per_step = max_ms / args.steps
     value = world * w.d * args.steps / (max_ms / 1e3)
     step_gbs = w.d * ab["step"] / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    k1_ms = kt["worker"][0] / max(1, kt["worker"][1])
-    k1_gbs = w.d * ab["worker"] / (k1_ms / 1e3) / 1e9
+    dom = "warmup" if args.step == "warmup" else "worker"
+    dom_ms = kt[dom][0] / max(1, kt[dom][1])
+    dom_gbs = w.d * ab[dom] / (dom_ms / 1e3) / 1e9
     per_kernel = {}
-    for name in ("worker", "worker_scale", "server", "server_scale", "update"):
+    for name in ("warmup", "worker", "worker_scale", "server", "server_scale", "update", "ec_update"):
         ms, cnt = kt[name]
+        if not cnt:
+            continue
         avg = ms / max(1, cnt)
         entry = {"avg_ms": avg, "launches": cnt, "share": ms / max(1e-9, sum(v[0] for v in kt.values()))}
         if name in ab:
@@ -334,7 +360,7 @@ def main():
 
     # ---- end to end through the C ABI with host gradient buffers (H2D copies inside the timing)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.step == "compress":
         host = []
         for g in gsets[0]:
             hb = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
@@ -360,24 +386,28 @@ def main():
         del host
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.step == "compress":
         cb = oracle_sample(w)
         cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC if args.step == "compress" else STEP_METRIC[args.step], "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(w, args),
             "step_gbs": step_gbs, "step_pct_of_8tbs": 100.0 * step_gbs / HBM_NOMINAL_GBS,
             "step_frac_of_measured_peak": step_gbs / peak,
             "bytes_per_elem": ab["step"],
-            "roofline": {"bound": "hbm", "kernel": "k_worker (momentum + error + sign pack + norm partials)",
-                         "achieved": k1_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": k1_gbs / peak,
-                         "traffic": traffic_from_profiles("k_worker", "// K1: worker momentum", w.d),
-                         "bytes_per_elem": ab["worker"], "elems_per_launch": w.d},
+            "roofline": {"bound": "hbm",
+                         "kernel": {"compress": "k_worker (momentum + error + sign pack + norm partials)",
+                                    "ec_adam": "k_worker (gradient + error + sign pack + norm partials)",
+                                    "warmup": "k_warmup (worker mean + Adam)"}[args.step],
+                         "achieved": dom_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": dom_gbs / peak,
+                         "traffic": traffic_from_profiles("k_worker", "// K1: worker momentum", w.d)
+                         if args.step == "compress" else None,
+                         "bytes_per_elem": ab[dom], "elems_per_launch": w.d},
             "kernels": per_kernel,
             "warmup_adam_ms_per_step": warm_ms,
             "gpu_launches": launches,

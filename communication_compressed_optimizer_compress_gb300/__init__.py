@@ -19,7 +19,8 @@ PHASE_WARMUP, PHASE_COMPRESS = 0, 1
 (STATE_M, STATE_V, STATE_WORKER_ERROR, STATE_SERVER_ERROR, STATE_WORKER_BITS, STATE_SERVER_BITS,
  STATE_WORKER_SCALES, STATE_SERVER_SCALES) = range(8)
 FAULT_NONE, FAULT_STALL_COPIES = 0, 1
-KERNEL_NAMES = ["warmup", "freeze", "worker", "worker_scale", "server", "server_scale", "update", "export"]
+KERNEL_NAMES = ["warmup", "freeze", "worker", "worker_scale", "server", "server_scale", "update", "export",
+                "ec_update"]
 NUM_KERNELS = len(KERNEL_NAMES)
 
 
@@ -68,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "onebit_adam_warmup_step": [vp, ctypes.POINTER(vp), vp],
             "onebit_adam_freeze_variance": [vp, vp],
             "onebit_adam_compress_step": [vp, ctypes.POINTER(vp), vp],
+            "onebit_adam_ec_adam_step": [vp, ctypes.POINTER(vp), vp],
             "onebit_adam_warmup_step_host": [vp, ctypes.POINTER(vp), vp],
             "onebit_adam_compress_step_host": [vp, ctypes.POINTER(vp), vp],
             "onebit_adam_free": [vp],
@@ -203,6 +205,11 @@ class OneBitAdam:
     def compress_step(self, grads, stream=None):
         _check(lib().onebit_adam_compress_step(self.h, self._grad_array(grads), _stream_ptr(stream)),
                "onebit_adam_compress_step", self.h)
+
+    def ec_adam_step(self, grads, stream=None):
+        """Gradient-compression baseline step (1-bit EC compression of the gradients, then Adam)."""
+        _check(lib().onebit_adam_ec_adam_step(self.h, self._grad_array(grads), _stream_ptr(stream)),
+               "onebit_adam_ec_adam_step", self.h)
 
     def warmup_step_host(self, grads, stream=None):
         _check(lib().onebit_adam_warmup_step_host(self.h, self._grad_array(grads, cuda=False), _stream_ptr(stream)),

@@ -365,7 +365,7 @@ onebit_status_t run_warmup(onebit_adam* h, StepArgs A, bool vec, cudaStream_t st
   return h->vmon ? run_warmup_m<GT, true>(h, A, vec, st) : run_warmup_m<GT, false>(h, A, vec, st);
 }
 
-template <typename GT, bool DM, bool HE>
+template <typename GT, int DM, bool HE>
 onebit_status_t run_worker_v(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
   const int64_t units = (int64_t)A.n_chunks * A.n;
   if (vec) {
@@ -377,12 +377,11 @@ onebit_status_t run_worker_v(onebit_adam* h, const StepArgs& A, bool vec, cudaSt
 }
 
 template <typename GT>
-onebit_status_t run_worker(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
-  const bool dm = h->m_dense, he = !h->werr_zero;
-  if (dm && he) return run_worker_v<GT, true, true>(h, A, vec, st);
-  if (dm) return run_worker_v<GT, true, false>(h, A, vec, st);
-  if (he) return run_worker_v<GT, false, true>(h, A, vec, st);
-  return run_worker_v<GT, false, false>(h, A, vec, st);
+onebit_status_t run_worker(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st, bool grad_only) {
+  const bool he = !h->werr_zero;
+  if (grad_only) return he ? run_worker_v<GT, kMomNone, true>(h, A, vec, st) : run_worker_v<GT, kMomNone, false>(h, A, vec, st);
+  if (h->m_dense) return he ? run_worker_v<GT, kMomDense, true>(h, A, vec, st) : run_worker_v<GT, kMomDense, false>(h, A, vec, st);
+  return he ? run_worker_v<GT, kMomBits, true>(h, A, vec, st) : run_worker_v<GT, kMomBits, false>(h, A, vec, st);
 }
 
 template <bool HE>
@@ -439,23 +438,35 @@ onebit_status_t do_warmup(onebit_adam* h, const void* const* grads, cudaStream_t
   return ONEBIT_OK;
 }
 
-onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream_t st) {
-  if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+// One compression-stage step, or (ec_adam) one step of the gradient-compression baseline: the
+// same worker/server compression of g_i + delta_i, then Adam on the broadcast.
+onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream_t st, bool ec_adam = false) {
+  if (h->phase != (ec_adam ? ONEBIT_PHASE_WARMUP : ONEBIT_PHASE_COMPRESS)) return ONEBIT_ERR_PHASE;
   StepArgs A = base_args(h);
   bool vec = false;
   onebit_status_t s = bind_grads(h, grads, st, &A.gptr, &vec);
   if (s) return s;
   switch (h->cfg.grad_dtype) {
-    case ONEBIT_F32: s = run_worker<float>(h, A, vec, st); break;
-    case ONEBIT_F16: s = run_worker<__half>(h, A, vec, st); break;
-    default: s = run_worker<__nv_bfloat16>(h, A, vec, st); break;
+    case ONEBIT_F32: s = run_worker<float>(h, A, vec, st, ec_adam); break;
+    case ONEBIT_F16: s = run_worker<__half>(h, A, vec, st, ec_adam); break;
+    default: s = run_worker<__nv_bfloat16>(h, A, vec, st, ec_adam); break;
   }
   if (s) return s;
   const int nt = h->plan.n * h->plan.T;
   if ((s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale, nt, kScaleThreads, st, A))) return s;
   if ((s = run_server(h, A, st))) return s;
   if ((s = launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale, nt, kScaleThreads, st, A))) return s;
-  if (h->params_aligned) {
+  if (ec_adam) {
+    const int64_t t = h->t + 1;
+    A.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, (double)t));
+    A.bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)t));
+    auto go = [&](auto k) {
+      return launch(h, ONEBIT_K_EC_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+    };
+    const bool bc = h->cfg.bias_correction != 0;
+    if (bc) s = h->params_aligned ? go(k_ec_adam_update<true, true>) : go(k_ec_adam_update<true, false>);
+    else s = h->params_aligned ? go(k_ec_adam_update<false, true>) : go(k_ec_adam_update<false, false>);
+  } else if (h->params_aligned) {
     auto k = k_update<true>;
     s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
   } else {
@@ -465,7 +476,7 @@ onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream
   if (s) return s;
   h->compress_steps += 1;
   h->t += 1;
-  h->m_dense = false;
+  if (!ec_adam) h->m_dense = false;  // the baseline keeps Adam's own fp32 momentum
   h->werr_zero = false;
   h->serr_zero = false;
   return ONEBIT_OK;
@@ -719,6 +730,12 @@ onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* g
   return do_compress(h, grads, as_stream(stream));
 }
 
+onebit_status_t onebit_adam_ec_adam_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
+  if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  return do_compress(h, grads, as_stream(stream), true);
+}
+
 onebit_status_t onebit_adam_warmup_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream) {
   if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
   if (h->phase != ONEBIT_PHASE_WARMUP || h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
@@ -855,12 +872,12 @@ onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worke
     case ONEBIT_STATE_M: return export_m(h, out, st);
     case ONEBIT_STATE_V: return run_export(h, kExportCopy, h->at<float>(h->lay.v), nullptr, nullptr, 0, 0, out, st);
     case ONEBIT_STATE_WORKER_ERROR:
-      if (h->phase != ONEBIT_PHASE_COMPRESS || h->werr_zero)
+      if (h->werr_zero)
         return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
       return run_export(h, kExportSignedErr, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, nullptr,
                         last_wscale(h) + (size_t)worker * P.T, 1, 0, out, st);
     case ONEBIT_STATE_SERVER_ERROR:
-      if (h->phase != ONEBIT_PHASE_COMPRESS || h->serr_zero)
+      if (h->serr_zero)
         return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
       return run_export(h, kExportSignedErr, h->at<float>(h->lay.a), nullptr, last_sscale(h), P.n, 1, out, st);
     case ONEBIT_STATE_WORKER_BITS:

@@ -244,8 +244,16 @@ __device__ __forceinline__ float error_of(float c, float s) {  // c - s*sign(c),
 // One unit = (chunk, worker).  c_i = (b1*m + (1-b1)*g_i) + delta_i, delta_i rebuilt from the
 // previous c_i and s_i; writes c_i, its sign byte and the chunk's sum of c_i^2.
 
-template <typename GT, bool DENSE_M, bool HAS_ERR, bool VEC>
+// Where the worker kernel's momentum comes from.
+enum MomentumSource : int {
+  kMomBits = 0,   // the previous broadcast: S * sign(a), from the server sign bits
+  kMomDense = 1,  // the fp32 buffer (first compression step, after an import)
+  kMomNone = 2    // no momentum: c_i = g_i + delta_i (the gradient-compression baseline)
+};
+
+template <typename GT, int MSRC, bool HAS_ERR, bool VEC>
 __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
+  constexpr bool DENSE_M = MSRC == kMomDense;
   __shared__ double red[kThreads / 32];
   const int64_t n_units = (int64_t)A.n_chunks * A.n;
   for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -258,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
     const uint8_t* __restrict__ sb = reinterpret_cast<const uint8_t*>(A.sbits) + (ch.off >> 3);
     const float* __restrict__ md = A.m + ch.off;
     const float sp = HAS_ERR ? A.wscale_prev[(int64_t)i * A.T + ch.seg] : 0.0f;
-    const float Sp = DENSE_M ? 0.0f : A.sscale_prev[(int64_t)ch.seg * A.n + ch.shard];
+    const float Sp = MSRC == kMomBits ? A.sscale_prev[(int64_t)ch.seg * A.n + ch.shard] : 0.0f;
     const float b1 = A.b1, omb1 = A.omb1;
 
     // one group of 8 elements: loads first (so that two groups are in flight), then math + stores
@@ -266,6 +274,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       float g[8], cp[8], m[8];
       uint32_t mb;
     };
+    (void)DENSE_M;
     auto load = [&](In& r, int gi) {
       const int64_t e = (int64_t)gi * 8;
       if (VEC) {
@@ -275,8 +284,8 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
         for (int q = 0; q < 8; ++q) r.g[q] = Grad<GT>::load1(g + e + q);
       }
       if (HAS_ERR) ld8_state(c + e, r.cp);
-      if (DENSE_M) ld8_stream(md + e, r.m);
-      else r.mb = sb[gi];
+      if (MSRC == kMomDense) ld8_stream(md + e, r.m);
+      if (MSRC == kMomBits) r.mb = sb[gi];
     };
     unsigned long long hi = 0, lo = 0;  // this thread's sum of c^2 over the unit (two lanes)
     auto work = [&](const In& r, int gi) {
@@ -284,8 +293,13 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       uint32_t byte = 0;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float mq = DENSE_M ? r.m[q] : (((r.mb >> q) & 1u) ? Sp : -Sp);
-        const float mi = momentum(b1, omb1, mq, r.g[q]);
+        float mi;
+        if (MSRC == kMomNone) {
+          mi = r.g[q];
+        } else {
+          const float mq = MSRC == kMomDense ? r.m[q] : (((r.mb >> q) & 1u) ? Sp : -Sp);
+          mi = momentum(b1, omb1, mq, r.g[q]);
+        }
         const float d = HAS_ERR ? error_of(r.cp[q], sp) : 0.0f;
         const float cq = __fadd_rn(mi, d);
         out[q] = cq;
@@ -317,8 +331,13 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       uint32_t byte = 0;
       for (int q = 0; q < rem; ++q) {
         const int64_t e = e0 + q;
-        const float mq = DENSE_M ? md[e] : (((sb[ng] >> q) & 1u) ? Sp : -Sp);
-        const float mi = momentum(b1, omb1, mq, Grad<GT>::load1(g + e));
+        float mi;
+        if (MSRC == kMomNone) {
+          mi = Grad<GT>::load1(g + e);
+        } else {
+          const float mq = MSRC == kMomDense ? md[e] : (((sb[ng] >> q) & 1u) ? Sp : -Sp);
+          mi = momentum(b1, omb1, mq, Grad<GT>::load1(g + e));
+        }
         const float d = HAS_ERR ? error_of(c[e], sp) : 0.0f;
         const float cq = __fadd_rn(mi, d);
         c[e] = cq;
@@ -832,6 +851,72 @@ __global__ void __launch_bounds__(kThreads) k_update(const StepArgs A) {
       for (int q = 0; q < rem; ++q) {
         const float mq = ((sb[ng] >> q) & 1u) ? S : -S;
         x[e0 + q] = __fsub_rn(x[e0 + q], __fmul_rn(lr, __fdiv_rn(mq, den[e0 + q])));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Gradient-compression baseline: every worker runs Adam on the broadcast g_hat = S * sign(a).
+
+template <bool BC, bool VEC>
+__global__ void __launch_bounds__(kThreads) k_ec_adam_update(const StepArgs A) {
+  for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
+    const Chunk ch = A.chunks[u];
+    const float S = A.sscale_cur[(int64_t)ch.seg * A.n + ch.shard];
+    float* __restrict__ x = A.pptr[ch.seg] + ch.start;
+    float* __restrict__ m = A.m + ch.off;
+    float* __restrict__ v = A.v + ch.off;
+    const uint8_t* __restrict__ sb = reinterpret_cast<const uint8_t*>(A.sbits) + (ch.off >> 3);
+    const int ng = (ch.len + 7) >> 3;
+    for (int gi = threadIdx.x; gi < ng; gi += kThreads) {
+      const int cnt = min(8, ch.len - gi * 8);
+      const int64_t e = (int64_t)gi * 8;
+      const bool vec = VEC && cnt == 8;
+      float mv[8], vv[8], xv[8];
+      if (cnt == 8) {
+        ld8_state(m + e, mv);
+        ld8_state(v + e, vv);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          mv[q] = q < cnt ? m[e + q] : 0.0f;
+          vv[q] = q < cnt ? v[e + q] : 0.0f;
+        }
+      }
+      if (vec) {
+        ld8_state(x + e, xv);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xv[q] = q < cnt ? x[e + q] : 0.0f;
+      }
+      const uint32_t byte = sb[gi];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float gh = ((byte >> q) & 1u) ? S : -S;
+        mv[q] = momentum(A.b1, A.omb1, mv[q], gh);
+        vv[q] = __fadd_rn(__fmul_rn(A.b2, vv[q]), __fmul_rn(A.omb2, __fmul_rn(gh, gh)));
+        const float mh = BC ? __fdiv_rn(mv[q], A.bc1) : mv[q];
+        const float vh = BC ? __fdiv_rn(vv[q], A.bc2) : vv[q];
+        xv[q] = __fsub_rn(xv[q], __fmul_rn(A.lr, __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), A.eps))));
+      }
+      if (cnt == 8) {
+        st8(m + e, mv);
+        st8(v + e, vv);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < cnt) {
+            m[e + q] = mv[q];
+            v[e + q] = vv[q];
+          }
+      }
+      if (vec) {
+        st8(x + e, xv);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < cnt) x[e + q] = xv[q];
       }
     }
   }

@@ -93,7 +93,8 @@ typedef enum {
   ONEBIT_K_SERVER_SCALE = 5,   /* server shard scales from the partials */
   ONEBIT_K_UPDATE = 6,         /* unpack broadcast + preconditioned update */
   ONEBIT_K_EXPORT = 7,         /* state export / import */
-  ONEBIT_NUM_KERNELS = 8
+  ONEBIT_K_EC_UPDATE = 8,      /* Adam on the broadcast gradient (gradient-compression baseline) */
+  ONEBIT_NUM_KERNELS = 9
 } onebit_kernel_t;
 
 typedef struct {
@@ -130,6 +131,15 @@ onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t st
 
 /* One compression-stage step (legal in phase COMPRESS).  grads as for warmup_step.  t += 1. */
 onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream);
+
+/* One step of the baseline the method is contrasted with ("1-bit Adam ...", Sec. 3.2 and 4.2):
+ * error-compensated 1-bit compression of the GRADIENTS (c_i = g_i + delta_i, worker and server
+ * compression and error feedback exactly as in the compression stage), then every worker runs plain
+ * Adam on the broadcast g_hat = S*sign(a): m = b1 m + (1-b1) g_hat, v = b2 v + (1-b2) g_hat^2,
+ * x -= lr * m/(sqrt(v)+eps) (bias-corrected if configured).  Legal in phase WARMUP (any t); it
+ * shares m and v with warmup_step, keeps its own error memories (exported as WORKER_ERROR /
+ * SERVER_ERROR) and a freeze resets them.  t += 1. */
+onebit_status_t onebit_adam_ec_adam_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream);
 
 /* The same two steps with HOST gradient buffers ([n*T] host pointers, pinned or pageable): the
  * library copies them into one of two device staging buffers it owns (allocated on first use,

@@ -89,6 +89,9 @@ class OracleLib:
         L.ora_compress_step.restype = ctypes.c_int
         L.ora_compress_step.argtypes = [ctypes.POINTER(_Cfg), _f32p, _f32p, _f32p, _f32p, _f32p, vpp,
                                         _u32p, _f32p, _u32p, _f32p]
+        L.ora_ec_adam_step.restype = ctypes.c_int
+        L.ora_ec_adam_step.argtypes = [ctypes.POINTER(_Cfg), ctypes.c_int64, _f32p, _f32p, _f32p, _f32p, _f32p,
+                                       vpp, _u32p, _f32p, _u32p, _f32p]
         self.c = L
         self.path = path
 
@@ -277,6 +280,17 @@ class OneBitAdamOracle:
         rc = self.lib.c.ora_compress_step(ctypes.byref(self.cfg), _fp(self.x), _fp(self.m), _fp(self.den),
                                      _fp(self.delta), _fp(self.eps_srv), ptrs, _up(self.wbits),
                                      _fp(self.wscale), _up(self.sbits), _fp(self.sscale))
+        assert rc == 0
+
+    def ec_adam_step(self, grads):
+        """The baseline of error-compensated 1-bit compression applied to the gradients, then Adam
+        ("1-bit Adam ...", Sec. 3.2).  Legal in the warm-up phase; shares m, v and the error memories."""
+        assert self.phase == "warmup"
+        self.t += 1
+        ptrs, keep = self._grad_ptrs(grads)
+        rc = self.lib.c.ora_ec_adam_step(ctypes.byref(self.cfg), self.t, _fp(self.x), _fp(self.m), _fp(self.v),
+                                         _fp(self.delta), _fp(self.eps_srv), ptrs, _up(self.wbits),
+                                         _fp(self.wscale), _up(self.sbits), _fp(self.sscale))
         assert rc == 0
 
     # views without the size-1 placeholder used for empty lists

@@ -124,13 +124,24 @@ static int check_cfg(const ora_config* cfg) {
   return 0;
 }
 
+/* One Adam update of one element with gradient g ([P2] summary formulas). */
+static void adam_element(const ora_config* cfg, float bc1, float bc2, float g, float* m, float* v, float* x) {
+  const float b1 = cfg->beta1, omb1 = 1.0f - cfg->beta1;
+  const float b2 = cfg->beta2, omb2 = 1.0f - cfg->beta2;
+  *m = b1 * *m + omb1 * g;
+  *v = b2 * *v + omb2 * (g * g);
+  float mh = *m, vh = *v;
+  if (cfg->bias_correction) {
+    mh = mh / bc1;
+    vh = vh / bc2;
+  }
+  *x = *x - cfg->lr * (mh / (sqrtf(vh) + cfg->eps));
+}
+
 int ora_warmup_step(const ora_config* cfg, int64_t t, float* x, float* m, float* v,
                     const void* const* grads) {
   if (check_cfg(cfg) || t < 1) return 1;
   const int n = cfg->n_workers, T = cfg->n_tensors;
-  const float b1 = cfg->beta1, omb1 = 1.0f - cfg->beta1;
-  const float b2 = cfg->beta2, omb2 = 1.0f - cfg->beta2;
-  const float lr = cfg->lr, eps = cfg->eps;
   const float bc1 = (float)(1.0 - pow((double)cfg->beta1, (double)t));
   const float bc2 = (float)(1.0 - pow((double)cfg->beta2, (double)t));
   int64_t off = 0;
@@ -143,14 +154,7 @@ int ora_warmup_step(const ora_config* cfg, int64_t t, float* x, float* m, float*
       for (int i = 0; i < n; ++i) acc = acc + ora_grad_value(grads[(int64_t)i * T + k], cfg->grad_dtype, e);
       const float g = acc / (float)n;
       const int64_t p = off + e;
-      m[p] = b1 * m[p] + omb1 * g;
-      v[p] = b2 * v[p] + omb2 * (g * g);
-      float mh = m[p], vh = v[p];
-      if (cfg->bias_correction) {
-        mh = mh / bc1;
-        vh = vh / bc2;
-      }
-      x[p] = x[p] - lr * (mh / (sqrtf(vh) + eps));
+      adam_element(cfg, bc1, bc2, g, &m[p], &v[p], &x[p]);
     }
     off += L;
   }
@@ -168,22 +172,92 @@ int ora_freeze(const ora_config* cfg, int64_t t_freeze, const float* v, float* d
   return 0;
 }
 
+/* Each worker, each tensor: 1-bit compression of c with error feedback ([P1] Sec. 4.3, 11). */
+static void workers_compress(const ora_config* cfg, const float* c, float* delta, uint32_t* wbits, float* wscale) {
+  const int n = cfg->n_workers, T = cfg->n_tensors;
+  const int64_t D = total_numel(cfg), W = total_words(cfg);
+  for (int i = 0; i < n; ++i) {
+    int64_t off = 0, woff = 0;
+    for (int k = 0; k < T; ++k) {
+      const int64_t L = cfg->numel[k];
+      wscale[(int64_t)i * T + k] =
+          ora_compress(c + (int64_t)i * D + off, L, wbits + (int64_t)i * W + woff, delta + (int64_t)i * D + off);
+      off += L;
+      woff += ora_words(L);
+    }
+  }
+}
+
+/* Server shard j of tensor k: average of the n decompressed messages, plus the server error. */
+static void server_average(const ora_config* cfg, const uint32_t* wbits, const float* wscale, const float* eps_srv,
+                           float* a) {
+  const int n = cfg->n_workers, T = cfg->n_tensors;
+  const int64_t W = total_words(cfg);
+  int64_t off = 0, woff = 0;
+  for (int k = 0; k < T; ++k) {
+    const int64_t L = cfg->numel[k];
+    for (int64_t e = 0; e < L; ++e) {
+      float acc = 0.0f;
+      for (int i = 0; i < n; ++i) {
+        const uint32_t bit = (wbits[(int64_t)i * W + woff + e / 32] >> (e % 32)) & 1u;
+        const float s = wscale[(int64_t)i * T + k];
+        acc = acc + (bit ? s : -s);
+      }
+      a[off + e] = acc / (float)n + eps_srv[off + e];
+    }
+    off += L;
+    woff += ora_words(L);
+  }
+}
+
+/* Recompress every shard with server error feedback; bcast receives the broadcast S*sign(a). */
+static void server_recompress(const ora_config* cfg, const float* a, float* eps_srv, uint32_t* sbits, float* sscale,
+                              float* bcast) {
+  const int n = cfg->n_workers, T = cfg->n_tensors;
+  int64_t off = 0, woff = 0;
+  for (int k = 0; k < T; ++k) {
+    const int64_t L = cfg->numel[k];
+    for (int64_t w = 0; w < ora_words(L); ++w) sbits[woff + w] = 0u;
+    for (int j = 0; j < n; ++j) {
+      int64_t lo, hi;
+      ora_shard(L, n, j, &lo, &hi);
+      const float S = ora_rms(a + off + lo, hi - lo);
+      sscale[(int64_t)k * n + j] = S;
+      for (int64_t e = lo; e < hi; ++e) {
+        const int64_t p = off + e;
+        const int bit = a[p] >= 0.0f;
+        if (bit) sbits[woff + e / 32] |= 1u << (e % 32);
+        eps_srv[p] = bit ? a[p] - S : a[p] + S;
+        bcast[p] = bit ? S : -S;
+      }
+    }
+    off += L;
+    woff += ora_words(L);
+  }
+}
+
+/* Scratch for one step: c [n][D], a [D], broadcast [D]. */
+static float* step_scratch(const ora_config* cfg, float** c, float** a, float** b) {
+  const int64_t D = total_numel(cfg);
+  const size_t d1 = (size_t)(D > 0 ? D : 1);
+  float* buf = (float*)malloc(sizeof(float) * d1 * ((size_t)cfg->n_workers + 2));
+  if (!buf) return NULL;
+  *c = buf;
+  *a = buf + d1 * (size_t)cfg->n_workers;
+  *b = *a + d1;
+  return buf;
+}
+
 int ora_compress_step(const ora_config* cfg, float* x, float* m, const float* den, float* delta,
                       float* eps_srv, const void* const* grads, uint32_t* wbits, float* wscale,
                       uint32_t* sbits, float* sscale) {
   if (check_cfg(cfg)) return 1;
   const int n = cfg->n_workers, T = cfg->n_tensors;
-  const int64_t D = total_numel(cfg), W = total_words(cfg);
+  const int64_t D = total_numel(cfg);
   const float b1 = cfg->beta1, omb1 = 1.0f - cfg->beta1;
-  const float lr = cfg->lr;
-
-  float* c = (float*)malloc(sizeof(float) * (size_t)(D > 0 ? D : 1) * (size_t)n);
-  float* a = (float*)malloc(sizeof(float) * (size_t)(D > 0 ? D : 1));
-  if (!c || !a) {
-    free(c);
-    free(a);
-    return 2;
-  }
+  float *c, *a, *bcast;
+  float* buf = step_scratch(cfg, &c, &a, &bcast);
+  if (!buf) return 2;
 
   /* 1. each worker: local momentum, then add its error memory */
   for (int i = 0; i < n; ++i) {
@@ -199,66 +273,50 @@ int ora_compress_step(const ora_config* cfg, float* x, float* m, const float* de
       off += L;
     }
   }
+  /* 2-3. worker compression; 4. server average + server error */
+  workers_compress(cfg, c, delta, wbits, wscale);
+  server_average(cfg, wbits, wscale, eps_srv, a);
+  /* 5-7. recompression; the broadcast is the shared m; x -= lr * m / (sqrt(v_frozen) + eps) */
+  server_recompress(cfg, a, eps_srv, sbits, sscale, bcast);
+  for (int64_t p = 0; p < D; ++p) {
+    m[p] = bcast[p];
+    x[p] = x[p] - cfg->lr * (m[p] / den[p]);
+  }
+  free(buf);
+  return 0;
+}
 
-  /* 2-3. each worker, each tensor: 1-bit compression with error feedback */
+int ora_ec_adam_step(const ora_config* cfg, int64_t t, float* x, float* m, float* v, float* delta,
+                     float* eps_srv, const void* const* grads, uint32_t* wbits, float* wscale, uint32_t* sbits,
+                     float* sscale) {
+  if (check_cfg(cfg) || t < 1) return 1;
+  const int n = cfg->n_workers, T = cfg->n_tensors;
+  const int64_t D = total_numel(cfg);
+  const float bc1 = (float)(1.0 - pow((double)cfg->beta1, (double)t));
+  const float bc2 = (float)(1.0 - pow((double)cfg->beta2, (double)t));
+  float *c, *a, *bcast;
+  float* buf = step_scratch(cfg, &c, &a, &bcast);
+  if (!buf) return 2;
+
+  /* 1. each worker: its gradient plus its error memory */
   for (int i = 0; i < n; ++i) {
-    int64_t off = 0, woff = 0;
+    int64_t off = 0;
     for (int k = 0; k < T; ++k) {
       const int64_t L = cfg->numel[k];
-      wscale[(int64_t)i * T + k] =
-          ora_compress(c + (int64_t)i * D + off, L, wbits + (int64_t)i * W + woff, delta + (int64_t)i * D + off);
-      off += L;
-      woff += ora_words(L);
-    }
-  }
-
-  /* 4. server shard j of tensor k: average of the n decompressed messages, plus the server error */
-  {
-    int64_t off = 0, woff = 0;
-    for (int k = 0; k < T; ++k) {
-      const int64_t L = cfg->numel[k];
+      const void* g = grads[(int64_t)i * T + k];
       for (int64_t e = 0; e < L; ++e) {
-        float acc = 0.0f;
-        for (int i = 0; i < n; ++i) {
-          const uint32_t bit = (wbits[(int64_t)i * W + woff + e / 32] >> (e % 32)) & 1u;
-          const float s = wscale[(int64_t)i * T + k];
-          acc = acc + (bit ? s : -s);
-        }
-        a[off + e] = acc / (float)n + eps_srv[off + e];
+        const int64_t p = off + e;
+        c[(int64_t)i * D + p] = ora_grad_value(g, cfg->grad_dtype, e) + delta[(int64_t)i * D + p];
       }
       off += L;
-      woff += ora_words(L);
     }
   }
-
-  /* 5-7. recompress each shard with server error feedback; the broadcast result is the shared m;
-   * preconditioned update x -= lr * m / (sqrt(v_frozen) + eps) */
-  {
-    int64_t off = 0, woff = 0;
-    for (int k = 0; k < T; ++k) {
-      const int64_t L = cfg->numel[k];
-      for (int64_t w = 0; w < ora_words(L); ++w) sbits[woff + w] = 0u;
-      for (int j = 0; j < n; ++j) {
-        int64_t lo, hi;
-        ora_shard(L, n, j, &lo, &hi);
-        const float S = ora_rms(a + off + lo, hi - lo);
-        sscale[(int64_t)k * n + j] = S;
-        for (int64_t e = lo; e < hi; ++e) {
-          const int64_t p = off + e;
-          const int bit = a[p] >= 0.0f;
-          if (bit) sbits[woff + e / 32] |= 1u << (e % 32);
-          eps_srv[p] = bit ? a[p] - S : a[p] + S;
-          m[p] = bit ? S : -S;
-          x[p] = x[p] - lr * (m[p] / den[p]);
-        }
-      }
-      off += L;
-      woff += ora_words(L);
-    }
-  }
-
-  free(c);
-  free(a);
-  (void)D;
+  /* 2. worker compression; 3. server average + error; 4. recompression and broadcast */
+  workers_compress(cfg, c, delta, wbits, wscale);
+  server_average(cfg, wbits, wscale, eps_srv, a);
+  server_recompress(cfg, a, eps_srv, sbits, sscale, bcast);
+  /* 5. every worker runs Adam on the broadcast gradient */
+  for (int64_t p = 0; p < D; ++p) adam_element(cfg, bc1, bc2, bcast[p], &m[p], &v[p], &x[p]);
+  free(buf);
   return 0;
 }

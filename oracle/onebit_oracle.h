@@ -98,6 +98,19 @@ int ora_compress_step(const ora_config* cfg, float* x, float* m, const float* de
                       float* eps_srv, const void* const* grads, uint32_t* wbits, float* wscale,
                       uint32_t* sbits, float* sscale);
 
+/* The baseline the method is contrasted with ([P1] Sec. 3.2 and 4.2): error-compensated 1-bit
+ * compression applied to the GRADIENTS, with plain Adam on the result.  t is the 1-based step index
+ * (bias correction only).
+ *   worker i:  c_i = g_i + delta_i;  per tensor: s_ik = rms(c_i);  bits_i = sign(c_i);
+ *              delta_i = c_i - s_ik sign(c_i)
+ *   server:    a = (sum_i s_ik sign_i) / n + eps_srv;  per shard: S = rms(a);  eps_srv = a - S sign(a)
+ *   every worker:  g_hat = S sign(a);  m = b1 m + (1-b1) g_hat;  v = b2 v + (1-b2) g_hat^2;
+ *              x = x - lr * (mh / (sqrt(vh) + eps))   (mh, vh bias-corrected if configured)
+ * Same array layouts as ora_compress_step. */
+int ora_ec_adam_step(const ora_config* cfg, int64_t t, float* x, float* m, float* v, float* delta,
+                     float* eps_srv, const void* const* grads, uint32_t* wbits, float* wscale, uint32_t* sbits,
+                     float* sscale);
+
 #ifdef __cplusplus
 }
 #endif

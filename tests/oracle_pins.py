@@ -507,4 +507,74 @@ def pin_tensors_are_independent(ora):
         assert np.array_equal(whole.sscale[k], p.sscale[0])
 
 
+def pin_ec_adam_lossless_is_adam(ora):
+    """Baseline of Sec. 3.2 (1-bit EC compression of the gradients, then Adam): when every worker's
+    gradient has equal magnitudes and all share one sign pattern, worker and server compression are
+    lossless, so the step is textbook Adam (torch.optim.Adam, bias-corrected) on the mean gradient."""
+    import torch
+
+    rng = np.random.default_rng(17)
+    d, n, T = 256, 4, 6
+    sig = np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    x0 = (rng.standard_normal(d) * 0.02).astype(np.float32)
+    o = ora.optimizer([d], n, x0, beta1=0.9, beta2=0.999, eps=1e-8, lr=1e-3, bias_correction=True)
+    p = torch.nn.Parameter(torch.from_numpy(x0.copy()))
+    b1, b2 = float(np.float32(0.9)), float(np.float32(0.999))
+    opt = torch.optim.Adam([p], lr=float(np.float32(1e-3)), betas=(b1, b2), eps=float(np.float32(1e-8)))
+    for t in range(T):
+        mags = [2.0 ** -(8 + (t + i) % 3) for i in range(n)]
+        gs = [(sig * a).astype(np.float32) for a in mags]
+        o.ec_adam_step(gs)
+        p.grad = torch.from_numpy((sig * (sum(mags) / n)).astype(np.float32))
+        opt.step()
+        assert not np.any(o.view("delta")) and not np.any(o.view("eps_srv")), t
+    assert np.allclose(o.view("x"), p.detach().numpy(), rtol=1e-6, atol=1e-9)
+    assert np.allclose(o.view("m"), opt.state[p]["exp_avg"].numpy(), rtol=1e-6, atol=0)
+    assert np.allclose(o.view("v"), opt.state[p]["exp_avg_sq"].numpy(), rtol=1e-6, atol=0)
+
+
+def pin_ec_adam_error_feedback_telescopes(ora):
+    """The baseline's error feedback telescopes on the gradients: sum of messages + final error =
+    sum of gradients (workers), and likewise for the server (Sec. 4.1)."""
+    rng = np.random.default_rng(18)
+    numel = [300, 0, 65]
+    D, n, T, steps = sum(numel), 3, len(numel), 5
+    offs = np.concatenate([[0], np.cumsum(numel)]).astype(int)
+    woffs = np.concatenate([[0], np.cumsum([ora.words(L) for L in numel])]).astype(int)
+    o = ora.optimizer(numel, n, np.zeros(D, np.float32))
+
+    def decode(words_row, scales_row):
+        out = np.zeros(D)
+        for k, L in enumerate(numel):
+            out[offs[k]: offs[k + 1]] = ora.unpack_signs(words_row[woffs[k]: woffs[k + 1]], L, scales_row[k])
+        return out
+
+    sum_g = np.zeros((n, D))
+    sum_msg = np.zeros((n, D))
+    sum_avg = np.zeros(D)
+    sum_srv = np.zeros(D)
+    for _ in range(steps):
+        flats = [(rng.standard_normal(D) * 1e-3).astype(np.float32) for _ in range(n)]
+        o.ec_adam_step([f[offs[k]: offs[k + 1]] for f in flats for k in range(T)])
+        avg = np.zeros(D)
+        for i in range(n):
+            sum_g[i] += flats[i]
+            msg = decode(o.view("wbits")[i], o.wscale[i])
+            sum_msg[i] += msg
+            avg += msg
+        avg /= n
+        sum_avg += avg
+        srv = np.zeros(D)
+        for k, L in enumerate(numel):
+            w = o.view("sbits")[woffs[k]: woffs[k + 1]]
+            for j in range(n):
+                lo, hi = ora.shard(L, n, j)
+                srv[offs[k] + lo: offs[k] + hi] = ora.unpack_signs(w, L, o.sscale[k, j])[lo:hi]
+        sum_srv += srv
+    for i in range(n):
+        scale = np.abs(sum_g[i]).max()
+        assert np.max(np.abs(sum_msg[i] + o.view("delta")[i] - sum_g[i])) <= 1e-6 * scale * steps, i
+    assert np.max(np.abs(sum_srv + o.view("eps_srv") - sum_avg)) <= 1e-6 * np.abs(sum_avg).max() * steps
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

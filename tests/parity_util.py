@@ -133,6 +133,14 @@ class Pair:
         if check:
             self.check_compress()
 
+    def ec_adam(self, check=True):
+        """One step of the gradient-compression baseline on both sides."""
+        g = self.grads()
+        self.gpu.ec_adam_step(self._to_dev(g))
+        self.ora.ec_adam_step([W.to_numpy_grad(t) for t in g])
+        if check:
+            self.check_compress(ec=True)
+
     def x(self):
         if self.D == 0:
             return np.zeros(0, np.float32)
@@ -152,7 +160,7 @@ class Pair:
         _close("m (warm-up)", gm, self.ora.view("m"))
         _close("v (warm-up)", gv, self.ora.view("v"))
 
-    def check_compress(self):
+    def check_compress(self, ec=False):
         torch.cuda.synchronize()
         assert self.gpu.get_status() == ob.OK
         w, o, n = self.w, self.ora, self.w.n_workers
@@ -214,6 +222,8 @@ class Pair:
         _close("server error", self.gpu.export_state(ob.STATE_SERVER_ERROR).cpu().numpy(), o.view("eps_srv"), keep)
         _close("m", self.gpu.export_state(ob.STATE_M).cpu().numpy(), o.view("m"), keep)
         _close("x", self.x(), o.view("x"), keep)
+        if ec:
+            _close("v", self.gpu.export_state(ob.STATE_V).cpu().numpy(), o.view("v"), keep)
         for k, L in enumerate(self.numel):
             for j in range(n):
                 lo, hi = oracle.shard(L, n, j)

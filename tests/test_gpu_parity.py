@@ -315,3 +315,24 @@ def test_warmup_until_stable_stops_where_the_closed_form_says():
     assert steps == t_star, (steps, t_star)
     assert p.gpu.get_step() == (t_star, ob.PHASE_COMPRESS)
     p.close()
+
+
+@pytest.mark.parametrize("numel,n,dtype,bc", [
+    ((1 << 20,), 4, W.F16, True), ((70_001, 33, 0, 5), 3, W.F32, False), ((200_000,), 16, W.BF16, False),
+], ids=["flat_f16_bc", "ragged_f32", "n16_bf16"])
+def test_ec_adam_baseline_then_compression(numel, n, dtype, bc):
+    """The gradient-compression baseline (1-bit EC compression of the gradients, then Adam) against
+    the oracle for several steps, then the variance freeze and compression-stage steps: every phase
+    transition (errors reset at the freeze, Adam's fp32 momentum feeding the first compression step)
+    is compared too."""
+    w = _tiny(numel=numel, n_workers=n, grad_dtype=dtype, warmup_steps=10, seed=121 + n)
+    p = Pair(w, bias_correction=bc)
+    for _ in range(4):
+        p.ec_adam()
+    p.warmup()
+    p.ec_adam()
+    p.freeze()
+    for _ in range(3):
+        p.compress()
+    assert p.stats.scales_exact >= 0.99 * p.stats.scales, p.stats
+    p.close()

@@ -37,11 +37,11 @@ MUTANTS = {
                      "if (v[e] > 0.0f) words[e / 32] |= 1u << (e % 32);"),
     "bit_order_reversed": ("if (v[e] >= 0.0f) words[e / 32] |= 1u << (e % 32);",
                            "if (v[e] >= 0.0f) words[e / 32] |= 1u << (31 - e % 32);"),
-    "update_sign": ("x[p] = x[p] - lr * (m[p] / den[p]);", "x[p] = x[p] + lr * (m[p] / den[p]);"),
-    "variance_not_decayed": ("v[p] = b2 * v[p] + omb2 * (g * g);", "v[p] = v[p] + omb2 * (g * g);"),
+    "update_sign": ("x[p] = x[p] - cfg->lr * (m[p] / den[p]);", "x[p] = x[p] + cfg->lr * (m[p] / den[p]);"),
+    "variance_not_decayed": ("*v = b2 * *v + omb2 * (g * g);", "*v = *v + omb2 * (g * g);"),
     "eps_inside_sqrt": ("den[p] = sqrtf(vu) + cfg->eps;", "den[p] = sqrtf(vu + cfg->eps);"),
     "bias_correction_inverted": ("mh = mh / bc1;", "mh = mh * bc1;"),
-    "broadcast_uncompressed": ("m[p] = bit ? S : -S;", "m[p] = a[p];"),
+    "broadcast_uncompressed": ("bcast[p] = bit ? S : -S;", "bcast[p] = a[p];"),
     "half_exponent_bias": ("mag = ldexpf((float)(1024 + frac), expo - 25);",
                            "mag = ldexpf((float)(1024 + frac), expo - 24);"),
     "bf16_shift": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
@@ -51,6 +51,13 @@ MUTANTS = {
                                       "const float s = wscale[(int64_t)k * n + i];"),
     "warmup_sum_not_averaged": ("const float g = acc / (float)n;", "const float g = acc;"),
     "norm2_without_sqrt": ("  return sqrt(sum + comp);\n}", "  return sum + comp;\n}"),
+    "ec_adam_compresses_momentum": (
+        "c[(int64_t)i * D + p] = ora_grad_value(g, cfg->grad_dtype, e) + delta[(int64_t)i * D + p];",
+        "c[(int64_t)i * D + p] = cfg->beta1 * m[p] + (1.0f - cfg->beta1) * ora_grad_value(g, cfg->grad_dtype, e)"
+        " + delta[(int64_t)i * D + p];"),
+    "ec_adam_update_from_local_gradient": (
+        "for (int64_t p = 0; p < D; ++p) adam_element(cfg, bc1, bc2, bcast[p], &m[p], &v[p], &x[p]);",
+        "for (int64_t p = 0; p < D; ++p) adam_element(cfg, bc1, bc2, c[p], &m[p], &v[p], &x[p]);"),
     "warmup_reads_one_worker": ("acc = acc + ora_grad_value(grads[(int64_t)i * T + k], cfg->grad_dtype, e);",
                                 "acc = acc + ora_grad_value(grads[k], cfg->grad_dtype, e);"),
 }
