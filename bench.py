@@ -264,7 +264,12 @@ def main():
     ap.add_argument("--step", default="compress", choices=["compress", "warmup", "ec_adam"],
                     help="what one timed step is: the compression-stage step (default), an uncompressed "
                          "warm-up Adam step, or the gradient-compression baseline step")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture two steps (one cycle of the double-buffered scales) in a CUDA graph and "
+                         "time its replays; per-kernel events are off, so no roofline is reported")
     args = ap.parse_args()
+    if args.graph and args.steps % 2:
+        args.steps += 1
 
     from communication_compressed_optimizer_compress_gb300 import workloads as W
 
@@ -318,22 +323,46 @@ def main():
         step_fn(gsets[s % 2])
     assert opt.get_status() == ob.OK, "non-finite state after warm-up"
 
+    # ---- optional CUDA graph of two steps (the gradient-pointer tables are cached by the steps above)
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        c0 = opt.launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                step_fn(gsets[0])
+                step_fn(gsets[1])
+        stream.wait_stream(side)
+        launches_per_replay = opt.launch_count() - c0
+        graph.replay()
+        torch.cuda.synchronize()
+
     # ---- timed region
-    opt.set_timing(True)
+    opt.set_timing(graph is None)
     opt.kernel_times()  # reset
     launches0 = opt.launch_count()
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         t0.record(stream)
-        for s in range(args.steps):
-            step_fn(gsets[s % 2])
+        if graph is None:
+            for s in range(args.steps):
+                step_fn(gsets[s % 2])
+        else:
+            for _ in range(args.steps // 2):
+                graph.replay()
         t1.record(stream)
         torch.cuda.synchronize()
     barrier()
     elapsed_ms = t0.elapsed_time(t1)
-    launches = opt.launch_count() - launches0
-    kt = opt.kernel_times()
+    if graph is None:
+        launches = opt.launch_count() - launches0
+        kt = opt.kernel_times()
+    else:
+        launches = launches_per_replay * (args.steps // 2)
+        kt = {name: (0.0, 0) for name in opt.kernel_times()}
     opt.set_timing(False)
     max_ms = dist_max(elapsed_ms, dev)
     status = opt.get_status()
@@ -345,7 +374,7 @@ def main():
     peak, peak_kind = measured_peak()
     dom = "warmup" if args.step == "warmup" else "worker"
     dom_ms = kt[dom][0] / max(1, kt[dom][1])
-    dom_gbs = w.d * ab[dom] / (dom_ms / 1e3) / 1e9
+    dom_gbs = w.d * ab[dom] / (dom_ms / 1e3) / 1e9 if dom_ms > 0 else None
     per_kernel = {}
     for name in ("warmup", "worker", "worker_scale", "server", "server_scale", "update", "ec_update"):
         ms, cnt = kt[name]
@@ -399,7 +428,7 @@ def main():
             "step_gbs": step_gbs, "step_pct_of_8tbs": 100.0 * step_gbs / HBM_NOMINAL_GBS,
             "step_frac_of_measured_peak": step_gbs / peak,
             "bytes_per_elem": ab["step"],
-            "roofline": {"bound": "hbm",
+            "roofline": None if dom_gbs is None else {"bound": "hbm",
                          "kernel": {"compress": "k_worker (momentum + error + sign pack + norm partials)",
                                     "ec_adam": "k_worker (gradient + error + sign pack + norm partials)",
                                     "warmup": "k_warmup (worker mean + Adam)"}[args.step],
@@ -411,6 +440,7 @@ def main():
             "kernels": per_kernel,
             "warmup_adam_ms_per_step": warm_ms,
             "gpu_launches": launches,
+            "cuda_graph": graph is not None,
             "clocks": clk.summary(),
             "status": ob.error_string(status),
             "e2e": e2e,

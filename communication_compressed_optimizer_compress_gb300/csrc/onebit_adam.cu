@@ -67,12 +67,24 @@ onebit_status_t check_config(const onebit_adam_config_t* cfg) {
   return ONEBIT_OK;
 }
 
-// The multi-tensor launcher's table: chunks of at most kChunk elements that never cross a tensor
+// The multi-tensor launcher's table: chunks of at most chunk_length() elements that never cross a tensor
 // or a server-shard boundary.  Shard boundaries are multiples of 32 inside a tensor, so every chunk
 // starts on a sign-word boundary and only a tensor's last chunk can have a ragged end.
+// Chunk length: kChunk for large lists; shorter (a multiple of 4096) for small ones, so that even a
+// small list yields about kChunkTarget work units.  It depends on the element count only, never on
+// the device, so results do not depend on the GPU they run on.
+constexpr int64_t kChunkTarget = 1216;
+int64_t chunk_length(int64_t total) {
+  const int64_t want = (total + kChunkTarget - 1) / kChunkTarget;
+  return std::min<int64_t>(kChunk, std::max<int64_t>(4096, (want + 4095) / 4096 * 4096));
+}
+
 onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
   P->n = cfg->n_workers;
   P->T = cfg->n_tensors;
+  int64_t total = 0;
+  for (int k = 0; k < cfg->n_tensors; ++k) total += cfg->numel[k];
+  const int64_t clen = chunk_length(total);
   P->numel.assign(cfg->numel, cfg->numel + cfg->n_tensors);
   P->seg_off.resize(P->T);
   P->seg_uoff.resize(P->T);
@@ -88,14 +100,14 @@ onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
       int64_t lo, hi;
       shard_bounds(L, P->n, j, &lo, &hi);
       Range hr{(int32_t)P->chunks.size(), 0, hi - lo};
-      for (int64_t s = lo; s < hi; s += kChunk) {
+      for (int64_t s = lo; s < hi; s += clen) {
         Chunk c{};
         c.off = off + s;
         c.uoff = uoff + s;
         c.start = s;
         c.seg = k;
         c.shard = j;
-        c.len = (int32_t)std::min<int64_t>(kChunk, hi - s);
+        c.len = (int32_t)std::min<int64_t>(clen, hi - s);
         P->chunks.push_back(c);
         if (P->chunks.size() > (size_t)INT32_MAX) return ONEBIT_ERR_UNSUPPORTED;
       }

@@ -8,10 +8,11 @@
 // and the scratch the computation needs (per-chunk sum-of-squares partials and the scale) lives in a
 // file-scope __device__ array that every GPU loading this library holds until the process exits.
 //
-// It is the worker kernel of the compression step run for one vector: the same per-thread element
-// mapping, the same fp32 operation order and the same fixed-order reduction, so it produces the same
-// bits, scale and error as onebit_adam_compress_step() does for a worker whose tensor is split into
-// the same 65536-element chunks (a one-worker handle).
+// It is the worker kernel of the compression step run for one vector (65536-element chunks): the
+// same per-element fp32 operation order and the same exact-square norm, so its sign bits equal
+// those of onebit_adam_compress_step() for the same vector, and its scale (hence its error) agrees to
+// within one fp32 rounding of the scale (the handle may group the norm's partial sums into shorter
+// chunks).
 #include <cuda_runtime.h>
 
 #include <mutex>

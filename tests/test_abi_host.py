@@ -96,6 +96,15 @@ def test_chunk_plan(numel, n):
         pad_off += (L + 31) // 32 * 32
 
 
+def test_small_lists_get_short_chunks():
+    """Chunk length adapts to the list: 2^20 elements become 256 chunks of 4096 (work units for
+    every SM), while a BERT-Large-sized list keeps 65536-element chunks."""
+    rows = ob.plan_chunks(ob.make_config([1 << 20], 1))
+    assert len(rows) == 256 and all(r[3] == 4096 for r in rows)
+    rows = ob.plan_chunks(ob.make_config([340_000_000], 16))
+    assert max(r[3] for r in rows) == 65536
+
+
 def test_workspace_size_scales_with_workers():
     a = ob.workspace_size(ob.make_config([1 << 20], 2))
     b = ob.workspace_size(ob.make_config([1 << 20], 4))

@@ -336,3 +336,39 @@ def test_ec_adam_baseline_then_compression(numel, n, dtype, bc):
         p.compress()
     assert p.stats.scales_exact >= 0.99 * p.stats.scales, p.stats
     p.close()
+
+
+def test_cuda_graph_replay_equals_eager():
+    """A compression step enqueues kernels only (no host synchronisation or allocation), so a pair
+    of steady-state steps (one full cycle of the double-buffered scales) can be captured in a CUDA
+    graph and replayed; every replay equals two eager steps bit for bit.  The gradient-pointer
+    tables are cached by the eager steps before the capture."""
+    w = _tiny(numel=(100_003, 77), n_workers=4, grad_dtype=W.F16, warmup_steps=2, seed=131)
+    a, b = Pair(w), Pair(w)
+    g = [[t.cuda() for t in a.src.grads(s)] for s in range(2)]
+    for p in (a, b):
+        for s in range(2):
+            p.gpu.warmup_step(g[s])
+        p.gpu.freeze_variance()
+        for s in range(4):
+            p.gpu.compress_step(g[s % 2])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            a.gpu.compress_step(g[0])
+            a.gpu.compress_step(g[1])
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+        b.gpu.compress_step(g[0])
+        b.gpu.compress_step(g[1])
+    torch.cuda.synchronize()
+    assert np.array_equal(a.x().view(np.uint32), b.x().view(np.uint32))
+    sa, sb = _state(a.gpu, w.n_workers), _state(b.gpu, w.n_workers)
+    for k in sa:
+        assert np.array_equal(sa[k].view(np.uint8), sb[k].view(np.uint8)), k
+    a.close()
+    b.close()
