@@ -247,7 +247,8 @@ def workload_config(w, args):
     return {"workload": desc, "d": w.d, "n_tensors": w.n_tensors, "n_workers": w.n_workers,
             "grad_dtype": W.DTYPE_NAME[w.grad_dtype], "warmup_adam_steps": w.warmup_steps,
             "l2": "inputs larger than L2 (working set per step >> 129 MB); no flush needed",
-            "parallelism": f"replicas x{dist_env()[0]} (workers simulated in one GPU)"}
+            "parallelism": f"replicas x{dist_env()[0]} (workers simulated in one GPU)",
+            "scale_block": getattr(args, "scale_block", 0)}
 
 
 def main():
@@ -267,6 +268,9 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="capture two steps (one cycle of the double-buffered scales) in a CUDA graph and "
                          "time its replays; per-kernel events are off, so no roofline is reported")
+    ap.add_argument("--scale-block", type=int, default=0,
+                    help="per-block scale granularity: every block of this many elements (a multiple of 32) "
+                         "gets its own worker scales and server shards; 0 = per tensor")
     args = ap.parse_args()
     if args.graph and args.steps % 2:
         args.steps += 1
@@ -301,7 +305,7 @@ def main():
     # a timed warm-up step needs room for the untimed and timed warm-up steps before T_w
     tw_handle = w.warmup_steps if args.step == "compress" else args.warmup + args.steps + 1
     opt = ob.OneBitAdam(params, w.n_workers, tw_handle, w.beta1, w.beta2, w.eps, w.lr,
-                        grad_dtype=W.TORCH_DTYPE[w.grad_dtype])
+                        grad_dtype=W.TORCH_DTYPE[w.grad_dtype], scale_block=args.scale_block)
     stream = torch.cuda.current_stream()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)

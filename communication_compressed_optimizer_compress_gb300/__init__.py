@@ -45,6 +45,7 @@ class Config(ctypes.Structure):
         ("numel", ctypes.POINTER(ctypes.c_int64)),
         ("grad_dtype", ctypes.c_int32),
         ("bias_correction", ctypes.c_int32),
+        ("scale_block", ctypes.c_int64),
     ]
 
 
@@ -114,10 +115,11 @@ def _check(status: int, where: str, handle=None):
 
 
 def make_config(numel, n_workers, warmup_steps=1, beta1=0.9, beta2=0.999, eps=1e-8, lr=1e-3,
-                grad_dtype=F32, bias_correction=False):
+                grad_dtype=F32, bias_correction=False, scale_block=0):
     arr = (ctypes.c_int64 * len(numel))(*[int(v) for v in numel])
     cfg = Config(beta1, beta2, eps, lr, int(warmup_steps), int(n_workers), len(numel),
-                 ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64)), int(grad_dtype), int(bool(bias_correction)))
+                 ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64)), int(grad_dtype), int(bool(bias_correction)),
+                 int(scale_block))
     cfg._keep = arr
     return cfg
 
@@ -157,10 +159,13 @@ class OneBitAdam:
     Methods mirror the C ABI: ``warmup_step``, ``freeze_variance``, ``compress_step`` (gradients:
     list of n*T CUDA tensors ordered [worker][tensor]), their ``*_host`` variants (CPU tensors),
     ``get_status``, ``export_state``/``import_state``, ``comm_bytes``, timing helpers and ``free``.
+    ``scale_block`` > 0 (a multiple of 32) gives every block of that many elements of a tensor its
+    own worker scales and server shards (the per-chunk parameter-server form); scale exports are then
+    indexed by block.
     """
 
     def __init__(self, params, n_workers, warmup_steps, beta1=0.9, beta2=0.999, eps=1e-8, lr=1e-3,
-                 grad_dtype=None, bias_correction=False, workspace=None, stream=None):
+                 grad_dtype=None, bias_correction=False, workspace=None, stream=None, scale_block=0):
         import torch
 
         self.params = list(params)
@@ -172,7 +177,8 @@ class OneBitAdam:
         self.numel = [p.numel() for p in self.params]
         gdt = F32 if grad_dtype is None else (grad_dtype if isinstance(grad_dtype, int) else _torch_dtype_code(grad_dtype))
         self.grad_dtype = gdt
-        self.cfg = make_config(self.numel, self.n, warmup_steps, beta1, beta2, eps, lr, gdt, bias_correction)
+        self.cfg = make_config(self.numel, self.n, warmup_steps, beta1, beta2, eps, lr, gdt, bias_correction,
+                               scale_block)
         self.workspace = workspace
         ptrs = (ctypes.c_void_p * self.T)(*[p.data_ptr() for p in self.params])
         h = ctypes.c_void_p()

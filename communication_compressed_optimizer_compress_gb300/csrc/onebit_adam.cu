@@ -31,8 +31,13 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t round32(int64_t v) { return (v + 31) / 32 * 32; }
 
 struct Plan {
-  int n = 0, T = 0;
-  std::vector<int64_t> numel;
+  int n = 0, T = 0;               // T: compressed segments (the tensors, or their scale blocks)
+  std::vector<int64_t> numel;     // [T]
+  int Tu = 0;                     // the caller's tensors
+  std::vector<int64_t> unumel;    // [Tu]
+  std::vector<int32_t> ufirst;    // [Tu+1]: segments of caller tensor k are ufirst[k] .. ufirst[k+1]-1
+  std::vector<int64_t> voff;      // [T]: a segment's first element within its caller tensor
+  bool split = false;             // scale_block > 0
   std::vector<int64_t> seg_off;   // padded offsets
   std::vector<int64_t> seg_uoff;  // unpadded offsets
   int64_t Dp = 0, D = 0, Wp = 0, Wr = 0;  // Wr: worker sign-row stride in words (multiple of 4)
@@ -58,6 +63,7 @@ onebit_status_t check_config(const onebit_adam_config_t* cfg) {
   if (!(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) || !std::isfinite(cfg->lr)) return ONEBIT_ERR_INVALID_ARG;
   if (cfg->warmup_steps < 1) return ONEBIT_ERR_INVALID_ARG;
   if (cfg->bias_correction != 0 && cfg->bias_correction != 1) return ONEBIT_ERR_INVALID_ARG;
+  if (cfg->scale_block < 0 || cfg->scale_block % 32 != 0) return ONEBIT_ERR_INVALID_ARG;
   int64_t total = 0;
   for (int k = 0; k < cfg->n_tensors; ++k) {
     if (cfg->numel[k] < 0) return ONEBIT_ERR_INVALID_ARG;
@@ -81,11 +87,28 @@ int64_t chunk_length(int64_t total) {
 
 onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
   P->n = cfg->n_workers;
-  P->T = cfg->n_tensors;
+  P->Tu = cfg->n_tensors;
+  P->unumel.assign(cfg->numel, cfg->numel + cfg->n_tensors);
+  P->split = cfg->scale_block > 0;
+  // Segments: with a scale block B, tensor k is cut into ceil(L_k/B) blocks (an empty tensor keeps
+  // one empty block) and every block is compressed as a tensor of its own.
   int64_t total = 0;
-  for (int k = 0; k < cfg->n_tensors; ++k) total += cfg->numel[k];
+  P->ufirst.assign(1, 0);
+  for (int k = 0; k < P->Tu; ++k) {
+    const int64_t L = P->unumel[k];
+    total += L;
+    const int64_t B = P->split ? cfg->scale_block : std::max<int64_t>(L, 1);
+    int64_t s = 0;
+    do {
+      P->numel.push_back(std::min<int64_t>(B, L - s));
+      P->voff.push_back(s);
+      s += B;
+    } while (s < L);
+    if ((int64_t)P->numel.size() * P->n > (int64_t)INT32_MAX) return ONEBIT_ERR_UNSUPPORTED;
+    P->ufirst.push_back((int32_t)P->numel.size());
+  }
+  P->T = (int)P->numel.size();
   const int64_t clen = chunk_length(total);
-  P->numel.assign(cfg->numel, cfg->numel + cfg->n_tensors);
   P->seg_off.resize(P->T);
   P->seg_uoff.resize(P->T);
   P->seg_ranges.resize(P->T);
@@ -186,6 +209,7 @@ struct onebit_adam {
   bool serr_zero = true;
   // gradient pointer table ring
   std::vector<std::vector<const void*>> ring;
+  std::vector<const void*> gexp;  // per-segment gradient pointers of the current step (scale blocks)
   int ring_next = 0;
   // host-gradient staging: two device buffers used alternately, so that one step's copies can run
   // while the previous step's kernels still read the other buffer
@@ -338,14 +362,25 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // the vector loads of the kernels.
 onebit_status_t bind_grads(onebit_adam* h, const void* const* grads, cudaStream_t stream, const void* const** dev,
                            bool* vec) {
-  const size_t cnt = (size_t)h->plan.n * h->plan.T;
-  const size_t galign = h->cfg.grad_dtype == ONEBIT_F32 ? 32 : 16;
-  bool ok = true;
-  for (size_t q = 0; q < cnt; ++q) {
-    const int k = (int)(q % h->plan.T);
-    if (!grads[q] && h->plan.numel[k] > 0) return ONEBIT_ERR_INVALID_ARG;
-    if (!aligned(grads[q], galign)) ok = false;
+  const Plan& P = h->plan;
+  const size_t cnt = (size_t)P.n * P.T;
+  const size_t gb = h->cfg.grad_dtype == ONEBIT_F32 ? 4 : 2;
+  for (size_t q = 0; q < (size_t)P.n * P.Tu; ++q)
+    if (!grads[q] && P.unumel[q % P.Tu] > 0) return ONEBIT_ERR_INVALID_ARG;
+  if (P.split) {  // one pointer per segment: its caller tensor's pointer advanced to the block
+    h->gexp.resize(cnt);
+    for (int i = 0; i < P.n; ++i)
+      for (int k = 0; k < P.Tu; ++k) {
+        const uint8_t* g = static_cast<const uint8_t*>(grads[(size_t)i * P.Tu + k]);
+        for (int v = P.ufirst[k]; v < P.ufirst[k + 1]; ++v)
+          h->gexp[(size_t)i * P.T + v] = g ? g + P.voff[v] * gb : nullptr;
+      }
+    grads = h->gexp.data();
   }
+  const size_t galign = gb == 4 ? 32 : 16;
+  bool ok = true;
+  for (size_t q = 0; q < cnt; ++q)
+    if (!aligned(grads[q], galign)) ok = false;
   *vec = ok;
   const void** base = h->at<const void*>(h->lay.gptr);
   for (int r = 0; r < kPtrRing; ++r) {
@@ -529,16 +564,18 @@ onebit_status_t export_m(onebit_adam* h, float* dst, cudaStream_t st) {
 // buffer index (to be marked free once the step that reads it is enqueued: release_stage()).
 onebit_status_t stage_copy(onebit_adam* h, const void* const* host_grads, cudaStream_t st,
                            std::vector<const void*>* dev, int* idx_out) {
-  const int n = h->plan.n, T = h->plan.T;
+  // copies follow the caller's tensors; bind_grads() cuts them into segments afterwards
+  const int n = h->plan.n, T = h->plan.Tu;
+  const std::vector<int64_t>& numel = h->plan.unumel;
   const size_t gb = h->cfg.grad_dtype == ONEBIT_F32 ? 4 : 2;
   if (!host_grads) return ONEBIT_ERR_INVALID_ARG;
   for (int i = 0; i < n; ++i)
     for (int k = 0; k < T; ++k)
-      if (h->plan.numel[k] > 0 && !host_grads[(size_t)i * T + k]) return ONEBIT_ERR_INVALID_ARG;
+      if (numel[k] > 0 && !host_grads[(size_t)i * T + k]) return ONEBIT_ERR_INVALID_ARG;
   if (!h->staging[0]) {
     size_t bytes = 0;
     for (int i = 0; i < n; ++i)
-      for (int k = 0; k < T; ++k) bytes += align_up(h->plan.numel[k] * gb, kAlign);
+      for (int k = 0; k < T; ++k) bytes += align_up(numel[k] * gb, kAlign);
     for (int b = 0; b < 2; ++b) {
       if (cudaMalloc(&h->staging[b], std::max<size_t>(bytes, 1)) != cudaSuccess) {
         cudaGetLastError();
@@ -563,7 +600,7 @@ onebit_status_t stage_copy(onebit_adam* h, const void* const* host_grads, cudaSt
   int r = 0;
   for (int i = 0; i < n; ++i)
     for (int k = 0; k < T; ++k) {
-      const size_t bytes = h->plan.numel[k] * gb;
+      const size_t bytes = numel[k] * gb;
       const size_t q = (size_t)i * T + k;
       (*dev)[q] = base + off;
       const uint8_t* src = static_cast<const uint8_t*>(host_grads[q]);
@@ -679,7 +716,10 @@ onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* 
     }
     h->ws_owned = true;
   }
-  h->params.assign(params, params + cfg->n_tensors);
+  h->params.resize(h->plan.T);
+  for (int k = 0; k < h->plan.Tu; ++k)
+    for (int v = h->plan.ufirst[k]; v < h->plan.ufirst[k + 1]; ++v)
+      h->params[v] = params[k] ? params[k] + h->plan.voff[v] : nullptr;
   h->params_aligned = true;
   for (float* p : h->params)
     if (!aligned(p, 32)) h->params_aligned = false;

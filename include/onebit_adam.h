@@ -79,8 +79,8 @@ typedef enum {
   ONEBIT_STATE_SERVER_ERROR = 3,  /* eps_srv: D fp32 */
   ONEBIT_STATE_WORKER_BITS = 4,   /* last message of one worker: W uint32 (export only) */
   ONEBIT_STATE_SERVER_BITS = 5,   /* last broadcast: W uint32 (export only) */
-  ONEBIT_STATE_WORKER_SCALES = 6, /* last worker scales: n*T fp32, [worker][tensor] (export only) */
-  ONEBIT_STATE_SERVER_SCALES = 7  /* last server scales: T*n fp32, [tensor][shard] (export only) */
+  ONEBIT_STATE_WORKER_SCALES = 6, /* last worker scales: n*T fp32, [worker][tensor or block] (export only) */
+  ONEBIT_STATE_SERVER_SCALES = 7  /* last server scales: T*n fp32, [tensor or block][shard] (export only) */
 } onebit_state_t;
 
 /* The kernels, for onebit_adam_kernel_times(). */
@@ -108,6 +108,16 @@ typedef struct {
   const int64_t* numel;    /* host array [T], L_k >= 0, sum L_k >= 1 */
   int32_t grad_dtype;      /* onebit_dtype_t */
   int32_t bias_correction; /* 0: the pages' formulas (default); 1: Kingma-Ba bias correction */
+  int64_t scale_block;     /* scale granularity.  0 (default): one worker scale per tensor and n
+                            * server shards per tensor.  B > 0, a multiple of 32: the per-chunk
+                            * parameter-server form of Tang et al. Sec. 11 -- every tensor is cut
+                            * into blocks of B elements (the last may be shorter; an empty tensor
+                            * keeps one empty block) and each block is compressed as a tensor of its
+                            * own, with its own worker scales and its own n server shards.  The
+                            * scale exports and onebit_adam_plan_chunks() then index blocks, tensor
+                            * k's blocks in order after those of tensor k-1; gradients, parameters
+                            * and every per-element state keep the caller's tensor layout.  Any other
+                            * value is ONEBIT_ERR_INVALID_ARG. */
 } onebit_adam_config_t;
 
 /* Bytes of device workspace a config needs (256-byte aligned pieces included). */

@@ -205,18 +205,38 @@ def compress(c):
 
 # ---------------------------------------------------------------- the optimizer
 
+def scale_blocks(numel, block):
+    """Sizes of the compressed segments: the tensors themselves (block 0), or each tensor cut into
+    consecutive blocks of ``block`` elements, the last one shorter, an empty tensor one empty block."""
+    if not block:
+        return [int(v) for v in numel]
+    out = []
+    for L in numel:
+        L = int(L)
+        out.extend([min(block, L - s) for s in range(0, L, block)] if L else [0])
+    return out
+
+
 class OneBitAdamOracle:
     """Whole optimizer state on the host, stepped by the C oracle.
 
     ``numel``: list of tensor sizes (one entry = one flat buffer).  Per-element arrays are the
     concatenation of the tensors.  Gradients are passed per step as a list of n*T numpy arrays
     ordered [worker][tensor]: float32 arrays, float16 arrays, or uint16 arrays of bfloat16 bits.
+
+    ``scale_block`` B > 0 is the per-chunk parameter-server form ("1-bit Adam ...", Sec. 11: the
+    server role is taken per chunk): every tensor is cut into consecutive blocks of B elements (the
+    last one shorter; an empty tensor stays one empty block) and each block is compressed as a tensor
+    of its own.  ``numel``, ``T`` and the scale arrays then describe the blocks; gradients are still
+    passed per caller tensor (``unumel``).
     """
 
     def __init__(self, numel, n_workers, x0, beta1=0.9, beta2=0.999, eps=1e-8, lr=1e-3,
-                 grad_dtype=F32, bias_correction=False, lib: OracleLib | None = None):
+                 grad_dtype=F32, bias_correction=False, lib: OracleLib | None = None, scale_block=0):
         self.lib = lib if lib is not None else globals()["lib"]()
-        self.numel = [int(v) for v in numel]
+        self.unumel = [int(v) for v in numel]
+        self.scale_block = int(scale_block)
+        self.numel = scale_blocks(self.unumel, self.scale_block)
         self.n = int(n_workers)
         self.T = len(self.numel)
         self.D = sum(self.numel)
@@ -243,6 +263,15 @@ class OneBitAdamOracle:
         self.phase = "warmup"
 
     def _grad_ptrs(self, grads):
+        if self.scale_block:  # cut each caller tensor's gradient into its blocks
+            Tu, B = len(self.unumel), self.scale_block
+            assert len(grads) == self.n * Tu
+            cut = []
+            for i in range(self.n):
+                for k, L in enumerate(self.unumel):
+                    g = np.ascontiguousarray(grads[i * Tu + k])
+                    cut.extend([g[s: s + B] for s in range(0, L, B)] if L else [g])
+            grads = cut
         assert len(grads) == self.n * self.T
         keep = []
         ptrs = (ctypes.c_void_p * len(grads))()

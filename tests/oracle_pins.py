@@ -507,6 +507,98 @@ def pin_tensors_are_independent(ora):
         assert np.array_equal(whole.sscale[k], p.sscale[0])
 
 
+def pin_scale_blocks_lossless_on_blockwise_magnitudes(ora):
+    """Per-chunk scale granularity ("1-bit Adam ...", Sec. 11: compression per chunk).  When every
+    block of B elements holds one magnitude (random signs), a per-block scale sends it exactly: the
+    worker and server errors stay 0, every scale equals that block's |c|, and the update is the
+    uncompressed momentum step.  The same input with one scale per tensor is lossy."""
+    import oracle as _o
+    numel, B, n = [224, 0, 96], 64, 2
+    assert _o.scale_blocks(numel, B) == [64, 64, 64, 32, 0, 64, 32]
+    assert _o.scale_blocks(numel, 0) == numel
+    rng = np.random.default_rng(21)
+    D = sum(numel)
+    x0 = (rng.standard_normal(D) * 0.1).astype(np.float32)
+    b1, lr = np.float32(0.75), np.float32(0.5)
+    mags = np.float32(2.0) ** np.arange(-6, 1).astype(np.float32)  # one per block
+    blk_of = np.concatenate([np.full(L, b) for b, L in enumerate(_o.scale_blocks(numel, B))]).astype(int)
+    g = (mags[blk_of] * np.where(rng.random(D) < 0.5, -1, 1)).astype(np.float32)
+    offs = np.concatenate([[0], np.cumsum(numel)]).astype(int)
+    per_tensor = [g[offs[k]: offs[k + 1]] for k in range(len(numel))]
+    zeros = [np.zeros(L, np.float32) for L in numel]
+    results = {}
+    for blk in (B, 0):
+        o = ora.optimizer(numel, n, x0, beta1=b1, eps=1.0, lr=lr, scale_block=blk)
+        o.warmup_step(zeros * n)         # m = v = 0, so den = 0 + eps = 1 after the freeze
+        o.freeze()
+        o.compress_step(per_tensor * n)  # identical workers
+        results[blk] = o
+    o = results[B]
+    c = (np.float32(1) - b1) * g
+    assert np.all(o.view("delta") == 0) and np.all(o.view("eps_srv") == 0)
+    for b, L in enumerate(_o.scale_blocks(numel, B)):
+        want = np.float32((np.float32(1) - b1) * mags[b]) if L else np.float32(0)
+        assert o.wscale[0, b] == want and o.wscale[1, b] == want
+        for j in range(n):
+            lo, hi = ora.shard(L, n, j)
+            assert o.sscale[b, j] == (want if hi > lo else 0)
+    assert np.array_equal(o.view("m"), c)
+    assert np.array_equal(o.view("x"), x0 - lr * c)
+    assert np.abs(results[0].view("delta")).max() > 0.1 * np.abs(c).max()
+
+
+def pin_scale_block_larger_than_tensors_is_per_tensor(ora):
+    """A block at least as long as every tensor leaves each tensor one block: the per-tensor method."""
+    rng = np.random.default_rng(22)
+    numel, n = [40, 0, 200, 7], 3
+    D = sum(numel)
+    x0 = (rng.standard_normal(D) * 0.05).astype(np.float32)
+    a = ora.optimizer(numel, n, x0)
+    b = ora.optimizer(numel, n, x0, scale_block=256)
+    assert b.numel == numel
+    offs = np.concatenate([[0], np.cumsum(numel)]).astype(int)
+    for step in range(6):
+        gf = [(rng.standard_normal(D) * 1e-2).astype(np.float32) for _ in range(n)]
+        gs = [gf[i][offs[k]: offs[k + 1]] for i in range(n) for k in range(len(numel))]
+        for o in (a, b):
+            if step < 2:
+                o.warmup_step(gs)
+            else:
+                o.compress_step(gs)
+            if step == 1:
+                o.freeze()
+    for name in ("x", "m", "delta", "eps_srv", "wbits", "sbits", "wscale", "sscale"):
+        assert np.array_equal(a.view(name), b.view(name)), name
+
+
+def pin_scale_blocks_equal_presplit_tensors(ora):
+    """Cutting tensors into blocks inside the optimizer equals handing it the blocks as separate
+    tensors (random data, ragged blocks, several workers and steps): the blocking is only a view."""
+    rng = np.random.default_rng(23)
+    numel, B, n = [300, 5, 0, 129], 64, 3
+    import oracle as _o
+    blocks = _o.scale_blocks(numel, B)
+    D = sum(numel)
+    x0 = (rng.standard_normal(D) * 0.05).astype(np.float32)
+    a = ora.optimizer(numel, n, x0, scale_block=B)
+    b = ora.optimizer(blocks, n, x0)
+    offs = np.concatenate([[0], np.cumsum(numel)]).astype(int)
+    boffs = np.concatenate([[0], np.cumsum(blocks)]).astype(int)
+    for step in range(6):
+        gf = [(rng.standard_normal(D) * 1e-2).astype(np.float32) for _ in range(n)]
+        ga = [gf[i][offs[k]: offs[k + 1]] for i in range(n) for k in range(len(numel))]
+        gb = [gf[i][boffs[k]: boffs[k + 1]] for i in range(n) for k in range(len(blocks))]
+        for o, gs in ((a, ga), (b, gb)):
+            if step < 2:
+                o.warmup_step(gs)
+            else:
+                o.compress_step(gs)
+            if step == 1:
+                o.freeze()
+    for name in ("x", "m", "delta", "eps_srv", "wbits", "sbits", "wscale", "sscale"):
+        assert np.array_equal(a.view(name), b.view(name)), name
+
+
 def pin_ec_adam_lossless_is_adam(ora):
     """Baseline of Sec. 3.2 (1-bit EC compression of the gradients, then Adam): when every worker's
     gradient has equal magnitudes and all share one sign pattern, worker and server compression are

@@ -68,7 +68,7 @@ def _bits(words, D, offs, woffs, numel):
 class Pair:
     """A CUDA optimizer and an oracle optimizer stepped in lock-free parallel on the same inputs."""
 
-    def __init__(self, w: W.Workload, device="cuda:0", bias_correction=False, misalign=False):
+    def __init__(self, w: W.Workload, device="cuda:0", bias_correction=False, misalign=False, scale_block=0):
         self.w = w
         self.dev = torch.device(device)
         self.src = W.GradSource(w, "cpu")
@@ -84,11 +84,12 @@ class Pair:
             self.params = [p.to(self.dev) for p in x0]
         gdt = W.TORCH_DTYPE[w.grad_dtype]
         self.gpu = ob.OneBitAdam(self.params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr,
-                                 grad_dtype=gdt, bias_correction=bias_correction)
+                                 grad_dtype=gdt, bias_correction=bias_correction, scale_block=scale_block)
         x0_np = torch.cat(x0).numpy() if sum(w.numel) else np.zeros(0, np.float32)
         self.ora = oracle.OneBitAdamOracle(list(w.numel), w.n_workers, x0_np, w.beta1, w.beta2, w.eps, w.lr,
-                                           grad_dtype=w.grad_dtype, bias_correction=bias_correction)
-        self.numel = list(w.numel)
+                                           grad_dtype=w.grad_dtype, bias_correction=bias_correction,
+                                           scale_block=scale_block)
+        self.numel = list(self.ora.numel)  # the compressed segments: tensors, or their scale blocks
         self.D = sum(self.numel)
         self.offs = np.concatenate([[0], np.cumsum(self.numel)]).astype(np.int64)
         self.woffs = np.concatenate([[0], np.cumsum([(L + 31) // 32 for L in self.numel])]).astype(np.int64)

@@ -48,6 +48,7 @@ def test_error_strings():
     (dict(numel=[0]), "empty"), (dict(numel=[-1, 5]), "negative"), (dict(n_workers=0), "n=0"),
     (dict(n_workers=257), "n too large"), (dict(beta1=1.0), "beta1"), (dict(beta2=-0.1), "beta2"),
     (dict(eps=-1.0), "eps"), (dict(warmup_steps=0), "T_w"), (dict(grad_dtype=3), "dtype"),
+    (dict(scale_block=-32), "negative block"), (dict(scale_block=48), "block not a multiple of 32"),
 ])
 def test_config_validation(kw, bad):
     base = dict(numel=[100], n_workers=2, warmup_steps=1)
@@ -94,6 +95,33 @@ def test_chunk_plan(numel, n):
             pos += length
         assert pos == L
         pad_off += (L + 31) // 32 * 32
+
+
+@pytest.mark.parametrize("numel,n,block", [([224, 0, 96], 2, 64), ([5000, 37], 20, 32), ([1 << 20], 4, 4096),
+                                            ([65536 * 3 + 17, 5], 3, 96), ([100], 4, 1 << 20)])
+def test_chunk_plan_scale_blocks(numel, n, block):
+    """With a scale block, the plan's segments are the blocks of the oracle's blocking rule: chunks
+    tile every block once, never cross that block's server shards, and keep the caller's padded
+    element offsets (blocks are multiples of 32, so only a tensor's last block can be ragged)."""
+    blocks = oracle.scale_blocks(numel, block)
+    rows = ob.plan_chunks(ob.make_config(numel, n, scale_block=block))
+    by_block = {b: [] for b in range(len(blocks))}
+    for (b, j, start, length, off) in rows:
+        by_block[b].append((j, start, length, off))
+    pad_starts, pad_off = [], 0
+    for L in numel:
+        pad_starts.extend(pad_off + s for s in (range(0, L, block) if L else [0]))
+        pad_off += (L + 31) // 32 * 32
+    assert len(pad_starts) == len(blocks)
+    for b, L in enumerate(blocks):
+        pos = 0
+        for (j, start, length, off) in by_block[b]:
+            assert start == pos
+            lo, hi = oracle.shard(L, n, j)
+            assert lo <= start and start + length <= hi
+            assert off == pad_starts[b] + start
+            pos += length
+        assert pos == L
 
 
 def test_small_lists_get_short_chunks():

@@ -338,6 +338,27 @@ def test_ec_adam_baseline_then_compression(numel, n, dtype, bc):
     p.close()
 
 
+@pytest.mark.parametrize("numel,n,dtype,block", [
+    ((1 << 20,), 4, W.F32, 4096), ((70_001, 33, 0, 5), 3, W.F16, 96), ((200_000, 1000), 16, W.BF16, 65536),
+    ((5000,), 20, W.F32, 32),
+], ids=["flat_f32_b4096", "ragged_f16_b96", "n16_bf16_b65536", "n20_b32"])
+def test_scale_blocks(numel, n, dtype, block):
+    """Per-chunk scale granularity: every block of `block` elements has its own worker scales and
+    server shards.  Blocks shorter than n*32 leave empty shards (block 96 with n = 3 is three shards
+    of 32; block 32 with n = 20 is one non-empty shard and 19 empty ones), and the last block of a
+    tensor is ragged."""
+    w = _tiny(numel=numel, n_workers=n, grad_dtype=dtype, warmup_steps=2, compress_steps=4, seed=141 + n)
+    p = Pair(w, scale_block=block)
+    T_blocks = len(p.numel)
+    st = p.run()
+    assert p.gpu.export_state(ob.STATE_WORKER_SCALES).numel() == n * T_blocks
+    assert st.scales_exact >= 0.99 * st.scales, st
+    ws = p.gpu.export_state(ob.STATE_WORKER_SCALES).cpu().numpy().reshape(n, T_blocks)
+    if T_blocks > len(numel):  # the scales really are per block
+        assert len(np.unique(ws[0])) > 1
+    p.close()
+
+
 def test_cuda_graph_replay_equals_eager():
     """A compression step enqueues kernels only (no host synchronisation or allocation), so a pair
     of steady-state steps (one full cycle of the double-buffered scales) can be captured in a CUDA
