@@ -323,7 +323,15 @@ def main():
         step_fn = opt.warmup_step
     else:
         step_fn = opt.ec_adam_step
+    first_ms = None
     for s in range(max(3, args.warmup)):
+        if s == 0 and args.step == "compress":  # the first step after the freeze reads the fp32 m
+            t0.record(stream)
+            step_fn(gsets[0])
+            t1.record(stream)
+            torch.cuda.synchronize()
+            first_ms = t0.elapsed_time(t1)
+            continue
         step_fn(gsets[s % 2])
     assert opt.get_status() == ob.OK, "non-finite state after warm-up"
 
@@ -349,18 +357,28 @@ def main():
     launches0 = opt.launch_count()
     barrier()
     torch.cuda.synchronize()
+    n_marks = args.steps if graph is None else args.steps // 2
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_marks)]
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         t0.record(stream)
         if graph is None:
             for s in range(args.steps):
                 step_fn(gsets[s % 2])
+                marks[s].record(stream)
         else:
-            for _ in range(args.steps // 2):
+            for r in range(args.steps // 2):
                 graph.replay()
+                marks[r].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
     barrier()
     elapsed_ms = t0.elapsed_time(t1)
+    per_mark = args.steps / n_marks
+    step_times = sorted([t0.elapsed_time(marks[0]) / per_mark] +
+                        [marks[i - 1].elapsed_time(marks[i]) / per_mark for i in range(1, n_marks)])
+
+    def pct(q):
+        return step_times[min(len(step_times) - 1, int(q * (len(step_times) - 1) + 0.5))]
     if graph is None:
         launches = opt.launch_count() - launches0
         kt = opt.kernel_times()
@@ -443,6 +461,8 @@ def main():
                          "bytes_per_elem": ab[dom], "elems_per_launch": w.d},
             "kernels": per_kernel,
             "warmup_adam_ms_per_step": warm_ms,
+            "step_ms_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
+            "first_compress_step_ms": first_ms,
             "gpu_launches": launches,
             "cuda_graph": graph is not None,
             "clocks": clk.summary(),

@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
 // its own copies still in flight (bounded again) before the block ends.
 
 constexpr int kTile = 4096;                 // elements per tile (two groups per consumer thread)
-constexpr int kStages = 3;
+constexpr int kStages = 2;                 // two stages leave room for three CTAs per SM
 constexpr int kStageMaxWorkers = 32;
 constexpr int kRowBytes = kTile / 8 + 32;   // a 16-byte aligned window around the tile's sign bytes
 constexpr int kConsumerWarps = kThreads / 32;
