@@ -430,9 +430,23 @@ def main():
         t1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = dist_max(t0.elapsed_time(t1), dev)
+        # the host link itself: one pinned 1 GiB host-to-device copy, best of 3
+        probe_h = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+        probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+        link_ms = []
+        for _ in range(3):
+            t0.record(stream)
+            probe_d.copy_(probe_h, non_blocking=True)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            link_ms.append(t0.elapsed_time(t1))
+        link_gbs = (1 << 30) / (min(link_ms) / 1e3) / 1e9
+        del probe_h, probe_d
         e2e = {"value": world * w.d * e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 4,
                "ms_per_step": e2e_ms / e2e_steps,
+               "link_h2d_gbs": link_gbs,
+               "frac_of_link": h2d / (e2e_ms / e2e_steps / 1e3) / 1e9 / link_gbs,
                "path": "onebit_adam_compress_step_host (pinned host grads) + D2H of the server scales"}
         del host
 
