@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
             "onebit_adam_kernel_times": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)],
             "onebit_adam_launch_count": [vp, ctypes.POINTER(i64)],
             "onebit_adam_plan_chunks": [cfgp, ctypes.POINTER(i64), i64, ctypes.POINTER(i64)],
+            "onebit_adam_plan_worker_chunks": [cfgp, ctypes.POINTER(i64), i64, ctypes.POINTER(i64)],
             "onebit_adam_set_fault_injection": [vp, i32, i64],
             "onebit_adam_set_variance_monitor": [vp, i32],
             "onebit_adam_variance_norm": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)],
@@ -138,6 +139,18 @@ def plan_chunks(cfg: Config):
     _check(lib().onebit_adam_plan_chunks(ctypes.byref(cfg), rows, count.value, ctypes.byref(count)),
            "onebit_adam_plan_chunks")
     return [tuple(rows[5 * q: 5 * q + 5]) for q in range(count.value)]
+
+
+def plan_worker_chunks(cfg: Config):
+    """The worker kernel's chunk table: list of (tensor, first shard, start, length, padded offset,
+    shard length when the chunk holds several shards else 0)."""
+    count = ctypes.c_int64()
+    _check(lib().onebit_adam_plan_worker_chunks(ctypes.byref(cfg), None, 0, ctypes.byref(count)),
+           "onebit_adam_plan_worker_chunks")
+    rows = (ctypes.c_int64 * (6 * max(count.value, 1)))()
+    _check(lib().onebit_adam_plan_worker_chunks(ctypes.byref(cfg), rows, count.value, ctypes.byref(count)),
+           "onebit_adam_plan_worker_chunks")
+    return [tuple(rows[6 * q: 6 * q + 6]) for q in range(count.value)]
 
 
 def _torch_dtype_code(dt) -> int:

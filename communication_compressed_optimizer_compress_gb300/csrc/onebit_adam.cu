@@ -44,6 +44,11 @@ struct Plan {
   std::vector<Chunk> chunks;
   std::vector<Range> seg_ranges;    // [T]
   std::vector<Range> shard_ranges;  // [T*n]
+  std::vector<Chunk> wchunks;       // worker-side chunks (never cross a tensor; may span shards)
+  std::vector<Range> wseg_ranges;   // [T]
+  int32_t max_wseg_count = 0, max_shard_count = 0;
+  bool worker_spans = false;  // some worker chunk holds several shards
+  bool contig = false;        // server kernels walk contiguous runs (see make_plan)
 };
 
 // Server shard j of a tensor of L elements: [j*S, min((j+1)*S, L)), S = 32*ceil(L/(32n)).
@@ -112,6 +117,7 @@ onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
   P->seg_off.resize(P->T);
   P->seg_uoff.resize(P->T);
   P->seg_ranges.resize(P->T);
+  P->wseg_ranges.resize(P->T);
   P->shard_ranges.resize((size_t)P->T * P->n);
   int64_t off = 0, uoff = 0;
   for (int k = 0; k < P->T; ++k) {
@@ -139,19 +145,54 @@ onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
     }
     sr.count = (int32_t)P->chunks.size() - sr.first;
     P->seg_ranges[k] = sr;
+    // Worker-side chunks.  With shards at least a chunk long they are the server-side chunks.  With
+    // shorter shards a worker chunk holds as many whole shards as fit in chunk_length() elements, so
+    // that the worker kernel's units stay long; such a chunk records the shard length, and each of
+    // its groups finds its own shard from its offset inside the chunk.
+    const int64_t per = 32 * ((L + 32 * (int64_t)P->n - 1) / (32 * (int64_t)P->n));
+    Range wr{(int32_t)P->wchunks.size(), 0, L};
+    if (per >= clen) {
+      P->wchunks.insert(P->wchunks.end(), P->chunks.begin() + sr.first, P->chunks.begin() + sr.first + sr.count);
+    } else if (L > 0) {
+      const int64_t step = clen / per * per;
+      for (int64_t s = 0; s < L; s += step) {
+        Chunk c{};
+        c.off = off + s;
+        c.uoff = uoff + s;
+        c.start = s;
+        c.seg = k;
+        c.len = (int32_t)std::min<int64_t>(step, L - s);
+        c.shard = (int32_t)(s / per);
+        c.per = c.len > per ? (int32_t)per : 0;
+        P->wchunks.push_back(c);
+      }
+    }
+    if (P->wchunks.size() > (size_t)INT32_MAX) return ONEBIT_ERR_UNSUPPORTED;
+    wr.count = (int32_t)P->wchunks.size() - wr.first;
+    P->wseg_ranges[k] = wr;
+    P->max_wseg_count = std::max(P->max_wseg_count, wr.count);
+    for (int j = 0; j < P->n; ++j)
+      P->max_shard_count = std::max(P->max_shard_count, P->shard_ranges[(size_t)k * P->n + j].count);
     off += round32(L);
     uoff += L;
   }
   P->Dp = off;
   P->D = uoff;
+  for (const Chunk& c : P->wchunks) P->worker_spans |= c.per != 0;
+  // The server rebuilds its sum tables (about 2^min(n,12) entries) whenever a CTA moves to another
+  // tensor.  Striding over the chunks, that happens at nearly every chunk once tensors are shorter
+  // than a grid's worth of chunks.  When those rebuilds would cost more than about 5% of the
+  // elements, the register variant of the server kernel walks contiguous runs of chunks instead.
+  const int64_t table = (int64_t(1) << std::min(P->n, 12)) + (P->n > 12 ? 512 : 0);
+  P->contig = P->T > 1 && table * (int64_t)P->chunks.size() * 20 > P->D;
   P->Wp = off / 32;
   P->Wr = (P->Wp + 3) / 4 * 4;
   return ONEBIT_OK;
 }
 
 struct Layout {
-  size_t m, v, a, c, wbits, sbits, wscale, sscale, wpart, spart, chunks, seg_ranges, shard_ranges, gptr, pptr,
-      status, total;
+  size_t m, v, a, c, wbits, sbits, wscale, sscale, wpart, spart, chunks, seg_ranges, shard_ranges, wchunks,
+      wseg_ranges, gptr, pptr, status, total;
 };
 
 Layout make_layout(const Plan& P) {
@@ -171,11 +212,13 @@ Layout make_layout(const Plan& P) {
   L.sbits = take(P.Wp * 4);
   L.wscale = take(2 * n * T * 4);
   L.sscale = take(2 * n * T * 4);
-  L.wpart = take(n * C * 8);
+  L.wpart = take(n * P.wchunks.size() * 8);
   L.spart = take(C * 8);
   L.chunks = take(C * sizeof(Chunk));
   L.seg_ranges = take(T * sizeof(Range));
   L.shard_ranges = take(T * n * sizeof(Range));
+  L.wchunks = take(P.wchunks.size() * sizeof(Chunk));
+  L.wseg_ranges = take(T * sizeof(Range));
   L.gptr = take(kPtrRing * n * T * sizeof(void*));
   L.pptr = take(T * sizeof(void*));
   L.status = take(256);
@@ -317,10 +360,15 @@ StepArgs base_args(onebit_adam* h) {
   StepArgs A{};
   A.chunks = h->at<Chunk>(L.chunks);
   A.n_chunks = (int32_t)P.chunks.size();
+  A.wchunks = h->at<Chunk>(L.wchunks);
+  A.n_wchunks = (int32_t)P.wchunks.size();
+  A.wseg_ranges = h->at<Range>(L.wseg_ranges);
   A.n = P.n;
   A.T = P.T;
   A.pow2 = (P.n & (P.n - 1)) == 0;
   A.Dp = P.Dp;
+  A.D = P.D;
+  A.contig = P.contig ? 1 : 0;
   A.Wp = P.Wp;
   A.Wr = P.Wr;
   A.pptr = h->at<float*>(L.pptr);
@@ -414,7 +462,7 @@ onebit_status_t run_warmup(onebit_adam* h, StepArgs A, bool vec, cudaStream_t st
 
 template <typename GT, int DM, bool HE>
 onebit_status_t run_worker_v(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
-  const int64_t units = (int64_t)A.n_chunks * A.n;
+  const int64_t units = (int64_t)A.n_wchunks * A.n;
   if (vec) {
     auto k = k_worker<GT, DM, HE, true>;
     return launch(h, ONEBIT_K_WORKER, k, grid_for(h, (const void*)k, kThreads, units), kThreads, st, A);
@@ -428,11 +476,19 @@ onebit_status_t run_worker(onebit_adam* h, const StepArgs& A, bool vec, cudaStre
   const bool he = !h->werr_zero;
   if (grad_only) return he ? run_worker_v<GT, kMomNone, true>(h, A, vec, st) : run_worker_v<GT, kMomNone, false>(h, A, vec, st);
   if (h->m_dense) return he ? run_worker_v<GT, kMomDense, true>(h, A, vec, st) : run_worker_v<GT, kMomDense, false>(h, A, vec, st);
+  if (h->plan.worker_spans)
+    return he ? run_worker_v<GT, kMomBitsShards, true>(h, A, vec, st) : run_worker_v<GT, kMomBitsShards, false>(h, A, vec, st);
   return he ? run_worker_v<GT, kMomBits, true>(h, A, vec, st) : run_worker_v<GT, kMomBits, false>(h, A, vec, st);
 }
 
 template <bool HE>
 onebit_status_t run_server_v(onebit_adam* h, const StepArgs& A, cudaStream_t st) {
+  if (A.contig) {
+    // many short tensors: the register variant over contiguous runs of chunks, so that the sum
+    // tables are rebuilt once per tensor and CTA
+    auto k = k_server<HE, true>;
+    return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+  }
   if (A.n <= kStageMaxWorkers) {
     // shared-memory staged variant: the tiles of a and the n sign rows arrive by bulk copies
     auto k = k_server_staged<HE>;
@@ -446,7 +502,7 @@ onebit_status_t run_server_v(onebit_adam* h, const StepArgs& A, cudaStream_t st)
     return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kStagedThreads, A.n_chunks, dyn), kStagedThreads,
                   st, A, dyn);
   }
-  auto k = k_server<HE>;
+  auto k = k_server<HE, false>;
   return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
 }
 
@@ -500,9 +556,19 @@ onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream
   }
   if (s) return s;
   const int nt = h->plan.n * h->plan.T;
-  if ((s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale, nt, kScaleThreads, st, A))) return s;
+  // many short ranges: one warp per scale; otherwise one CTA per scale
+  constexpr int kPerCta = kScaleThreads / 32;
+  if (h->plan.max_wseg_count <= kWarpScaleMax)
+    s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale_warp, (nt + kPerCta - 1) / kPerCta, kScaleThreads, st, A);
+  else
+    s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale, nt, kScaleThreads, st, A);
+  if (s) return s;
   if ((s = run_server(h, A, st))) return s;
-  if ((s = launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale, nt, kScaleThreads, st, A))) return s;
+  if (h->plan.max_shard_count <= kWarpScaleMax)
+    s = launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale_warp, (nt + kPerCta - 1) / kPerCta, kScaleThreads, st, A);
+  else
+    s = launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale, nt, kScaleThreads, st, A);
+  if (s) return s;
   if (ec_adam) {
     const int64_t t = h->t + 1;
     A.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, (double)t));
@@ -675,6 +741,26 @@ onebit_status_t onebit_adam_plan_chunks(const onebit_adam_config_t* cfg, int64_t
   return ONEBIT_OK;
 }
 
+onebit_status_t onebit_adam_plan_worker_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap,
+                                               int64_t* count) {
+  if (!count || (cap > 0 && !rows)) return ONEBIT_ERR_INVALID_ARG;
+  onebit_status_t s = check_config(cfg);
+  if (s) return s;
+  Plan P;
+  if ((s = make_plan(cfg, &P))) return s;
+  *count = (int64_t)P.wchunks.size();
+  for (int64_t q = 0; q < std::min<int64_t>(cap, *count); ++q) {
+    const Chunk& c = P.wchunks[q];
+    rows[q * 6 + 0] = c.seg;
+    rows[q * 6 + 1] = c.shard;
+    rows[q * 6 + 2] = c.start;
+    rows[q * 6 + 3] = c.len;
+    rows[q * 6 + 4] = c.off;
+    rows[q * 6 + 5] = c.per;
+  }
+  return ONEBIT_OK;
+}
+
 onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* params, void* workspace,
                                  size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out) {
   if (!out || !params) return ONEBIT_ERR_INVALID_ARG;
@@ -734,6 +820,8 @@ onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* 
   std::memcpy(tables.data() + (h->lay.seg_ranges - h->lay.chunks), P.seg_ranges.data(), P.T * sizeof(Range));
   std::memcpy(tables.data() + (h->lay.shard_ranges - h->lay.chunks), P.shard_ranges.data(),
               (size_t)P.T * P.n * sizeof(Range));
+  std::memcpy(tables.data() + (h->lay.wchunks - h->lay.chunks), P.wchunks.data(), P.wchunks.size() * sizeof(Chunk));
+  std::memcpy(tables.data() + (h->lay.wseg_ranges - h->lay.chunks), P.wseg_ranges.data(), P.T * sizeof(Range));
   if (cudaMemcpyAsync(h->ws + h->lay.chunks, tables.data(), tables.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
     return fail(cuda_fail(h, cudaGetLastError(), "upload tables"));
   if (cudaMemcpyAsync(h->ws + h->lay.pptr, h->params.data(), P.T * sizeof(float*), cudaMemcpyHostToDevice, st) !=

@@ -21,8 +21,10 @@
 //   scales       double-buffered by step parity: a step reads the previous step's scales (to rebuild
 //                the errors and m) and writes its own.
 //
-// Work decomposition: a host-built table of chunks (<= kChunk elements, never crossing a tensor or a
-// server-shard boundary, starting on a 32-element boundary).  Each lane owns 8 consecutive elements
+// Work decomposition: host-built tables of chunks (<= kChunk elements, never crossing a tensor,
+// starting on a 32-element boundary).  The server-side table never crosses a server shard either;
+// the worker-side table is the same except inside tensors whose shards are shorter than a chunk,
+// where one worker chunk holds several whole shards.  Each lane owns 8 consecutive elements
 // (one byte of sign bits, one 256-bit load of fp32 state), so sign packing needs no cross-lane
 // exchange and every warp access is a contiguous 1 KB (fp32) or 512 B (16-bit) span.
 //
@@ -52,7 +54,8 @@ struct Chunk {
   int32_t seg;    // tensor k
   int32_t shard;  // server shard j of tensor k
   int32_t len;    // elements, 1..kChunk
-  int32_t pad_;
+  int32_t per;    // worker chunks only: the tensor's shard length S_k when the chunk spans several
+                  // server shards (its groups then look up their own shard), else 0
 };
 
 struct Range {    // a contiguous run of chunks with its element count
@@ -62,7 +65,7 @@ struct Range {    // a contiguous run of chunks with its element count
 };
 
 struct StepArgs {
-  const Chunk* chunks;
+  const Chunk* chunks;       // server-side chunks: never cross a tensor or a server shard
   int32_t n_chunks;
   int32_t n;      // workers
   int32_t T;      // tensors
@@ -82,13 +85,18 @@ struct StepArgs {
   float* wscale_cur;         // [n*T]
   const float* sscale_prev;  // [T*n]
   float* sscale_cur;         // [T*n]
-  double* wpart;             // [n*n_chunks]
+  double* wpart;             // [n*n_wchunks]
   double* spart;             // [n_chunks]
   const Range* seg_ranges;   // [T]   chunks of each tensor
   const Range* shard_ranges; // [T*n] chunks of each server shard
   unsigned int* status;
   float b1, omb1, b2, omb2, lr, eps, inv_n, nf, bc1, bc2;
   uint32_t stall_tx;  // test hook: extra bytes the staged kernels' copy barriers wait for (normally 0)
+  const Chunk* wchunks;      // worker-side chunks: never cross a tensor; may span several shards
+  const Range* wseg_ranges;  // [T]   worker chunks of each tensor
+  int32_t n_wchunks;
+  int32_t contig;            // the register server kernel walks contiguous runs (many short tensors)
+  int64_t D;                 // elements (unpadded)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -246,33 +254,40 @@ __device__ __forceinline__ float error_of(float c, float s) {  // c - s*sign(c),
 
 // Where the worker kernel's momentum comes from.
 enum MomentumSource : int {
-  kMomBits = 0,   // the previous broadcast: S * sign(a), from the server sign bits
-  kMomDense = 1,  // the fp32 buffer (first compression step, after an import)
-  kMomNone = 2    // no momentum: c_i = g_i + delta_i (the gradient-compression baseline)
+  kMomBits = 0,        // the previous broadcast: S * sign(a), from the server sign bits
+  kMomDense = 1,       // the fp32 buffer (first compression step, after an import)
+  kMomNone = 2,        // no momentum: c_i = g_i + delta_i (the gradient-compression baseline)
+  kMomBitsShards = 3   // as kMomBits, for plans whose worker chunks may hold several shards
 };
 
 template <typename GT, int MSRC, bool HAS_ERR, bool VEC>
 __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
   constexpr bool DENSE_M = MSRC == kMomDense;
+  constexpr bool BITS = MSRC == kMomBits || MSRC == kMomBitsShards;
   __shared__ double red[kThreads / 32];
-  const int64_t n_units = (int64_t)A.n_chunks * A.n;
+  const int64_t n_units = (int64_t)A.n_wchunks * A.n;
   for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
     const int ci = (int)(u / A.n);
     const int i = (int)(u - (int64_t)ci * A.n);
-    const Chunk ch = A.chunks[ci];
+    const Chunk ch = A.wchunks[ci];
     const GT* __restrict__ g = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start;
     float* __restrict__ c = A.c + (int64_t)i * A.Dp + ch.off;
     uint8_t* __restrict__ wb = reinterpret_cast<uint8_t*>(A.wbits + (int64_t)i * A.Wr) + (ch.off >> 3);
     const uint8_t* __restrict__ sb = reinterpret_cast<const uint8_t*>(A.sbits) + (ch.off >> 3);
     const float* __restrict__ md = A.m + ch.off;
     const float sp = HAS_ERR ? A.wscale_prev[(int64_t)i * A.T + ch.seg] : 0.0f;
-    const float Sp = MSRC == kMomBits ? A.sscale_prev[(int64_t)ch.seg * A.n + ch.shard] : 0.0f;
+    const float Sp = BITS ? A.sscale_prev[(int64_t)ch.seg * A.n + ch.shard] : 0.0f;
     const float b1 = A.b1, omb1 = A.omb1;
+    // a chunk that holds several whole server shards (short shards only) takes each group's broadcast
+    // scale from that group's own shard: shard + (offset inside the chunk) / shard length
+    const float* __restrict__ Sseg = A.sscale_prev + (int64_t)ch.seg * A.n + ch.shard;
+    auto scale_of = [&](int gi) { return ch.per ? Sseg[(uint32_t)(gi * 8) / (uint32_t)ch.per] : Sp; };
 
     // one group of 8 elements: loads first (so that two groups are in flight), then math + stores
     struct In {
       float g[8], cp[8], m[8];
       uint32_t mb;
+      float S;
     };
     (void)DENSE_M;
     auto load = [&](In& r, int gi) {
@@ -285,7 +300,8 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       }
       if (HAS_ERR) ld8_state(c + e, r.cp);
       if (MSRC == kMomDense) ld8_stream(md + e, r.m);
-      if (MSRC == kMomBits) r.mb = sb[gi];
+      if (BITS) r.mb = sb[gi];
+      if (MSRC == kMomBitsShards) r.S = scale_of(gi);
     };
     unsigned long long hi = 0, lo = 0;  // this thread's sum of c^2 over the unit (two lanes)
     auto work = [&](const In& r, int gi) {
@@ -297,7 +313,8 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
         if (MSRC == kMomNone) {
           mi = r.g[q];
         } else {
-          const float mq = MSRC == kMomDense ? r.m[q] : (((r.mb >> q) & 1u) ? Sp : -Sp);
+          const float Sg = MSRC == kMomBitsShards ? r.S : Sp;
+          const float mq = MSRC == kMomDense ? r.m[q] : (((r.mb >> q) & 1u) ? Sg : -Sg);
           mi = momentum(b1, omb1, mq, r.g[q]);
         }
         const float d = HAS_ERR ? error_of(r.cp[q], sp) : 0.0f;
@@ -328,6 +345,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
     const int rem = ch.len & 7;
     if (rem && threadIdx.x == (ng % kThreads)) {  // the ragged end of a tensor: scalar
       const int64_t e0 = (int64_t)ng * 8;
+      const float St = MSRC == kMomBitsShards ? scale_of(ng) : Sp;
       uint32_t byte = 0;
       for (int q = 0; q < rem; ++q) {
         const int64_t e = e0 + q;
@@ -335,7 +353,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
         if (MSRC == kMomNone) {
           mi = Grad<GT>::load1(g + e);
         } else {
-          const float mq = MSRC == kMomDense ? md[e] : (((sb[ng] >> q) & 1u) ? Sp : -Sp);
+          const float mq = MSRC == kMomDense ? md[e] : (((sb[ng] >> q) & 1u) ? St : -St);
           mi = momentum(b1, omb1, mq, Grad<GT>::load1(g + e));
         }
         const float d = HAS_ERR ? error_of(c[e], sp) : 0.0f;
@@ -347,7 +365,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       wb[ng] = (uint8_t)byte;
     }
     const double tot = block_sum<kThreads>(square_total(hi, lo), red);
-    if (threadIdx.x == 0) A.wpart[(int64_t)i * A.n_chunks + ci] = tot;
+    if (threadIdx.x == 0) A.wpart[(int64_t)i * A.n_wchunks + ci] = tot;
   }
 }
 
@@ -371,7 +389,7 @@ __device__ __forceinline__ float finish_scale(const double* part, const Range r,
 static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale(const StepArgs A) {
   __shared__ double red[kScaleThreads / 32];
   const int i = blockIdx.x / A.T, k = blockIdx.x % A.T;
-  const float s = finish_scale(A.wpart + (int64_t)i * A.n_chunks, A.seg_ranges[k], A.status, red);
+  const float s = finish_scale(A.wpart + (int64_t)i * A.n_wchunks, A.wseg_ranges[k], A.status, red);
   if (threadIdx.x == 0) A.wscale_cur[blockIdx.x] = s;
 }
 
@@ -379,6 +397,38 @@ static __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const Ste
   __shared__ double red[kScaleThreads / 32];
   const float s = finish_scale(A.spart, A.shard_ranges[blockIdx.x], A.status, red);
   if (threadIdx.x == 0) A.sscale_cur[blockIdx.x] = s;
+}
+
+// The same sums for lists of many short ranges (at most kWarpScaleMax partials each): one warp per
+// scale, kScaleThreads/32 scales per CTA.  A plan uses one form or the other for all its scales of a
+// kind, so the summation order is fixed for a given plan.
+constexpr int kWarpScaleMax = 256;
+__device__ __forceinline__ float finish_scale_warp(const double* part, const Range r, unsigned int* status) {
+  const int lane = threadIdx.x & 31;
+  double acc = 0.0;
+  for (int c = lane; c < r.count; c += 32) acc += __ldcg(part + r.first + c);
+  acc = warp_sum(acc);
+  float s = 0.0f;
+  if (lane == 0) {
+    s = r.len > 0 ? __double2float_rn(sqrt(acc / (double)r.len)) : 0.0f;
+    if (!isfinite(s)) atomicOr(status, 1u);
+  }
+  return s;
+}
+
+static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale_warp(const StepArgs A) {
+  const int item = blockIdx.x * (kScaleThreads / 32) + (threadIdx.x >> 5);
+  if (item >= A.n * A.T) return;  // the whole warp
+  const int i = item / A.T, k = item % A.T;
+  const float s = finish_scale_warp(A.wpart + (int64_t)i * A.n_wchunks, A.wseg_ranges[k], A.status);
+  if ((threadIdx.x & 31) == 0) A.wscale_cur[item] = s;
+}
+
+static __global__ void __launch_bounds__(kScaleThreads) k_server_scale_warp(const StepArgs A) {
+  const int item = blockIdx.x * (kScaleThreads / 32) + (threadIdx.x >> 5);
+  if (item >= A.n * A.T) return;
+  const float s = finish_scale_warp(A.spart, A.shard_ranges[item], A.status);
+  if ((threadIdx.x & 31) == 0) A.sscale_cur[item] = s;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -507,14 +557,37 @@ __device__ __forceinline__ void store_a(float* a, int64_t e, int cnt, const floa
   }
 }
 
+// Which chunks a server CTA takes.  Normally every gridDim.x-th chunk.  For lists of many short
+// tensors (CONTIG, register variant only) one contiguous run instead, so that consecutive chunks of a
+// tensor share one CTA and its sum tables are rebuilt once per tensor and CTA, not once per chunk;
+// the runs split the elements evenly (the first chunk whose element offset reaches b*D/gridDim.x).
+__device__ __forceinline__ int run_begin(const StepArgs& A, int b) {
+  if (b >= (int)gridDim.x) return A.n_chunks;
+  const int64_t target = b * A.D / gridDim.x;
+  int lo = 0, hi = A.n_chunks;  // first chunk with uoff >= target
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (A.chunks[mid].uoff < target) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+
 // K2, register variant (any n): every thread loads its group's sign bytes and a directly.
-template <bool HAS_ERR>
+template <bool HAS_ERR, bool CONTIG>
 __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
   __shared__ ServerTables S;
   const int n = A.n;
   const int64_t wrow = A.Wr * 4;  // bytes per worker row of sign words
   int cur_seg = -1;
-  for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
+  int u_begin = blockIdx.x, u_end = A.n_chunks, u_step = gridDim.x;
+  if constexpr (CONTIG) {
+    u_begin = run_begin(A, blockIdx.x);
+    u_end = run_begin(A, blockIdx.x + 1);
+    u_step = 1;
+  }
+  for (int u = u_begin; u < u_end; u += u_step) {
     const Chunk ch = A.chunks[u];
     if (ch.seg != cur_seg) {  // block-uniform
       build_server_tables(S, A, ch.seg);
@@ -924,8 +997,9 @@ __global__ void __launch_bounds__(kThreads) k_ec_adam_update(const StepArgs A) {
 
 // ------------------------------------------------------------------------------------------------
 // K0: warm-up.  Mean of the n worker gradients (summed in worker order), then one Adam step.
-// The gradients are fetched in batches (8 workers for 16-bit, 4 for fp32 gradients) whose loads are
-// all issued before the batch is added in order, so one memory latency covers a whole batch.
+// The gradients are fetched in batches (16 workers for 16-bit, 8 for fp32 gradients) whose loads are
+// all issued before the batch is added in order, so one memory latency covers a whole batch.  The
+// kernel is held to 128 registers (two CTAs per SM) so that a batch fits without spilling.
 
 template <typename GT> struct RawGrad;  // one 8-element gradient group as loaded
 template <> struct RawGrad<float> {
@@ -953,8 +1027,8 @@ template <> struct RawGrad<__nv_bfloat16> {
 // With MON the kernel also writes each chunk's exact sum of the new v^2 to A.spart (the "fused
 // variance norm" monitor; k_variance_norm reduces it).
 template <typename GT, bool BC, bool VEC, bool MON>
-__global__ void __launch_bounds__(kThreads) k_warmup(const StepArgs A) {
-  constexpr int B = sizeof(GT) == 4 ? 4 : 8;
+__global__ void __launch_bounds__(kThreads, 2) k_warmup(const StepArgs A) {
+  constexpr int B = sizeof(GT) == 4 ? 8 : 16;
   __shared__ const GT* gsm[kMaxWorkers];
   __shared__ double red[kThreads / 32];
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {

@@ -221,8 +221,17 @@ onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, 
 
 /* The work chunks the kernels use for a config (host only, no GPU needed): up to `cap` rows of
  * five int64 {tensor, shard, start element within the tensor, length, padded state offset}.
- * *count receives the total number of chunks. */
+ * *count receives the total number of chunks.  These are the server-side chunks (server, update,
+ * warm-up and export kernels): they never cross a tensor or a server shard. */
 onebit_status_t onebit_adam_plan_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap, int64_t* count);
+
+/* The worker kernel's chunks (host only): rows of six int64 {tensor, first shard, start element
+ * within the tensor, length, padded state offset, shard length if the chunk holds several whole
+ * shards else 0}.  They never cross a tensor.  Where a tensor's shards are at least a chunk long they
+ * equal the server-side chunks; where shards are shorter, one worker chunk holds several whole shards,
+ * so that the worker kernel keeps long units. */
+onebit_status_t onebit_adam_plan_worker_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap,
+                                               int64_t* count);
 
 /* Largest vector onebit_worker_compress_noalloc() accepts (elements). */
 #define ONEBIT_NOALLOC_MAX_LEN 268435456

@@ -124,6 +124,45 @@ def test_chunk_plan_scale_blocks(numel, n, block):
         assert pos == L
 
 
+WORKER_PLANS = [([1 << 20], 4, 0), ([1000], 16, 0), ([5, 0, 33, 200], 4, 0), ([340_000_000], 16, 0),
+                ([224, 0, 96], 3, 96), ([1 << 20], 16, 65536), ([70_001, 33, 0, 5], 3, 96), ([5000], 20, 32)]
+
+
+@pytest.mark.parametrize("numel,n,block", WORKER_PLANS, ids=[f"{sum(a)}_n{b}_B{c}" for a, b, c in WORKER_PLANS])
+def test_worker_chunk_plan(numel, n, block):
+    """Worker chunks tile every segment once, start on a 32-element boundary, hold at most one chunk
+    length; a chunk that spans shards holds whole shards (its first shard and the recorded shard
+    length follow the oracle's shard rule); where shards are at least a chunk long the worker table
+    equals the server-side table."""
+    import oracle as _o
+    cfg = ob.make_config(numel, n, scale_block=block)
+    rows = ob.plan_worker_chunks(cfg)
+    server = ob.plan_chunks(cfg)
+    segs = _o.scale_blocks(numel, block)
+    want = -(-sum(numel) // 1216)
+    clen = min(65536, max(4096, -(-want // 4096) * 4096))  # the chunk-length rule
+    by_seg = {k: [] for k in range(len(segs))}
+    for r in rows:
+        by_seg[r[0]].append(r)
+    for k, L in enumerate(segs):
+        per = 32 * -(-L // (32 * n)) if L else 0
+        pos = 0
+        for (seg, j, start, length, off, rper) in by_seg[k]:
+            assert start == pos and start % 32 == 0 and 1 <= length <= 65536
+            lo, hi = oracle.shard(L, n, j)
+            assert lo == start if rper else lo <= start < hi
+            if rper:
+                assert rper == per and start % per == 0 and length > per
+                last = (start + length - 1) // per
+                assert last < n and (start + length == L or (start + length) % per == 0)
+            else:
+                assert start + length <= hi
+            pos += length
+        assert pos == L
+        if per >= clen:
+            assert [r[:5] for r in by_seg[k]] == [r for r in server if r[0] == k]
+
+
 def test_small_lists_get_short_chunks():
     """Chunk length adapts to the list: 2^20 elements become 256 chunks of 4096 (work units for
     every SM), while a BERT-Large-sized list keeps 65536-element chunks."""
