@@ -997,9 +997,10 @@ __global__ void __launch_bounds__(kThreads) k_ec_adam_update(const StepArgs A) {
 
 // ------------------------------------------------------------------------------------------------
 // K0: warm-up.  Mean of the n worker gradients (summed in worker order), then one Adam step.
-// The gradients are fetched in batches (16 workers for 16-bit, 8 for fp32 gradients) whose loads are
-// all issued before the batch is added in order, so one memory latency covers a whole batch.  The
-// kernel is held to 128 registers (two CTAs per SM) so that a batch fits without spilling.
+// The gradients are fetched in batches whose loads are all issued before the batch is added in order,
+// so one memory latency covers a whole batch.  Large batches (16 workers for 16-bit, 8 for fp32
+// gradients) hold the kernel to 128 registers, two CTAs per SM; for n <= 4 16-bit gradients a batch
+// of 4 needs far fewer registers and the kernel runs three CTAs per SM.
 
 template <typename GT> struct RawGrad;  // one 8-element gradient group as loaded
 template <> struct RawGrad<float> {
@@ -1026,9 +1027,9 @@ template <> struct RawGrad<__nv_bfloat16> {
 
 // With MON the kernel also writes each chunk's exact sum of the new v^2 to A.spart (the "fused
 // variance norm" monitor; k_variance_norm reduces it).
-template <typename GT, bool BC, bool VEC, bool MON>
-__global__ void __launch_bounds__(kThreads, 2) k_warmup(const StepArgs A) {
-  constexpr int B = sizeof(GT) == 4 ? 8 : 16;
+template <typename GT, bool BC, bool VEC, bool MON, bool SMALL>
+__global__ void __launch_bounds__(kThreads, SMALL ? 3 : 2) k_warmup(const StepArgs A) {
+  constexpr int B = SMALL ? 4 : (sizeof(GT) == 4 ? 8 : 16);
   __shared__ const GT* gsm[kMaxWorkers];
   __shared__ double red[kThreads / 32];
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
