@@ -1,6 +1,8 @@
 // onebit_adam.cu -- host side of the C ABI declared in include/onebit_adam.h.
 //
-// The handle owns: the chunk plan (the multi-tensor launcher's work table), the workspace layout,
+// The handle owns: the chunk plan (the multi-tensor launcher's work tables: server-side chunks that
+// never cross a server shard, and the worker kernel's chunks, which may hold several short shards),
+// the workspace layout,
 // the phase machine (warm-up -> freeze -> compression), the representation flags of the lazily
 // materialised state (see onebit_kernels.cuh), a small ring of device-side gradient pointer tables,
 // and optional per-kernel CUDA-event timing.  Every hot-path operation runs in the kernels.
