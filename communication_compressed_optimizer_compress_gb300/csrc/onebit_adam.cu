@@ -15,6 +15,7 @@
 #include <mutex>
 #include <string>
 #include <unordered_map>
+#include <unordered_set>
 #include <vector>
 
 #include "../../include/onebit_adam.h"
@@ -271,6 +272,7 @@ struct onebit_adam {
   int64_t launches = 0;
   std::unordered_map<const void*, int> occupancy;
   bool smem_configured[2] = {false, false};
+  std::unordered_set<const void*> dyn_smem_set;  // kernels whose dynamic shared-memory limit is raised
   uint32_t stall_tx = 0;  // fault injection (see onebit_adam_set_fault_injection)
   // variance-norm monitor (warm-up)
   bool vmon = false;
@@ -452,6 +454,23 @@ template <typename GT, bool MON>
 onebit_status_t run_warmup_m(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
   const int C = A.n_chunks;
   const bool bc = h->cfg.bias_correction != 0;
+  if constexpr (sizeof(GT) == 2) {
+    if (vec && A.n >= kWarmStagedMin && A.n <= kWarmStagedMax) {
+      // many 16-bit gradient streams: the shared-memory staged variant keeps enough bytes in flight
+      const size_t dyn = warmup_dyn_smem(A.n);
+      auto go = [&](auto kern) -> onebit_status_t {
+        if (!h->dyn_smem_set.count((const void*)kern)) {
+          cudaError_t e = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)warmup_dyn_smem(kWarmStagedMax));
+          if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute");
+          h->dyn_smem_set.insert((const void*)kern);
+        }
+        return launch(h, ONEBIT_K_WARMUP, kern, grid_for(h, (const void*)kern, kStagedThreads, C, dyn), kStagedThreads,
+                      st, A, dyn);
+      };
+      return bc ? go(k_warmup_staged<GT, true, MON>) : go(k_warmup_staged<GT, false, MON>);
+    }
+  }
   auto pick = [&](auto kern) { return launch(h, ONEBIT_K_WARMUP, kern, grid_for(h, (const void*)kern, kThreads, C), kThreads, st, A); };
   if (A.n <= 4 && sizeof(GT) == 2) {  // 16-bit gradients, all in one small batch (measured slower for fp32)
     if (bc) return vec ? pick(k_warmup<GT, true, true, MON, true>) : pick(k_warmup<GT, true, false, MON, true>);

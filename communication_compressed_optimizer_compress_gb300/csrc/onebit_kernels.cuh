@@ -1125,6 +1125,184 @@ __global__ void __launch_bounds__(kThreads, SMALL ? 3 : 2) k_warmup(const StepAr
   }
 }
 
+// K0, staged variant: 16-bit gradients, kWarmStagedMin <= n <= kWarmStagedMax, every pointer
+// aligned.  Per-thread register batches cannot keep enough bytes in flight for 16 gradient streams
+// read 16 bytes at a time, so a producer warp streams each tile of the n gradient rows and of m, v
+// and x into shared memory with bulk copies (two stages), and the consumer warps add the gradients
+// in worker order and run the same fp32 Adam arithmetic as k_warmup, writing m, v and x straight
+// back.  A tile's last partial group (a tensor's ragged end) is read with plain loads.  Waits are
+// bounded exactly as in the staged server kernel.
+constexpr int kWTile = 2048;   // elements per tile: one 8-element group per consumer thread
+constexpr int kWStages = 2;
+constexpr int kWarmStagedMin = 8;
+constexpr int kWarmStagedMax = 20;  // two stages of 2048 * (2n + 12) bytes fit the 227 KB per CTA
+__host__ __device__ constexpr size_t warmup_stage_bytes(int n) { return (size_t)kWTile * (2 * n + 12); }
+__host__ __device__ constexpr size_t warmup_dyn_smem(int n) { return kWStages * warmup_stage_bytes(n) + 2 * kWStages * 8; }
+
+template <typename GT, bool BC, bool MON>
+__global__ void __launch_bounds__(kStagedThreads) k_warmup_staged(const StepArgs A) {
+  __shared__ double red[kConsumerWarps];
+  __shared__ volatile int abort_flag;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  const int n = A.n;
+  const size_t stage_bytes = warmup_stage_bytes(n);
+  uint64_t* full = reinterpret_cast<uint64_t*>(dyn + kWStages * stage_bytes);
+  uint64_t* empty = full + kWStages;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int st = 0; st < kWStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto advance = [&](TileCursor& c) {
+    if (++c.t >= (A.chunks[c.u].len + kWTile - 1) / kWTile) {
+      c.t = 0;
+      c.u += gridDim.x;
+    }
+  };
+  const size_t mofs = (size_t)n * kWTile * 2;  // stage layout: n gradient rows, then m, v, x
+
+  if (threadIdx.x >= kThreads) {
+    // ---------------- producer warp (one elected lane issues the copies)
+    if (threadIdx.x != kThreads) return;
+    TileCursor c{(int)blockIdx.x, 0};
+    int j = 0;
+    for (; c.u < A.n_chunks; ++j, advance(c)) {
+      const int st = j % kWStages;
+      if (j >= kWStages && !abort_flag && !mbar_wait(&empty[st], (uint32_t)((j / kWStages - 1) & 1))) {
+        atomicOr(A.status, 2u);
+        abort_flag = 1;
+      }
+      if (abort_flag) break;
+      const Chunk ch = A.chunks[c.u];
+      const int e0 = c.t * kWTile;
+      const int tv = min(kWTile, ch.len - e0) & ~7;  // whole groups: every copy a multiple of 16 bytes
+      unsigned char* sb = dyn + (size_t)st * stage_bytes;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_expect_tx(&full[st], (uint32_t)tv * (uint32_t)(2 * n + 12) + A.stall_tx);
+      if (tv > 0) {
+        for (int i = 0; i < n; ++i)
+          bulk_copy_g2s(sb + (size_t)i * kWTile * 2,
+                        static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start + e0, (uint32_t)tv * 2,
+                        &full[st]);
+        bulk_copy_g2s(sb + mofs, A.m + ch.off + e0, (uint32_t)tv * 4, &full[st]);
+        bulk_copy_g2s(sb + mofs + kWTile * 4, A.v + ch.off + e0, (uint32_t)tv * 4, &full[st]);
+        bulk_copy_g2s(sb + mofs + kWTile * 8, A.pptr[ch.seg] + ch.start + e0, (uint32_t)tv * 4, &full[st]);
+      }
+    }
+    if (abort_flag) {
+      for (int q = j - kWStages; q < j; ++q)
+        if (q >= 0 && !mbar_wait(&full[q % kWStages], (uint32_t)((q / kWStages) & 1))) break;
+    }
+    return;
+  }
+
+  // ---------------- consumer warps: thread t owns elements [8t, 8t+8) of every tile
+  const int lane = threadIdx.x & 31;
+  TileCursor cons{(int)blockIdx.x, 0};
+  int k = 0;
+  unsigned long long vhi = 0, vlo = 0;
+  while (cons.u < A.n_chunks) {
+    const Chunk ch = A.chunks[cons.u];
+    const int st = k % kWStages;
+    if (!abort_flag && !mbar_wait(&full[st], (uint32_t)((k / kWStages) & 1))) {
+      atomicOr(A.status, 2u);
+      abort_flag = 1;
+    }
+    if (!abort_flag) {
+      const unsigned char* sb = dyn + (size_t)st * stage_bytes;
+      const int e0 = cons.t * kWTile;
+      const int tlen = min(kWTile, ch.len - e0);
+      const int eg = threadIdx.x * 8;
+      if (eg < tlen) {
+        const int cnt = min(8, tlen - eg);
+        const int64_t ge = (int64_t)e0 + eg;  // element within the chunk
+        float* m = A.m + ch.off + ge;
+        float* v = A.v + ch.off + ge;
+        float* x = A.pptr[ch.seg] + ch.start + ge;
+        float mv[8], vv[8], xv[8], acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        if (eg + 8 <= (tlen & ~7)) {  // the whole group is in the stage
+          const float4* ms = reinterpret_cast<const float4*>(sb + mofs) + eg / 4;
+          const float4* vs = reinterpret_cast<const float4*>(sb + mofs + kWTile * 4) + eg / 4;
+          const float4* xs = reinterpret_cast<const float4*>(sb + mofs + kWTile * 8) + eg / 4;
+          const float4 m0 = ms[0], m1 = ms[1], v0 = vs[0], v1 = vs[1], x0 = xs[0], x1 = xs[1];
+          mv[0] = m0.x; mv[1] = m0.y; mv[2] = m0.z; mv[3] = m0.w; mv[4] = m1.x; mv[5] = m1.y; mv[6] = m1.z; mv[7] = m1.w;
+          vv[0] = v0.x; vv[1] = v0.y; vv[2] = v0.z; vv[3] = v0.w; vv[4] = v1.x; vv[5] = v1.y; vv[6] = v1.z; vv[7] = v1.w;
+          xv[0] = x0.x; xv[1] = x0.y; xv[2] = x0.z; xv[3] = x0.w; xv[4] = x1.x; xv[5] = x1.y; xv[6] = x1.z; xv[7] = x1.w;
+          for (int i = 0; i < n; ++i) {
+            RawGrad<GT> r;
+            r.u = *reinterpret_cast<const uint4*>(sb + (size_t)i * kWTile * 2 + (size_t)eg * 2);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], r.get(q));
+          }
+        } else {  // a tensor's ragged end: plain loads
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            mv[q] = q < cnt ? m[q] : 0.0f;
+            vv[q] = q < cnt ? v[q] : 0.0f;
+            xv[q] = q < cnt ? x[q] : 0.0f;
+          }
+          for (int i = 0; i < n; ++i) {
+            const GT* gp = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start + ge;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], q < cnt ? Grad<GT>::load1(gp + q) : 0.0f);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float gbar = A.pow2 ? __fmul_rn(acc[q], A.inv_n) : __fdiv_rn(acc[q], A.nf);
+          mv[q] = momentum(A.b1, A.omb1, mv[q], gbar);
+          vv[q] = __fadd_rn(__fmul_rn(A.b2, vv[q]), __fmul_rn(A.omb2, __fmul_rn(gbar, gbar)));
+          const float mh = BC ? __fdiv_rn(mv[q], A.bc1) : mv[q];
+          const float vh = BC ? __fdiv_rn(vv[q], A.bc2) : vv[q];
+          xv[q] = __fsub_rn(xv[q], __fmul_rn(A.lr, __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), A.eps))));
+        }
+        if (MON) {
+#pragma unroll
+          for (int q = 0; q < 8; q += 2)
+            add_square2(vhi, vlo, q < cnt ? vv[q] : 0.0f, q + 1 < cnt ? vv[q + 1] : 0.0f);
+        }
+        if (cnt == 8) {
+          st8(m, mv);
+          st8(v, vv);
+          st8(x, xv);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < cnt) {
+              m[q] = mv[q];
+              v[q] = vv[q];
+              x[q] = xv[q];
+            }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    ++k;
+    const bool last_tile = cons.t == (ch.len + kWTile - 1) / kWTile - 1;
+    const int u_done = cons.u;
+    advance(cons);
+    if (MON && last_tile) {  // chunk total of v^2 among the consumers (fixed order)
+      double t = warp_sum(square_total(vhi, vlo));
+      if (lane == 0) red[threadIdx.x >> 5] = t;
+      consumers_sync();
+      if (threadIdx.x < 32) {
+        double r = lane < kConsumerWarps ? red[lane] : 0.0;
+        r = warp_sum(r);
+        if (threadIdx.x == 0 && !abort_flag) A.spart[u_done] = r;
+      }
+      consumers_sync();
+      vhi = vlo = 0;
+    }
+  }
+}
+
 // ||v||_2 after a monitored warm-up step: one CTA, fixed-order sum of the chunk partials.
 static __global__ void __launch_bounds__(kScaleThreads) k_variance_norm(const double* part, int n_chunks, double* out) {
   __shared__ double red[kScaleThreads / 32];
