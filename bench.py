@@ -59,14 +59,15 @@ def measured_peak():
 
 
 def _kernel_source_hash(marker: str):
-    """Hash of one kernel's source: the shared tuning constants plus the kernel's own region (from
-    its heading comment to the next separator)."""
+    """Hash of one kernel's source: the constants declared before it (the shared tuning constants
+    and those of the kernels it builds on) plus the kernel's own region (from its heading comment to
+    the next separator)."""
     import hashlib
 
     path = os.path.join(ROOT, "communication_compressed_optimizer_compress_gb300", "csrc", "onebit_kernels.cuh")
     src = open(path).read()
-    consts = "\n".join(ln for ln in src.splitlines() if ln.startswith("constexpr "))
     i = src.index(marker)
+    consts = "\n".join(ln for ln in src[:i].splitlines() if ln.startswith("constexpr "))
     j = src.index("// ------", i)
     return hashlib.sha256((consts + src[i:j]).encode()).hexdigest()[:16]
 

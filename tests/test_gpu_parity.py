@@ -285,11 +285,13 @@ def test_workspace_caller_owned():
     a.close()
 
 
-def test_variance_norm_monitor_matches_oracle():
-    """||v_t||_2 reported during warm-up equals the oracle's norm of its own v after every step."""
+@pytest.mark.parametrize("n,dtype", [(3, W.F16), (16, W.BF16), (8, W.F32)], ids=["small_batch", "staged", "batched"])
+def test_variance_norm_monitor_matches_oracle(n, dtype):
+    """||v_t||_2 reported during warm-up equals the oracle's norm of its own v after every step, for
+    each form of the warm-up kernel (small register batch, shared-memory staged, register batch)."""
     import oracle
 
-    w = _tiny(numel=(70_001, 333, 5), n_workers=3, grad_dtype=W.F16, warmup_steps=4, seed=101)
+    w = _tiny(numel=(70_001, 333, 5), n_workers=n, grad_dtype=dtype, warmup_steps=4, seed=101 + n)
     p = Pair(w)
     p.gpu.set_variance_monitor(True)
     for t in range(1, 5):
