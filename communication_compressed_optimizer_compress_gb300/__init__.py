@@ -18,7 +18,7 @@ F32, F16, BF16 = 0, 1, 2
 PHASE_WARMUP, PHASE_COMPRESS = 0, 1
 (STATE_M, STATE_V, STATE_WORKER_ERROR, STATE_SERVER_ERROR, STATE_WORKER_BITS, STATE_SERVER_BITS,
  STATE_WORKER_SCALES, STATE_SERVER_SCALES) = range(8)
-FAULT_NONE, FAULT_STALL_COPIES = 0, 1
+FAULT_NONE, FAULT_STALL_COPIES, FAULT_FAIL_ALLOC = 0, 1, 2
 KERNEL_NAMES = ["warmup", "freeze", "worker", "worker_scale", "server", "server_scale", "update", "export",
                 "ec_update"]
 NUM_KERNELS = len(KERNEL_NAMES)

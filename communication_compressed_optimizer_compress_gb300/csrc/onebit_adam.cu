@@ -7,6 +7,7 @@
 // materialised state (see onebit_kernels.cuh), a small ring of device-side gradient pointer tables,
 // and optional per-kernel CUDA-event timing.  Every hot-path operation runs in the kernels.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -274,6 +275,7 @@ struct onebit_adam {
   bool smem_configured[2] = {false, false};
   std::unordered_set<const void*> dyn_smem_set;  // kernels whose dynamic shared-memory limit is raised
   uint32_t stall_tx = 0;  // fault injection (see onebit_adam_set_fault_injection)
+  int fail_allocs = 0;    // allocations still to refuse (fault injection)
   // variance-norm monitor (warm-up)
   bool vmon = false;
   double* vnorm_host = nullptr;  // pinned
@@ -285,6 +287,13 @@ struct onebit_adam {
 };
 
 namespace {
+
+// Tracing: every public step and state call is one named NVTX range (visible in Nsight tools;
+// a no-op when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 struct DeviceGuard {
   int prev = -1;
@@ -298,6 +307,13 @@ struct DeviceGuard {
     if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
   }
 };
+
+// Fault injection: true when this allocation is to be refused (ONEBIT_FAULT_FAIL_ALLOC).
+bool refuse_alloc(onebit_adam* h) {
+  if (h->fail_allocs <= 0) return false;
+  --h->fail_allocs;
+  return true;
+}
 
 onebit_status_t cuda_fail(onebit_adam* h, cudaError_t e, const char* where) {
   if (h) h->last_error = std::string(where) + ": " + cudaGetErrorString(e);
@@ -668,7 +684,7 @@ onebit_status_t stage_copy(onebit_adam* h, const void* const* host_grads, cudaSt
     for (int i = 0; i < n; ++i)
       for (int k = 0; k < T; ++k) bytes += align_up(numel[k] * gb, kAlign);
     for (int b = 0; b < 2; ++b) {
-      if (cudaMalloc(&h->staging[b], std::max<size_t>(bytes, 1)) != cudaSuccess) {
+      if (refuse_alloc(h) || cudaMalloc(&h->staging[b], std::max<size_t>(bytes, 1)) != cudaSuccess) {
         cudaGetLastError();
         if (b == 1) cudaFree(h->staging[0]);
         h->staging[0] = h->staging[1] = nullptr;
@@ -788,6 +804,7 @@ onebit_status_t onebit_adam_plan_worker_chunks(const onebit_adam_config_t* cfg, 
 
 onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* params, void* workspace,
                                  size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out) {
+  NvtxRange trace("onebit_adam_init");
   if (!out || !params) return ONEBIT_ERR_INVALID_ARG;
   *out = nullptr;
   onebit_status_t s = check_config(cfg);
@@ -884,24 +901,28 @@ onebit_status_t onebit_adam_free(onebit_adam_t* h) {
 }
 
 onebit_status_t onebit_adam_warmup_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
+  NvtxRange trace("onebit_adam_warmup_step");
   if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
   DeviceGuard g(h->device);
   return do_warmup(h, grads, as_stream(stream));
 }
 
 onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
+  NvtxRange trace("onebit_adam_compress_step");
   if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
   DeviceGuard g(h->device);
   return do_compress(h, grads, as_stream(stream));
 }
 
 onebit_status_t onebit_adam_ec_adam_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
+  NvtxRange trace("onebit_adam_ec_adam_step");
   if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
   DeviceGuard g(h->device);
   return do_compress(h, grads, as_stream(stream), true);
 }
 
 onebit_status_t onebit_adam_warmup_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream) {
+  NvtxRange trace("onebit_adam_warmup_step_host");
   if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
   if (h->phase != ONEBIT_PHASE_WARMUP || h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
   DeviceGuard g(h->device);
@@ -915,6 +936,7 @@ onebit_status_t onebit_adam_warmup_step_host(onebit_adam_t* h, const void* const
 }
 
 onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream) {
+  NvtxRange trace("onebit_adam_compress_step_host");
   if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
   if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
   DeviceGuard g(h->device);
@@ -928,6 +950,7 @@ onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* con
 }
 
 onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t stream) {
+  NvtxRange trace("onebit_adam_freeze_variance");
   if (!h) return ONEBIT_ERR_INVALID_ARG;
   if (h->phase != ONEBIT_PHASE_WARMUP || h->t < 1) return ONEBIT_ERR_PHASE;
   DeviceGuard g(h->device);
@@ -1026,6 +1049,7 @@ onebit_status_t onebit_adam_state_size(const onebit_adam_t* h, int32_t what, siz
 }
 
 onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worker, void* dst, onebit_stream_t stream) {
+  NvtxRange trace("onebit_adam_export");
   if (!h || !dst) return ONEBIT_ERR_INVALID_ARG;
   const Plan& P = h->plan;
   const bool per_worker = what == ONEBIT_STATE_WORKER_ERROR || what == ONEBIT_STATE_WORKER_BITS;
@@ -1063,6 +1087,7 @@ onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worke
 }
 
 onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worker, const void* src, onebit_stream_t stream) {
+  NvtxRange trace("onebit_adam_import");
   if (!h || !src) return ONEBIT_ERR_INVALID_ARG;
   const Plan& P = h->plan;
   DeviceGuard g(h->device);
@@ -1151,7 +1176,8 @@ onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enabl
   if (!h) return ONEBIT_ERR_INVALID_ARG;
   DeviceGuard g(h->device);
   if (enable && !h->vnorm_host) {
-    if (cudaHostAlloc(reinterpret_cast<void**>(&h->vnorm_host), sizeof(double), cudaHostAllocDefault) != cudaSuccess) {
+    if (refuse_alloc(h) ||
+        cudaHostAlloc(reinterpret_cast<void**>(&h->vnorm_host), sizeof(double), cudaHostAllocDefault) != cudaSuccess) {
       cudaGetLastError();
       h->vnorm_host = nullptr;
       return ONEBIT_ERR_NOMEM;
@@ -1176,10 +1202,17 @@ onebit_status_t onebit_adam_variance_norm(onebit_adam_t* h, double* norm, int64_
 onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, int64_t value) {
   if (!h) return ONEBIT_ERR_INVALID_ARG;
   switch (kind) {
-    case ONEBIT_FAULT_NONE: h->stall_tx = 0; return ONEBIT_OK;
+    case ONEBIT_FAULT_NONE:
+      h->stall_tx = 0;
+      h->fail_allocs = 0;
+      return ONEBIT_OK;
     case ONEBIT_FAULT_STALL_COPIES:
       if (value < 1 || value > (1 << 20)) return ONEBIT_ERR_INVALID_ARG;
       h->stall_tx = (uint32_t)value;
+      return ONEBIT_OK;
+    case ONEBIT_FAULT_FAIL_ALLOC:
+      if (value < 1 || value > 1000) return ONEBIT_ERR_INVALID_ARG;
+      h->fail_allocs = (int)value;
       return ONEBIT_OK;
     default: return ONEBIT_ERR_INVALID_ARG;
   }

@@ -211,12 +211,16 @@ onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launch
 onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enable);
 onebit_status_t onebit_adam_variance_norm(onebit_adam_t* h, double* norm, int64_t* step);
 
-/* Failure-detection test hook.  ONEBIT_FAULT_STALL_COPIES makes the next steps' shared-memory staged
- * kernels wait for `value` bytes (1..2^20) that no copy delivers, so that their bounded waits run out
- * (about one second): the kernel stops early, the sticky flag is set and onebit_adam_get_status()
- * returns ONEBIT_ERR_CUDA, with the CUDA context still usable.  The state of that step is not
- * meaningful.  ONEBIT_FAULT_NONE turns it off. */
-typedef enum { ONEBIT_FAULT_NONE = 0, ONEBIT_FAULT_STALL_COPIES = 1 } onebit_fault_t;
+/* Failure-detection test hooks; nothing here makes the GPU fault.
+ *   ONEBIT_FAULT_STALL_COPIES makes the next steps' shared-memory staged kernels wait for `value`
+ *     bytes (1..2^20) that no copy delivers, so that their bounded waits run out (about one second):
+ *     the kernel stops early, the sticky flag is set and onebit_adam_get_status() returns
+ *     ONEBIT_ERR_CUDA, with the CUDA context still usable.  The state of that step is not meaningful.
+ *   ONEBIT_FAULT_FAIL_ALLOC makes the handle's next `value` (1..1000) device or pinned allocations
+ *     fail as if memory were exhausted (the host-gradient staging buffers, the variance monitor's
+ *     slot): the call returns ONEBIT_ERR_NOMEM and, like every failed check, changes no state.
+ *   ONEBIT_FAULT_NONE turns both off. */
+typedef enum { ONEBIT_FAULT_NONE = 0, ONEBIT_FAULT_STALL_COPIES = 1, ONEBIT_FAULT_FAIL_ALLOC = 2 } onebit_fault_t;
 onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, int64_t value);
 
 /* The work chunks the kernels use for a config (host only, no GPU needed): up to `cap` rows of

@@ -239,6 +239,37 @@ def test_stalled_copies_are_reported_not_hung():
     q.close()
 
 
+def test_allocation_failure_is_reported_and_changes_nothing():
+    """Failure detection on the host: refused allocations (the host-gradient staging buffers, the
+    variance monitor's pinned slot) come back as ONEBIT_ERR_NOMEM with the step count, phase and
+    state untouched; once the hook is cleared the same calls succeed and the run matches the oracle
+    bit for bit."""
+    w = _tiny(numel=(20_000, 77), n_workers=4, grad_dtype=W.F16, warmup_steps=3, seed=87)
+    p = Pair(w)
+    p.warmup()  # one device-pointer step first, so that there is state to protect
+    before = (p.x().copy(), p.gpu.export_state(ob.STATE_M).cpu().numpy().copy())
+    g = p.grads()
+    host = [t.contiguous().pin_memory() for t in g]
+    p.gpu.set_fault_injection(ob.FAULT_FAIL_ALLOC, 1)
+    with pytest.raises(ob.OneBitError) as e:
+        p.gpu.warmup_step_host(host)
+    assert e.value.status == ob.ERR_NOMEM
+    torch.cuda.synchronize()
+    assert p.gpu.get_step() == (1, ob.PHASE_WARMUP)
+    assert np.array_equal(p.x().view(np.uint32), before[0].view(np.uint32))
+    assert np.array_equal(p.gpu.export_state(ob.STATE_M).cpu().numpy().view(np.uint32), before[1].view(np.uint32))
+    p.gpu.set_fault_injection(ob.FAULT_FAIL_ALLOC, 1)  # the one refusal above is used up
+    with pytest.raises(ob.OneBitError) as e:
+        p.gpu.set_variance_monitor(True)
+    assert e.value.status == ob.ERR_NOMEM
+    p.gpu.set_fault_injection(ob.FAULT_NONE)
+    p.gpu.set_variance_monitor(True)
+    p.gpu.warmup_step_host(host)
+    p.ora.warmup_step([W.to_numpy_grad(t) for t in g])
+    p.check_warmup(exact=True)
+    p.close()
+
+
 def test_timing_and_launch_counts():
     w = _tiny(numel=(50_000,), n_workers=4, warmup_steps=1)
     p = Pair(w)
