@@ -276,6 +276,7 @@ struct onebit_adam {
   std::unordered_set<const void*> dyn_smem_set;  // kernels whose dynamic shared-memory limit is raised
   uint32_t stall_tx = 0;  // fault injection (see onebit_adam_set_fault_injection)
   int fail_allocs = 0;    // allocations still to refuse (fault injection)
+  int max_ctas = 0;       // cap on the CTAs of a streaming launch (0: fill the GPU)
   // variance-norm monitor (warm-up)
   bool vmon = false;
   double* vnorm_host = nullptr;  // pinned
@@ -338,8 +339,9 @@ int grid_for(onebit_adam* h, const void* fn, int threads, int64_t units, size_t 
   } else {
     per_sm = it->second;
   }
-  const int64_t full = (int64_t)h->num_sms * per_sm;
-  return (int)std::max<int64_t>(1, std::min<int64_t>(units, full));
+  int64_t g = std::min<int64_t>(units, (int64_t)h->num_sms * per_sm);
+  if (h->max_ctas > 0) g = std::min<int64_t>(g, h->max_ctas);
+  return (int)std::max<int64_t>(1, g);
 }
 
 cudaEvent_t take_event(onebit_adam* h) {
@@ -1216,6 +1218,12 @@ onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, 
       return ONEBIT_OK;
     default: return ONEBIT_ERR_INVALID_ARG;
   }
+}
+
+onebit_status_t onebit_adam_set_max_ctas(onebit_adam_t* h, int32_t max_ctas) {
+  if (!h || max_ctas < 0) return ONEBIT_ERR_INVALID_ARG;
+  h->max_ctas = max_ctas;
+  return ONEBIT_OK;
 }
 
 onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launches) {

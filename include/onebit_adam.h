@@ -211,6 +211,13 @@ onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launch
 onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enable);
 onebit_status_t onebit_adam_variance_norm(onebit_adam_t* h, double* norm, int64_t* step);
 
+/* Caps the CTAs that every streaming kernel launch of this handle uses (0, the default: as many as
+ * fill the GPU).  No counterpart on the method's pages: it lets a caller leave SMs to work running
+ * concurrently on other streams.  Results do not depend on it, bit for bit: every partial sum is
+ * per chunk and reduced in a fixed order, whatever the grid.  Negative values are
+ * ONEBIT_ERR_INVALID_ARG. */
+onebit_status_t onebit_adam_set_max_ctas(onebit_adam_t* h, int32_t max_ctas);
+
 /* Failure-detection test hooks; nothing here makes the GPU fault.
  *   ONEBIT_FAULT_STALL_COPIES makes the next steps' shared-memory staged kernels wait for `value`
  *     bytes (1..2^20) that no copy delivers, so that their bounded waits run out (about one second):

@@ -270,6 +270,87 @@ def test_allocation_failure_is_reported_and_changes_nothing():
     p.close()
 
 
+@pytest.mark.parametrize("numel,n,dtype", [((300_000,), 16, W.F16), ((70_001, 33, 0, 5, 4096), 16, W.F16),
+                                           ((50_000, 7), 33, W.BF16)],
+                         ids=["flat_n16_staged", "ragged_n16_runs", "n33_register"])
+def test_results_do_not_depend_on_the_grid(numel, n, dtype):
+    """The same schedule with every streaming launch capped at 1, 7 or 152 CTAs, or uncapped, leaves
+    bit-identical state: partial sums are per chunk and reduced in a fixed order, whatever the grid."""
+    w = _tiny(numel=numel, n_workers=n, grad_dtype=dtype, warmup_steps=2, seed=151)
+    src = W.GradSource(w, "cpu")
+    g = [[t.cuda() for t in src.grads(s)] for s in range(5)]
+    results = []
+    for cap in (0, 1, 7, 152):
+        params = [p.cuda() for p in W.params(w, "cpu")]
+        opt = ob.OneBitAdam(params, n, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr, grad_dtype=W.TORCH_DTYPE[dtype])
+        opt.set_max_ctas(cap)
+        opt.set_variance_monitor(True)
+        opt.warmup_step(g[0])
+        opt.warmup_step(g[1])
+        vnorm = opt.variance_norm()
+        opt.freeze_variance()
+        for s in range(2, 5):
+            opt.compress_step(g[s])
+        torch.cuda.synchronize()
+        assert opt.get_status() == ob.OK
+        st = _state(opt, n)
+        st["x"] = torch.cat(params).cpu().numpy()
+        results.append((st, vnorm))
+        opt.free()
+    ref, ref_norm = results[0]
+    for st, vnorm in results[1:]:
+        assert vnorm == ref_norm
+        for k in ref:
+            assert np.array_equal(st[k].view(np.uint8), ref[k].view(np.uint8)), k
+
+
+def test_guard_bands_untouched():
+    """Bounds: parameters, gradients and a caller-owned workspace sit between canary bands; a full
+    schedule (warm-up, freeze, compression, host-buffer steps, export) writes none of the bands and
+    never writes the gradients."""
+    w = _tiny(numel=(70_001, 33, 5, 4096), n_workers=16, grad_dtype=W.F16, warmup_steps=2, seed=161)
+    n, T = w.n_workers, w.n_tensors
+    G = 4096  # guard elements on each side (keeps 256-byte alignment)
+    dev = torch.device("cuda")
+
+    def guarded(values, fill):
+        buf = torch.full((values.numel() + 2 * G,), fill, dtype=values.dtype, device=dev)
+        buf[G:G + values.numel()].copy_(values.reshape(-1))
+        return buf, buf[G:G + values.numel()]
+
+    pbufs, params = zip(*[guarded(p.cuda(), float("nan")) for p in W.params(w, "cpu")])
+    ws_bytes = ob.workspace_size(ob.make_config(list(w.numel), n, w.warmup_steps, grad_dtype=ob.F16))
+    wsbuf = torch.full((ws_bytes + 2 * G,), 0xA5, dtype=torch.uint8, device=dev)
+    opt = ob.OneBitAdam(list(params), n, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr,
+                        grad_dtype=torch.float16, workspace=wsbuf[G:G + ws_bytes])
+    src = W.GradSource(w, "cpu")
+    gbufs_all = []
+    for step in range(6):
+        pairs = [guarded(t.cuda(), float("inf")) for t in src.grads(step)]
+        gbufs, grads = zip(*pairs)
+        before = [b.clone() for b in gbufs]
+        if step < 2:
+            opt.warmup_step(list(grads))
+        elif step < 4:
+            if step == 2:
+                opt.freeze_variance()
+            opt.compress_step(list(grads))
+        else:
+            opt.compress_step_host([t.cpu().pin_memory() for t in grads])
+        torch.cuda.synchronize()
+        for b, b0 in zip(gbufs, before):
+            assert torch.equal(b.view(torch.int16), b0.view(torch.int16)), "a gradient was written"
+        gbufs_all.append(gbufs)
+    for what in (ob.STATE_M, ob.STATE_V, ob.STATE_SERVER_ERROR, ob.STATE_SERVER_BITS, ob.STATE_WORKER_SCALES):
+        opt.export_state(what)
+    torch.cuda.synchronize()
+    assert opt.get_status() == ob.OK
+    for b in pbufs:
+        assert torch.isnan(b[:G]).all() and torch.isnan(b[-G:]).all(), "a parameter guard band was written"
+    assert bool((wsbuf[:G] == 0xA5).all()) and bool((wsbuf[-G:] == 0xA5).all()), "a workspace guard band was written"
+    opt.free()
+
+
 def test_timing_and_launch_counts():
     w = _tiny(numel=(50_000,), n_workers=4, warmup_steps=1)
     p = Pair(w)
