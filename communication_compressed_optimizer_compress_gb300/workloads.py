@@ -86,6 +86,8 @@ WORKLOADS = {
                                   warmup_steps=5, compress_steps=20, seed=3),
     "gpt2_1p5b": Workload("gpt2_1p5b", (1_560_000_000,), 4, BF16, "heavy_tail", warmup_steps=5,
                           compress_steps=20, seed=4),
+    # one flat buffer past 2^31 elements: checks that no element index is held in 32 bits
+    "over_2g": Workload("over_2g", (2_200_000_000,), 2, BF16, "iid", warmup_steps=2, compress_steps=2, seed=5),
 }
 
 BLOCK = 1 << 20

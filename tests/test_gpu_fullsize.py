@@ -177,6 +177,6 @@ def _run(name, compress_steps=2):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", ["bert_large", "bert_base", "ragged_bert_large", "gpt2_1p5b"])
+@pytest.mark.parametrize("name", ["bert_large", "bert_base", "ragged_bert_large", "gpt2_1p5b", "over_2g"])
 def test_full_size(name):
     _run(name)
