@@ -68,7 +68,7 @@ def _kernel_source_hash(marker: str):
     src = open(path).read()
     i = src.index(marker)
     consts = "\n".join(ln for ln in src[:i].splitlines() if ln.startswith("constexpr "))
-    j = src.index("// ------", i)
+    j = src.index("\n// " + "-" * 40, i)  # the next full-width section separator
     return hashlib.sha256((consts + src[i:j]).encode()).hexdigest()[:16]
 
 
