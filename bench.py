@@ -299,6 +299,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--d", type=int, default=0, help="override the parameter count (flat workloads)")
     ap.add_argument("--tw", type=int, default=-1, help="override the number of warm-up Adam steps")
+    ap.add_argument("--n", type=int, default=0, help="override the number of simulated workers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--step", default="compress", choices=["compress", "warmup", "ec_adam"],
@@ -321,6 +322,8 @@ def main():
         w = w.with_(numel=(args.d,))
     if args.tw >= 0:
         w = w.with_(warmup_steps=max(1, args.tw))
+    if args.n > 0:
+        w = w.with_(n_workers=args.n)
     if args.impl == "reference":
         return run_reference(args, w)
 
