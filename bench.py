@@ -466,17 +466,14 @@ def main():
         torch.cuda.synchronize()
 
         def link_probe():
-            """The host link itself: one pinned 1 GiB host-to-device copy, best of 3 (GB/s)."""
-            probe_h = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
-            probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-            best = float("inf")
-            for _ in range(3):
-                t0.record(stream)
-                probe_d.copy_(probe_h, non_blocking=True)
-                t1.record(stream)
-                torch.cuda.synchronize()
-                best = min(best, t0.elapsed_time(t1))
-            return (1 << 30) / (best / 1e3) / 1e9
+            """The host link at this moment: plain copies of this step's own host gradients into
+            device buffers of the same shapes (one stream, nothing else running), in GB/s."""
+            t0.record(stream)
+            for hb, db in zip(host, gsets[1]):
+                db.copy_(hb, non_blocking=True)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return h2d / (t0.elapsed_time(t1) / 1e3) / 1e9
 
         link_before = link_probe()
         barrier()
