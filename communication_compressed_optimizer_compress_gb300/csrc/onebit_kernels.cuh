@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
 
 constexpr int kTile = 4096;                 // elements per tile (two groups per consumer thread)
 constexpr int kStages = 2;                 // two stages leave room for three CTAs per SM
-constexpr int kStageMaxWorkers = 32;
+constexpr int kStageMaxWorkers = 128;         // two stages of n sign rows + a still fit (one CTA per SM at 128)
 constexpr int kRowBytes = kTile / 8 + 32;   // a 16-byte aligned window around the tile's sign bytes
 constexpr int kConsumerWarps = kThreads / 32;
 constexpr int kStagedThreads = kThreads + 32;      // consumers + one producer warp

@@ -34,6 +34,7 @@ ODD = [
     ([1], 1), ([31], 2), ([33], 3), ([32 * 4 - 1], 4), ([32 * 4 + 1], 4), ([(1 << 20) + 7], 8),
     ([1, 5, 32, 33], 3), ([5, 0, 33, 200], 4), ([65536 * 2 + 100, 7], 16), ([1000], 16),
     ([5000, 37], 20), ([3000, 2049], 33), ([777, 4100], 32), ([1000, 65], 17), ([300, 1], 256),
+    ([5000], 128), ([2000], 200),
 ]
 
 
@@ -43,8 +44,8 @@ def test_odd_sizes(numel, n, dtype):
     """Ragged tensors, tails that are not a multiple of 8 or 32, empty tensors and shards, several
     chunks per shard, worker counts that are not powers of two, all gradient dtypes.  The worker
     counts cover the server's paths: table only (n <= 12), table + ordered float4 adds (13..16),
-    further workers added one by one (17..32, staged kernel), the register kernel (33..256), and the
-    library's maximum n = 256."""
+    further workers added one by one (17..128, staged kernel), the register kernel (129..256, one
+    flat buffer; and short-tensor lists at any n), and the library's maximum n = 256."""
     w = _tiny(numel=tuple(numel), n_workers=n, grad_dtype=dtype, warmup_steps=2, compress_steps=3,
               seed=7 + n + len(numel))
     p = Pair(w)
