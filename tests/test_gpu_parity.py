@@ -352,6 +352,44 @@ def test_guard_bands_untouched():
     opt.free()
 
 
+@pytest.mark.parametrize("dtype", [W.F32, W.F16], ids=["f32", "f16"])
+def test_degenerate_inputs(dtype):
+    """Degenerate inputs, compared with the oracle bit for bit: all-zero and all-negative-zero
+    gradients (every c and a is a signed zero, every sign bit +1 by the sign(0) = +1 convention, all
+    scales 0, x unchanged), then gradients of one magnitude with a fixed sign pattern (compression
+    lossless, errors exactly 0)."""
+    w = _tiny(numel=(4096 + 13, 77), n_workers=4, grad_dtype=dtype, warmup_steps=2, seed=171)
+    p = Pair(w)
+    tdt = W.TORCH_DTYPE[dtype]
+    rng = np.random.default_rng(7)
+    signs = [np.where(rng.random(L) < 0.5, -1.0, 1.0) for L in w.numel]
+
+    def step(grads_np, kind):
+        dev = [torch.from_numpy(g).to(tdt).cuda() for g in grads_np]
+        host = [W.to_numpy_grad(torch.from_numpy(g).to(tdt)) for g in grads_np]
+        if kind == "warmup":
+            p.gpu.warmup_step(dev)
+            p.ora.warmup_step(host)
+        else:
+            p.gpu.compress_step(dev)
+            p.ora.compress_step(host)
+
+    zeros = [np.zeros(L, np.float32) for L in w.numel] * w.n_workers
+    negz = [np.full(L, -0.0, np.float32) for L in w.numel] * w.n_workers
+    const = [(s * 2.0 ** -7).astype(np.float32) for s in signs] * w.n_workers
+    step(zeros, "warmup")
+    step(negz, "warmup")
+    p.check_warmup(exact=True)
+    p.freeze()
+    for g in (zeros, negz, const, const, zeros):
+        step(g, "compress")
+        p.check_compress()
+    assert p.stats.excluded_worker == 0 and p.stats.excluded_server == 0
+    # after the zero steps every broadcast bit is +1; the constant steps compress losslessly
+    assert np.all(p.gpu.export_state(ob.STATE_WORKER_ERROR, 0).cpu().numpy() == p.ora.view("delta")[0])
+    p.close()
+
+
 def test_timing_and_launch_counts():
     w = _tiny(numel=(50_000,), n_workers=4, warmup_steps=1)
     p = Pair(w)
