@@ -121,11 +121,12 @@ def test_determinism():
         assert np.array_equal(res[0][k].view(np.uint8), res[1][k].view(np.uint8)), k
 
 
-def test_checkpoint_resume():
+@pytest.mark.parametrize("block", [0, 96], ids=["per_tensor", "blocks_96"])
+def test_checkpoint_resume(block):
     """Export the state after some steps, import it into a fresh handle, continue: the result is
-    identical to the uninterrupted run."""
+    identical to the uninterrupted run (also with per-block scales, whose exports are per block)."""
     w = _tiny(numel=(70_001, 33), n_workers=3, warmup_steps=2, compress_steps=4, seed=51)
-    ref = Pair(w)
+    ref = Pair(w, scale_block=block)
     for _ in range(2):
         ref.warmup(check=False)
     ref.freeze(check=False)
@@ -141,7 +142,7 @@ def test_checkpoint_resume():
     want_x = ref.x()
 
     params = [x.clone() for x in x_snap]
-    opt = ob.OneBitAdam(params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr)
+    opt = ob.OneBitAdam(params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr, scale_block=block)
     opt.set_step(2 + 2, ob.PHASE_COMPRESS)
     opt.import_state(ob.STATE_V, snap["v"])
     opt.import_state(ob.STATE_M, snap["m"])
