@@ -162,11 +162,13 @@ def test_checkpoint_resume(block):
     ref.close()
 
 
-def test_host_gradient_entry_points():
+@pytest.mark.parametrize("block", [0, 4096], ids=["per_tensor", "blocks_4096"])
+def test_host_gradient_entry_points(block):
     """warmup_step_host / compress_step_host (host buffers copied by the library) equal the
-    device-pointer entry points."""
+    device-pointer entry points, also when the library cuts the tensors into scale blocks after
+    staging them."""
     w = _tiny(numel=(10_007, 64), n_workers=2, grad_dtype=W.F16, warmup_steps=2, compress_steps=2, seed=61)
-    a, b = Pair(w), Pair(w)
+    a, b = Pair(w, scale_block=block), Pair(w, scale_block=block)
     for step in range(4):
         g = a.grads()
         b.grads()
