@@ -14,6 +14,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <string>
 #include <unordered_map>
 #include <unordered_set>
@@ -33,6 +34,7 @@ constexpr size_t kCopyPiece = size_t(64) << 20;  // and are cut into pieces of a
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t round32(int64_t v) { return (v + 31) / 32 * 32; }
+constexpr int64_t kMaxElements = int64_t(1) << 40;  // a parameter list's largest element count
 
 struct Plan {
   int n = 0, T = 0;               // T: compressed segments (the tensors, or their scale blocks)
@@ -79,6 +81,7 @@ onebit_status_t check_config(const onebit_adam_config_t* cfg) {
     total += cfg->numel[k];
   }
   if (total < 1) return ONEBIT_ERR_INVALID_ARG;
+  if (total > kMaxElements) return ONEBIT_ERR_UNSUPPORTED;  // far beyond any device's memory
   return ONEBIT_OK;
 }
 
@@ -107,13 +110,15 @@ onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
     const int64_t L = P->unumel[k];
     total += L;
     const int64_t B = P->split ? cfg->scale_block : std::max<int64_t>(L, 1);
+    const int64_t blocks = L > 0 ? (L + B - 1) / B : 1;
+    // checked before anything is built: a tiny block on a huge tensor must not exhaust host memory
+    if (((int64_t)P->numel.size() + blocks) * P->n > (int64_t)INT32_MAX) return ONEBIT_ERR_UNSUPPORTED;
     int64_t s = 0;
     do {
       P->numel.push_back(std::min<int64_t>(B, L - s));
       P->voff.push_back(s);
       s += B;
     } while (s < L);
-    if ((int64_t)P->numel.size() * P->n > (int64_t)INT32_MAX) return ONEBIT_ERR_UNSUPPORTED;
     P->ufirst.push_back((int32_t)P->numel.size());
   }
   P->T = (int)P->numel.size();
@@ -734,6 +739,19 @@ onebit_status_t release_stage(onebit_adam* h, int idx, cudaStream_t st) {
   return ONEBIT_OK;
 }
 
+// No exception may cross the C ABI: a host allocation that fails (std::bad_alloc) becomes
+// ONEBIT_ERR_NOMEM, anything else ONEBIT_ERR_INVALID_ARG.
+template <typename F>
+onebit_status_t guarded(F&& body) noexcept {
+  try {
+    return body();
+  } catch (const std::bad_alloc&) {
+    return ONEBIT_ERR_NOMEM;
+  } catch (...) {
+    return ONEBIT_ERR_INVALID_ARG;
+  }
+}
+
 }  // namespace
 
 // =================================================================================== C ABI
@@ -757,256 +775,285 @@ const char* onebit_adam_error_string(onebit_status_t s) {
 const char* onebit_adam_last_error(const onebit_adam_t* h) { return h ? h->last_error.c_str() : ""; }
 
 onebit_status_t onebit_adam_workspace_size(const onebit_adam_config_t* cfg, size_t* bytes) {
-  if (!bytes) return ONEBIT_ERR_INVALID_ARG;
-  onebit_status_t s = check_config(cfg);
-  if (s) return s;
-  Plan P;
-  if ((s = make_plan(cfg, &P))) return s;
-  *bytes = make_layout(P).total;
-  return ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!bytes) return ONEBIT_ERR_INVALID_ARG;
+    onebit_status_t s = check_config(cfg);
+    if (s) return s;
+    Plan P;
+    if ((s = make_plan(cfg, &P))) return s;
+    *bytes = make_layout(P).total;
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_plan_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap, int64_t* count) {
-  if (!count || (cap > 0 && !rows)) return ONEBIT_ERR_INVALID_ARG;
-  onebit_status_t s = check_config(cfg);
-  if (s) return s;
-  Plan P;
-  if ((s = make_plan(cfg, &P))) return s;
-  *count = (int64_t)P.chunks.size();
-  for (int64_t q = 0; q < std::min<int64_t>(cap, *count); ++q) {
-    const Chunk& c = P.chunks[q];
-    rows[q * 5 + 0] = c.seg;
-    rows[q * 5 + 1] = c.shard;
-    rows[q * 5 + 2] = c.start;
-    rows[q * 5 + 3] = c.len;
-    rows[q * 5 + 4] = c.off;
-  }
-  return ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!count || (cap > 0 && !rows)) return ONEBIT_ERR_INVALID_ARG;
+    onebit_status_t s = check_config(cfg);
+    if (s) return s;
+    Plan P;
+    if ((s = make_plan(cfg, &P))) return s;
+    *count = (int64_t)P.chunks.size();
+    for (int64_t q = 0; q < std::min<int64_t>(cap, *count); ++q) {
+      const Chunk& c = P.chunks[q];
+      rows[q * 5 + 0] = c.seg;
+      rows[q * 5 + 1] = c.shard;
+      rows[q * 5 + 2] = c.start;
+      rows[q * 5 + 3] = c.len;
+      rows[q * 5 + 4] = c.off;
+    }
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_plan_worker_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap,
                                                int64_t* count) {
-  if (!count || (cap > 0 && !rows)) return ONEBIT_ERR_INVALID_ARG;
-  onebit_status_t s = check_config(cfg);
-  if (s) return s;
-  Plan P;
-  if ((s = make_plan(cfg, &P))) return s;
-  *count = (int64_t)P.wchunks.size();
-  for (int64_t q = 0; q < std::min<int64_t>(cap, *count); ++q) {
-    const Chunk& c = P.wchunks[q];
-    rows[q * 6 + 0] = c.seg;
-    rows[q * 6 + 1] = c.shard;
-    rows[q * 6 + 2] = c.start;
-    rows[q * 6 + 3] = c.len;
-    rows[q * 6 + 4] = c.off;
-    rows[q * 6 + 5] = c.per;
-  }
-  return ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!count || (cap > 0 && !rows)) return ONEBIT_ERR_INVALID_ARG;
+    onebit_status_t s = check_config(cfg);
+    if (s) return s;
+    Plan P;
+    if ((s = make_plan(cfg, &P))) return s;
+    *count = (int64_t)P.wchunks.size();
+    for (int64_t q = 0; q < std::min<int64_t>(cap, *count); ++q) {
+      const Chunk& c = P.wchunks[q];
+      rows[q * 6 + 0] = c.seg;
+      rows[q * 6 + 1] = c.shard;
+      rows[q * 6 + 2] = c.start;
+      rows[q * 6 + 3] = c.len;
+      rows[q * 6 + 4] = c.off;
+      rows[q * 6 + 5] = c.per;
+    }
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* params, void* workspace,
                                  size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out) {
-  NvtxRange trace("onebit_adam_init");
-  if (!out || !params) return ONEBIT_ERR_INVALID_ARG;
-  *out = nullptr;
-  onebit_status_t s = check_config(cfg);
-  if (s) return s;
-  for (int k = 0; k < cfg->n_tensors; ++k)
-    if (!params[k] && cfg->numel[k] > 0) return ONEBIT_ERR_INVALID_ARG;
-  if (workspace && !aligned(workspace, kAlign)) return ONEBIT_ERR_WORKSPACE;
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_init");
+    if (!out || !params) return ONEBIT_ERR_INVALID_ARG;
+    *out = nullptr;
+    onebit_status_t s = check_config(cfg);
+    if (s) return s;
+    for (int k = 0; k < cfg->n_tensors; ++k)
+      if (!params[k] && cfg->numel[k] > 0) return ONEBIT_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, kAlign)) return ONEBIT_ERR_WORKSPACE;
 
-  onebit_adam* h = new (std::nothrow) onebit_adam();
-  if (!h) return ONEBIT_ERR_NOMEM;
-  h->cfg = *cfg;
-  if ((s = make_plan(cfg, &h->plan))) {
-    delete h;
-    return s;
-  }
-  h->cfg.numel = nullptr;  // the plan keeps its own copy
-  h->lay = make_layout(h->plan);
-  if (workspace && workspace_bytes < h->lay.total) {
-    delete h;
-    return ONEBIT_ERR_WORKSPACE;
-  }
-  cudaStream_t st = as_stream(stream);
-  auto fail = [&](onebit_status_t code) {
-    onebit_adam_free(h);
-    return code;
-  };
-  if (cudaGetDevice(&h->device) != cudaSuccess) return fail(cuda_fail(h, cudaGetLastError(), "cudaGetDevice"));
-  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
-    return fail(cuda_fail(h, cudaGetLastError(), "cudaDeviceGetAttribute"));
-  if (workspace) {
-    h->ws = static_cast<uint8_t*>(workspace);
-  } else {
-    if (cudaMalloc(&h->ws, h->lay.total) != cudaSuccess) {
-      cudaGetLastError();
-      h->ws = nullptr;
-      return fail(ONEBIT_ERR_NOMEM);
+    Plan plan;  // built before the handle, so that a failure here leaves nothing to release
+    if ((s = make_plan(cfg, &plan))) return s;
+    onebit_adam* h = new (std::nothrow) onebit_adam();
+    if (!h) return ONEBIT_ERR_NOMEM;
+    // from here on every exit but success releases the handle (an exception included)
+    struct Release {
+      onebit_adam* h;
+      bool cuda;  // the handle holds CUDA resources: free it through onebit_adam_free
+      ~Release() {
+        if (h && cuda) onebit_adam_free(h);
+        else delete h;
+      }
+    } release{h, false};
+    h->cfg = *cfg;
+    h->plan = std::move(plan);
+    h->cfg.numel = nullptr;  // the plan keeps its own copy
+    h->lay = make_layout(h->plan);
+    if (workspace && workspace_bytes < h->lay.total) return ONEBIT_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    release.cuda = true;
+    if (cudaGetDevice(&h->device) != cudaSuccess) return cuda_fail(h, cudaGetLastError(), "cudaGetDevice");
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
+      return cuda_fail(h, cudaGetLastError(), "cudaDeviceGetAttribute");
+    if (workspace) {
+      h->ws = static_cast<uint8_t*>(workspace);
+    } else {
+      if (cudaMalloc(&h->ws, h->lay.total) != cudaSuccess) {
+        cudaGetLastError();
+        h->ws = nullptr;
+        return ONEBIT_ERR_NOMEM;
+      }
+      h->ws_owned = true;
     }
-    h->ws_owned = true;
-  }
-  h->params.resize(h->plan.T);
-  for (int k = 0; k < h->plan.Tu; ++k)
-    for (int v = h->plan.ufirst[k]; v < h->plan.ufirst[k + 1]; ++v)
-      h->params[v] = params[k] ? params[k] + h->plan.voff[v] : nullptr;
-  h->params_aligned = true;
-  for (float* p : h->params)
-    if (!aligned(p, 32)) h->params_aligned = false;
-  h->ring.assign(kPtrRing, {});
+    h->params.resize(h->plan.T);
+    for (int k = 0; k < h->plan.Tu; ++k)
+      for (int v = h->plan.ufirst[k]; v < h->plan.ufirst[k + 1]; ++v)
+        h->params[v] = params[k] ? params[k] + h->plan.voff[v] : nullptr;
+    h->params_aligned = true;
+    for (float* p : h->params)
+      if (!aligned(p, 32)) h->params_aligned = false;
+    h->ring.assign(kPtrRing, {});
 
-  // zero every piece of state, then upload the tables
-  if (cudaMemsetAsync(h->ws, 0, h->lay.total, st) != cudaSuccess)
-    return fail(cuda_fail(h, cudaGetLastError(), "cudaMemsetAsync"));
-  const Plan& P = h->plan;
-  std::vector<uint8_t> tables(h->lay.gptr - h->lay.chunks);
-  std::memcpy(tables.data(), P.chunks.data(), P.chunks.size() * sizeof(Chunk));
-  std::memcpy(tables.data() + (h->lay.seg_ranges - h->lay.chunks), P.seg_ranges.data(), P.T * sizeof(Range));
-  std::memcpy(tables.data() + (h->lay.shard_ranges - h->lay.chunks), P.shard_ranges.data(),
-              (size_t)P.T * P.n * sizeof(Range));
-  std::memcpy(tables.data() + (h->lay.wchunks - h->lay.chunks), P.wchunks.data(), P.wchunks.size() * sizeof(Chunk));
-  std::memcpy(tables.data() + (h->lay.wseg_ranges - h->lay.chunks), P.wseg_ranges.data(), P.T * sizeof(Range));
-  if (cudaMemcpyAsync(h->ws + h->lay.chunks, tables.data(), tables.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return fail(cuda_fail(h, cudaGetLastError(), "upload tables"));
-  if (cudaMemcpyAsync(h->ws + h->lay.pptr, h->params.data(), P.T * sizeof(float*), cudaMemcpyHostToDevice, st) !=
-      cudaSuccess)
-    return fail(cuda_fail(h, cudaGetLastError(), "upload params"));
-  // the pageable sources above are staged before the copies return; wait anyway so that the
-  // tables vector may go out of scope with no doubt
-  if (cudaStreamSynchronize(st) != cudaSuccess) return fail(cuda_fail(h, cudaGetLastError(), "init sync"));
-  *out = h;
-  return ONEBIT_OK;
+    // zero every piece of state, then upload the tables
+    if (cudaMemsetAsync(h->ws, 0, h->lay.total, st) != cudaSuccess)
+      return cuda_fail(h, cudaGetLastError(), "cudaMemsetAsync");
+    const Plan& P = h->plan;
+    std::vector<uint8_t> tables(h->lay.gptr - h->lay.chunks);
+    std::memcpy(tables.data(), P.chunks.data(), P.chunks.size() * sizeof(Chunk));
+    std::memcpy(tables.data() + (h->lay.seg_ranges - h->lay.chunks), P.seg_ranges.data(), P.T * sizeof(Range));
+    std::memcpy(tables.data() + (h->lay.shard_ranges - h->lay.chunks), P.shard_ranges.data(),
+                (size_t)P.T * P.n * sizeof(Range));
+    std::memcpy(tables.data() + (h->lay.wchunks - h->lay.chunks), P.wchunks.data(), P.wchunks.size() * sizeof(Chunk));
+    std::memcpy(tables.data() + (h->lay.wseg_ranges - h->lay.chunks), P.wseg_ranges.data(), P.T * sizeof(Range));
+    if (cudaMemcpyAsync(h->ws + h->lay.chunks, tables.data(), tables.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return cuda_fail(h, cudaGetLastError(), "upload tables");
+    if (cudaMemcpyAsync(h->ws + h->lay.pptr, h->params.data(), P.T * sizeof(float*), cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+      return cuda_fail(h, cudaGetLastError(), "upload params");
+    // the pageable sources above are staged before the copies return; wait anyway so that the
+    // tables vector may go out of scope with no doubt
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_fail(h, cudaGetLastError(), "init sync");
+    release.h = nullptr;  // success: the caller owns the handle
+    *out = h;
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_free(onebit_adam_t* h) {
-  if (!h) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  cudaDeviceSynchronize();
-  for (auto& tl : h->timed) {
-    cudaEventDestroy(tl.start);
-    cudaEventDestroy(tl.stop);
-  }
-  for (auto e : h->event_pool) cudaEventDestroy(e);
-  if (h->ws_owned && h->ws) cudaFree(h->ws);
-  if (h->vnorm_host) cudaFreeHost(h->vnorm_host);
-  if (h->ev_vnorm) cudaEventDestroy(h->ev_vnorm);
-  for (int b = 0; b < 2; ++b) {
-    if (h->staging[b]) cudaFree(h->staging[b]);
-    if (h->ev_free[b]) cudaEventDestroy(h->ev_free[b]);
-  }
-  for (int c = 0; c < kCopyStreams; ++c) {
-    if (h->copy_st[c]) cudaStreamDestroy(h->copy_st[c]);
-    if (h->ev_copied[c]) cudaEventDestroy(h->ev_copied[c]);
-  }
-  delete h;
-  return ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!h) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    for (auto& tl : h->timed) {
+      cudaEventDestroy(tl.start);
+      cudaEventDestroy(tl.stop);
+    }
+    for (auto e : h->event_pool) cudaEventDestroy(e);
+    if (h->ws_owned && h->ws) cudaFree(h->ws);
+    if (h->vnorm_host) cudaFreeHost(h->vnorm_host);
+    if (h->ev_vnorm) cudaEventDestroy(h->ev_vnorm);
+    for (int b = 0; b < 2; ++b) {
+      if (h->staging[b]) cudaFree(h->staging[b]);
+      if (h->ev_free[b]) cudaEventDestroy(h->ev_free[b]);
+    }
+    for (int c = 0; c < kCopyStreams; ++c) {
+      if (h->copy_st[c]) cudaStreamDestroy(h->copy_st[c]);
+      if (h->ev_copied[c]) cudaEventDestroy(h->ev_copied[c]);
+    }
+    delete h;
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_warmup_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
-  NvtxRange trace("onebit_adam_warmup_step");
-  if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  return do_warmup(h, grads, as_stream(stream));
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_warmup_step");
+    if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    return do_warmup(h, grads, as_stream(stream));
+  });
 }
 
 onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
-  NvtxRange trace("onebit_adam_compress_step");
-  if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  return do_compress(h, grads, as_stream(stream));
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_compress_step");
+    if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    return do_compress(h, grads, as_stream(stream));
+  });
 }
 
 onebit_status_t onebit_adam_ec_adam_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream) {
-  NvtxRange trace("onebit_adam_ec_adam_step");
-  if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  return do_compress(h, grads, as_stream(stream), true);
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_ec_adam_step");
+    if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    return do_compress(h, grads, as_stream(stream), true);
+  });
 }
 
 onebit_status_t onebit_adam_warmup_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream) {
-  NvtxRange trace("onebit_adam_warmup_step_host");
-  if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
-  if (h->phase != ONEBIT_PHASE_WARMUP || h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
-  DeviceGuard g(h->device);
-  std::vector<const void*> dev;
-  int idx = 0;
-  onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev, &idx);
-  if (s) return s;
-  s = do_warmup(h, dev.data(), as_stream(stream));
-  const onebit_status_t r = release_stage(h, idx, as_stream(stream));
-  return s ? s : r;
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_warmup_step_host");
+    if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
+    if (h->phase != ONEBIT_PHASE_WARMUP || h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
+    DeviceGuard g(h->device);
+    std::vector<const void*> dev;
+    int idx = 0;
+    onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev, &idx);
+    if (s) return s;
+    s = do_warmup(h, dev.data(), as_stream(stream));
+    const onebit_status_t r = release_stage(h, idx, as_stream(stream));
+    return s ? s : r;
+  });
 }
 
 onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* const* host_grads, onebit_stream_t stream) {
-  NvtxRange trace("onebit_adam_compress_step_host");
-  if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
-  if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
-  DeviceGuard g(h->device);
-  std::vector<const void*> dev;
-  int idx = 0;
-  onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev, &idx);
-  if (s) return s;
-  s = do_compress(h, dev.data(), as_stream(stream));
-  const onebit_status_t r = release_stage(h, idx, as_stream(stream));
-  return s ? s : r;
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_compress_step_host");
+    if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
+    if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+    DeviceGuard g(h->device);
+    std::vector<const void*> dev;
+    int idx = 0;
+    onebit_status_t s = stage_copy(h, host_grads, as_stream(stream), &dev, &idx);
+    if (s) return s;
+    s = do_compress(h, dev.data(), as_stream(stream));
+    const onebit_status_t r = release_stage(h, idx, as_stream(stream));
+    return s ? s : r;
+  });
 }
 
 onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t stream) {
-  NvtxRange trace("onebit_adam_freeze_variance");
-  if (!h) return ONEBIT_ERR_INVALID_ARG;
-  if (h->phase != ONEBIT_PHASE_WARMUP || h->t < 1) return ONEBIT_ERR_PHASE;
-  DeviceGuard g(h->device);
-  cudaStream_t st = as_stream(stream);
-  const int64_t groups = h->plan.Dp / 8;
-  const float bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)h->t));
-  float* v = h->at<float>(h->lay.v);
-  onebit_status_t s;
-  auto go = [&](auto kern) -> onebit_status_t {
-    TimedLaunch tl{ONEBIT_K_FREEZE, nullptr, nullptr};
-    if (h->timing) {
-      tl.start = take_event(h);
-      tl.stop = take_event(h);
-      if (tl.start) cudaEventRecord(tl.start, st);
-    }
-    const int grid = grid_for(h, (const void*)kern, kThreads, (groups + kThreads - 1) / kThreads);
-    kern<<<grid, kThreads, 0, st>>>(v, groups, bc2, h->cfg.eps);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(h, e, "freeze launch");
-    ++h->launches;
-    if (h->timing && tl.start && tl.stop) {
-      cudaEventRecord(tl.stop, st);
-      h->timed.push_back(tl);
-    }
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_freeze_variance");
+    if (!h) return ONEBIT_ERR_INVALID_ARG;
+    if (h->phase != ONEBIT_PHASE_WARMUP || h->t < 1) return ONEBIT_ERR_PHASE;
+    DeviceGuard g(h->device);
+    cudaStream_t st = as_stream(stream);
+    const int64_t groups = h->plan.Dp / 8;
+    const float bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)h->t));
+    float* v = h->at<float>(h->lay.v);
+    onebit_status_t s;
+    auto go = [&](auto kern) -> onebit_status_t {
+      TimedLaunch tl{ONEBIT_K_FREEZE, nullptr, nullptr};
+      if (h->timing) {
+        tl.start = take_event(h);
+        tl.stop = take_event(h);
+        if (tl.start) cudaEventRecord(tl.start, st);
+      }
+      const int grid = grid_for(h, (const void*)kern, kThreads, (groups + kThreads - 1) / kThreads);
+      kern<<<grid, kThreads, 0, st>>>(v, groups, bc2, h->cfg.eps);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(h, e, "freeze launch");
+      ++h->launches;
+      if (h->timing && tl.start && tl.stop) {
+        cudaEventRecord(tl.stop, st);
+        h->timed.push_back(tl);
+      }
+      return ONEBIT_OK;
+    };
+    s = h->cfg.bias_correction ? go(k_freeze<true>) : go(k_freeze<false>);
+    if (s) return s;
+    h->phase = ONEBIT_PHASE_COMPRESS;
+    h->m_dense = true;
+    h->werr_zero = true;
+    h->serr_zero = true;
     return ONEBIT_OK;
-  };
-  s = h->cfg.bias_correction ? go(k_freeze<true>) : go(k_freeze<false>);
-  if (s) return s;
-  h->phase = ONEBIT_PHASE_COMPRESS;
-  h->m_dense = true;
-  h->werr_zero = true;
-  h->serr_zero = true;
-  return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_get_status(onebit_adam_t* h, onebit_stream_t stream) {
-  if (!h) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  unsigned int flag = 0;
-  cudaStream_t st = as_stream(stream);
-  ONEBIT_CUDA(h, cudaMemcpyAsync(&flag, h->ws + h->lay.status, sizeof flag, cudaMemcpyDeviceToHost, st));
-  ONEBIT_CUDA(h, cudaStreamSynchronize(st));
-  if (flag & 2u) {
-    h->last_error = "a kernel's wait for its asynchronous copies timed out";
-    return ONEBIT_ERR_CUDA;
-  }
-  return flag ? ONEBIT_ERR_NONFINITE : ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!h) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    unsigned int flag = 0;
+    cudaStream_t st = as_stream(stream);
+    ONEBIT_CUDA(h, cudaMemcpyAsync(&flag, h->ws + h->lay.status, sizeof flag, cudaMemcpyDeviceToHost, st));
+    ONEBIT_CUDA(h, cudaStreamSynchronize(st));
+    if (flag & 2u) {
+      h->last_error = "a kernel's wait for its asynchronous copies timed out";
+      return ONEBIT_ERR_CUDA;
+    }
+    return flag ? ONEBIT_ERR_NONFINITE : ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_clear_status(onebit_adam_t* h, onebit_stream_t stream) {
-  if (!h) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  ONEBIT_CUDA(h, cudaMemsetAsync(h->ws + h->lay.status, 0, sizeof(unsigned int), as_stream(stream)));
-  return ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!h) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    ONEBIT_CUDA(h, cudaMemsetAsync(h->ws + h->lay.status, 0, sizeof(unsigned int), as_stream(stream)));
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_get_step(const onebit_adam_t* h, int64_t* t, int32_t* phase) {
@@ -1017,21 +1064,23 @@ onebit_status_t onebit_adam_get_step(const onebit_adam_t* h, int64_t* t, int32_t
 }
 
 onebit_status_t onebit_adam_set_step(onebit_adam_t* h, int64_t t, int32_t phase, onebit_stream_t stream) {
-  if (!h || t < 0) return ONEBIT_ERR_INVALID_ARG;
-  if (phase == ONEBIT_PHASE_WARMUP) {
-    if (t >= h->cfg.warmup_steps) return ONEBIT_ERR_INVALID_ARG;
-  } else if (phase == ONEBIT_PHASE_COMPRESS) {
-    if (t < 1) return ONEBIT_ERR_INVALID_ARG;
-    h->m_dense = true;
-    h->werr_zero = true;
-    h->serr_zero = true;
-  } else {
-    return ONEBIT_ERR_INVALID_ARG;
-  }
-  (void)stream;
-  h->t = t;
-  h->phase = phase;
-  return ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!h || t < 0) return ONEBIT_ERR_INVALID_ARG;
+    if (phase == ONEBIT_PHASE_WARMUP) {
+      if (t >= h->cfg.warmup_steps) return ONEBIT_ERR_INVALID_ARG;
+    } else if (phase == ONEBIT_PHASE_COMPRESS) {
+      if (t < 1) return ONEBIT_ERR_INVALID_ARG;
+      h->m_dense = true;
+      h->werr_zero = true;
+      h->serr_zero = true;
+    } else {
+      return ONEBIT_ERR_INVALID_ARG;
+    }
+    (void)stream;
+    h->t = t;
+    h->phase = phase;
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_state_size(const onebit_adam_t* h, int32_t what, size_t* bytes) {
@@ -1051,88 +1100,92 @@ onebit_status_t onebit_adam_state_size(const onebit_adam_t* h, int32_t what, siz
 }
 
 onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worker, void* dst, onebit_stream_t stream) {
-  NvtxRange trace("onebit_adam_export");
-  if (!h || !dst) return ONEBIT_ERR_INVALID_ARG;
-  const Plan& P = h->plan;
-  const bool per_worker = what == ONEBIT_STATE_WORKER_ERROR || what == ONEBIT_STATE_WORKER_BITS;
-  if (per_worker && (worker < 0 || worker >= P.n)) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  cudaStream_t st = as_stream(stream);
-  float* out = static_cast<float*>(dst);
-  switch (what) {
-    case ONEBIT_STATE_M: return export_m(h, out, st);
-    case ONEBIT_STATE_V: return run_export(h, kExportCopy, h->at<float>(h->lay.v), nullptr, nullptr, 0, 0, out, st);
-    case ONEBIT_STATE_WORKER_ERROR:
-      if (h->werr_zero)
-        return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
-      return run_export(h, kExportSignedErr, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, nullptr,
-                        last_wscale(h) + (size_t)worker * P.T, 1, 0, out, st);
-    case ONEBIT_STATE_SERVER_ERROR:
-      if (h->serr_zero)
-        return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
-      return run_export(h, kExportSignedErr, h->at<float>(h->lay.a), nullptr, last_sscale(h), P.n, 1, out, st);
-    case ONEBIT_STATE_WORKER_BITS:
-      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.wbits) + (size_t)worker * P.Wr, P.Wp * 4,
-                                     cudaMemcpyDeviceToDevice, st));
-      return ONEBIT_OK;
-    case ONEBIT_STATE_SERVER_BITS:
-      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.sbits), P.Wp * 4, cudaMemcpyDeviceToDevice, st));
-      return ONEBIT_OK;
-    case ONEBIT_STATE_WORKER_SCALES:
-      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, last_wscale(h), (size_t)P.n * P.T * 4, cudaMemcpyDeviceToDevice, st));
-      return ONEBIT_OK;
-    case ONEBIT_STATE_SERVER_SCALES:
-      ONEBIT_CUDA(h, cudaMemcpyAsync(dst, last_sscale(h), (size_t)P.n * P.T * 4, cudaMemcpyDeviceToDevice, st));
-      return ONEBIT_OK;
-    default: return ONEBIT_ERR_INVALID_ARG;
-  }
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_export");
+    if (!h || !dst) return ONEBIT_ERR_INVALID_ARG;
+    const Plan& P = h->plan;
+    const bool per_worker = what == ONEBIT_STATE_WORKER_ERROR || what == ONEBIT_STATE_WORKER_BITS;
+    if (per_worker && (worker < 0 || worker >= P.n)) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    cudaStream_t st = as_stream(stream);
+    float* out = static_cast<float*>(dst);
+    switch (what) {
+      case ONEBIT_STATE_M: return export_m(h, out, st);
+      case ONEBIT_STATE_V: return run_export(h, kExportCopy, h->at<float>(h->lay.v), nullptr, nullptr, 0, 0, out, st);
+      case ONEBIT_STATE_WORKER_ERROR:
+        if (h->werr_zero)
+          return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
+        return run_export(h, kExportSignedErr, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, nullptr,
+                          last_wscale(h) + (size_t)worker * P.T, 1, 0, out, st);
+      case ONEBIT_STATE_SERVER_ERROR:
+        if (h->serr_zero)
+          return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
+        return run_export(h, kExportSignedErr, h->at<float>(h->lay.a), nullptr, last_sscale(h), P.n, 1, out, st);
+      case ONEBIT_STATE_WORKER_BITS:
+        ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.wbits) + (size_t)worker * P.Wr, P.Wp * 4,
+                                       cudaMemcpyDeviceToDevice, st));
+        return ONEBIT_OK;
+      case ONEBIT_STATE_SERVER_BITS:
+        ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.sbits), P.Wp * 4, cudaMemcpyDeviceToDevice, st));
+        return ONEBIT_OK;
+      case ONEBIT_STATE_WORKER_SCALES:
+        ONEBIT_CUDA(h, cudaMemcpyAsync(dst, last_wscale(h), (size_t)P.n * P.T * 4, cudaMemcpyDeviceToDevice, st));
+        return ONEBIT_OK;
+      case ONEBIT_STATE_SERVER_SCALES:
+        ONEBIT_CUDA(h, cudaMemcpyAsync(dst, last_sscale(h), (size_t)P.n * P.T * 4, cudaMemcpyDeviceToDevice, st));
+        return ONEBIT_OK;
+      default: return ONEBIT_ERR_INVALID_ARG;
+    }
+  });
 }
 
 onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worker, const void* src, onebit_stream_t stream) {
-  NvtxRange trace("onebit_adam_import");
-  if (!h || !src) return ONEBIT_ERR_INVALID_ARG;
-  const Plan& P = h->plan;
-  DeviceGuard g(h->device);
-  cudaStream_t st = as_stream(stream);
-  const float* in = static_cast<const float*>(src);
-  const size_t nt = (size_t)P.n * P.T;
-  onebit_status_t s;
-  switch (what) {
-    case ONEBIT_STATE_M:
-      if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.m), st))) return s;
-      h->m_dense = true;
-      return ONEBIT_OK;
-    case ONEBIT_STATE_V:
-      return run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.v), st);
-    case ONEBIT_STATE_WORKER_ERROR: {
-      if (worker < 0 || worker >= P.n) return ONEBIT_ERR_INVALID_ARG;
-      if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
-      float* ws_prev = last_wscale(h);  // what the next step reads as the previous scales
-      if (h->werr_zero) {
-        ONEBIT_CUDA(h, cudaMemsetAsync(h->at<float>(h->lay.c), 0, (size_t)P.n * P.Dp * 4, st));
-        ONEBIT_CUDA(h, cudaMemsetAsync(ws_prev, 0, nt * 4, st));
-        h->werr_zero = false;
-      }
-      // store delta as c with a zero scale: the next step rebuilds c - 0*sign(c) = delta exactly
-      if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, st)))
-        return s;
-      ONEBIT_CUDA(h, cudaMemsetAsync(ws_prev + (size_t)worker * P.T, 0, (size_t)P.T * 4, st));
-      return ONEBIT_OK;
-    }
-    case ONEBIT_STATE_SERVER_ERROR: {
-      if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
-      if (!h->m_dense) {  // m is carried by the server scales about to be zeroed: materialise it
-        if ((s = export_m(h, h->at<float>(h->lay.m), st))) return s;
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_import");
+    if (!h || !src) return ONEBIT_ERR_INVALID_ARG;
+    const Plan& P = h->plan;
+    DeviceGuard g(h->device);
+    cudaStream_t st = as_stream(stream);
+    const float* in = static_cast<const float*>(src);
+    const size_t nt = (size_t)P.n * P.T;
+    onebit_status_t s;
+    switch (what) {
+      case ONEBIT_STATE_M:
+        if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.m), st))) return s;
         h->m_dense = true;
+        return ONEBIT_OK;
+      case ONEBIT_STATE_V:
+        return run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.v), st);
+      case ONEBIT_STATE_WORKER_ERROR: {
+        if (worker < 0 || worker >= P.n) return ONEBIT_ERR_INVALID_ARG;
+        if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+        float* ws_prev = last_wscale(h);  // what the next step reads as the previous scales
+        if (h->werr_zero) {
+          ONEBIT_CUDA(h, cudaMemsetAsync(h->at<float>(h->lay.c), 0, (size_t)P.n * P.Dp * 4, st));
+          ONEBIT_CUDA(h, cudaMemsetAsync(ws_prev, 0, nt * 4, st));
+          h->werr_zero = false;
+        }
+        // store delta as c with a zero scale: the next step rebuilds c - 0*sign(c) = delta exactly
+        if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, st)))
+          return s;
+        ONEBIT_CUDA(h, cudaMemsetAsync(ws_prev + (size_t)worker * P.T, 0, (size_t)P.T * 4, st));
+        return ONEBIT_OK;
       }
-      // store eps as a with a zero scale: the next step rebuilds a - 0*sign(a) = eps exactly
-      if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.a), st))) return s;
-      ONEBIT_CUDA(h, cudaMemsetAsync(last_sscale(h), 0, nt * 4, st));
-      h->serr_zero = false;
-      return ONEBIT_OK;
+      case ONEBIT_STATE_SERVER_ERROR: {
+        if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+        if (!h->m_dense) {  // m is carried by the server scales about to be zeroed: materialise it
+          if ((s = export_m(h, h->at<float>(h->lay.m), st))) return s;
+          h->m_dense = true;
+        }
+        // store eps as a with a zero scale: the next step rebuilds a - 0*sign(a) = eps exactly
+        if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.a), st))) return s;
+        ONEBIT_CUDA(h, cudaMemsetAsync(last_sscale(h), 0, nt * 4, st));
+        h->serr_zero = false;
+        return ONEBIT_OK;
+      }
+      default: return ONEBIT_ERR_INVALID_ARG;
     }
-    default: return ONEBIT_ERR_INVALID_ARG;
-  }
+  });
 }
 
 onebit_status_t onebit_adam_comm_bytes(const onebit_adam_t* h, uint64_t* compressed, uint64_t* fp32_bytes) {
@@ -1148,57 +1201,65 @@ onebit_status_t onebit_adam_comm_bytes(const onebit_adam_t* h, uint64_t* compres
 }
 
 onebit_status_t onebit_adam_set_timing(onebit_adam_t* h, int32_t enable) {
-  if (!h) return ONEBIT_ERR_INVALID_ARG;
-  h->timing = enable != 0;
-  return ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!h) return ONEBIT_ERR_INVALID_ARG;
+    h->timing = enable != 0;
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_kernel_times(onebit_adam_t* h, double* ms, int64_t* launches) {
-  if (!h || !ms || !launches) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  for (int k = 0; k < ONEBIT_NUM_KERNELS; ++k) {
-    ms[k] = 0.0;
-    launches[k] = 0;
-  }
-  onebit_status_t rc = ONEBIT_OK;
-  for (auto& tl : h->timed) {
-    float t = 0.0f;
-    if (cudaEventSynchronize(tl.stop) != cudaSuccess || cudaEventElapsedTime(&t, tl.start, tl.stop) != cudaSuccess)
-      rc = cuda_fail(h, cudaGetLastError(), "kernel timing");
-    ms[tl.kernel] += t;
-    launches[tl.kernel] += 1;
-    h->event_pool.push_back(tl.start);
-    h->event_pool.push_back(tl.stop);
-  }
-  h->timed.clear();
-  return rc;
+  return guarded([&]() -> onebit_status_t {
+    if (!h || !ms || !launches) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    for (int k = 0; k < ONEBIT_NUM_KERNELS; ++k) {
+      ms[k] = 0.0;
+      launches[k] = 0;
+    }
+    onebit_status_t rc = ONEBIT_OK;
+    for (auto& tl : h->timed) {
+      float t = 0.0f;
+      if (cudaEventSynchronize(tl.stop) != cudaSuccess || cudaEventElapsedTime(&t, tl.start, tl.stop) != cudaSuccess)
+        rc = cuda_fail(h, cudaGetLastError(), "kernel timing");
+      ms[tl.kernel] += t;
+      launches[tl.kernel] += 1;
+      h->event_pool.push_back(tl.start);
+      h->event_pool.push_back(tl.stop);
+    }
+    h->timed.clear();
+    return rc;
+  });
 }
 
 onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enable) {
-  if (!h) return ONEBIT_ERR_INVALID_ARG;
-  DeviceGuard g(h->device);
-  if (enable && !h->vnorm_host) {
-    if (refuse_alloc(h) ||
-        cudaHostAlloc(reinterpret_cast<void**>(&h->vnorm_host), sizeof(double), cudaHostAllocDefault) != cudaSuccess) {
-      cudaGetLastError();
-      h->vnorm_host = nullptr;
-      return ONEBIT_ERR_NOMEM;
+  return guarded([&]() -> onebit_status_t {
+    if (!h) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (enable && !h->vnorm_host) {
+      if (refuse_alloc(h) ||
+          cudaHostAlloc(reinterpret_cast<void**>(&h->vnorm_host), sizeof(double), cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        h->vnorm_host = nullptr;
+        return ONEBIT_ERR_NOMEM;
+      }
+      *h->vnorm_host = 0.0;
+      ONEBIT_CUDA(h, cudaEventCreateWithFlags(&h->ev_vnorm, cudaEventDisableTiming));
     }
-    *h->vnorm_host = 0.0;
-    ONEBIT_CUDA(h, cudaEventCreateWithFlags(&h->ev_vnorm, cudaEventDisableTiming));
-  }
-  h->vmon = enable != 0;
-  return ONEBIT_OK;
+    h->vmon = enable != 0;
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_variance_norm(onebit_adam_t* h, double* norm, int64_t* step) {
-  if (!h || !norm || !step) return ONEBIT_ERR_INVALID_ARG;
-  if (h->vnorm_step == 0) return ONEBIT_ERR_PHASE;  // no monitored warm-up step yet
-  DeviceGuard g(h->device);
-  ONEBIT_CUDA(h, cudaEventSynchronize(h->ev_vnorm));
-  *norm = *h->vnorm_host;
-  *step = h->vnorm_step;
-  return ONEBIT_OK;
+  return guarded([&]() -> onebit_status_t {
+    if (!h || !norm || !step) return ONEBIT_ERR_INVALID_ARG;
+    if (h->vnorm_step == 0) return ONEBIT_ERR_PHASE;  // no monitored warm-up step yet
+    DeviceGuard g(h->device);
+    ONEBIT_CUDA(h, cudaEventSynchronize(h->ev_vnorm));
+    *norm = *h->vnorm_host;
+    *step = h->vnorm_step;
+    return ONEBIT_OK;
+  });
 }
 
 onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, int64_t value) {

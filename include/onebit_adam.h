@@ -105,7 +105,8 @@ typedef struct {
   int64_t warmup_steps;    /* T_w >= 1: warm-up steps before the variance is frozen */
   int32_t n_workers;       /* n, 1 <= n <= 256 */
   int32_t n_tensors;       /* T >= 1 (1 = one flat buffer) */
-  const int64_t* numel;    /* host array [T], L_k >= 0, sum L_k >= 1 */
+  const int64_t* numel;    /* host array [T], L_k >= 0, 1 <= sum L_k <= 2^40 (more is
+                            * ONEBIT_ERR_UNSUPPORTED: no device holds that much state) */
   int32_t grad_dtype;      /* onebit_dtype_t */
   int32_t bias_correction; /* 0: the pages' formulas (default); 1: Kingma-Ba bias correction */
   int64_t scale_block;     /* scale granularity.  0 (default): one worker scale per tensor and n

@@ -163,6 +163,20 @@ def test_worker_chunk_plan(numel, n, block):
             assert [r[:5] for r in by_seg[k]] == [r for r in server if r[0] == k]
 
 
+def test_oversized_plans_are_refused_before_they_are_built():
+    """A tiny scale block on a huge tensor (2^40 elements in blocks of 32), a list too long for
+    32-bit segment indices, or more than 2^40 elements in all is ONEBIT_ERR_UNSUPPORTED, returned at
+    once, without building the plan."""
+    import time
+
+    for numel, n, block in (([1 << 40], 16, 32), ([1 << 36], 256, 32), ([1 << 40, 1], 2, 0), ([1 << 41], 1, 0)):
+        t = time.perf_counter()
+        with pytest.raises(ob.OneBitError) as e:
+            ob.workspace_size(ob.make_config(numel, n, scale_block=block))
+        assert e.value.status == ob.ERR_UNSUPPORTED
+        assert time.perf_counter() - t < 1.0
+
+
 def test_small_lists_get_short_chunks():
     """Chunk length adapts to the list: 2^20 elements become 256 chunks of 4096 (work units for
     every SM), while a BERT-Large-sized list keeps 65536-element chunks."""
