@@ -184,6 +184,21 @@ def pin_volume_reduction(ora):
     assert abs(frac16 - gd["fraction_of_fp16_pct"]) <= 0.5
 
 
+def pin_volume_reduction_including_warmup(ora):
+    """The pages' 'up to 5x less communication, including the warm-up' from the message sizes: with
+    the warm-up at f of the steps (uncompressed fp16 messages) and compressed messages after it, the
+    run's volume falls by 1 / (f + (1 - f) * ratio).  Over the pages' 10-25% warm-up this spans the
+    printed figure, and at 15% it is 5x (golden/volume_reduction.json)."""
+    g = _golden("volume_reduction.json")
+    d = 340_000_000
+    ratio = (4 * ora.words(d) + 4) / (2.0 * d)
+    total = lambda f: 1.0 / (f + (1.0 - f) * ratio)  # noqa: E731
+    lo_f, hi_f = g["warmup_fraction_range"]
+    printed = g["printed"]["total_reduction_including_warmup_x"]
+    assert total(hi_f) < printed < total(lo_f)
+    assert abs(total(0.15) - printed) <= 0.5
+
+
 # ------------------------------------------------------------------------------ warm-up Adam
 
 def pin_warmup_golden(ora):
