@@ -342,6 +342,13 @@ class OneBitAdam:
             lib().onebit_adam_free(self.h)
             self.h = None
 
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.free()
+        return False
+
     def __del__(self):
         try:
             self.free()
