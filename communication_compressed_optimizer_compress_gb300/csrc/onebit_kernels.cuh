@@ -750,17 +750,31 @@ __global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs
   }
   __syncthreads();
 
-  auto advance = [&](TileCursor& c) {
-    if (++c.t >= tiles_of(A.chunks[c.u])) {
+  // a cursor over this block's (chunk, tile) sequence that keeps the current chunk's descriptor in
+  // registers, so that it is read from memory once per chunk rather than at every tile
+  struct Cur {
+    int u, t, nt;
+    Chunk ch;
+  };
+  auto load = [&](Cur& c) {
+    if (c.u < A.n_chunks) {
+      c.ch = A.chunks[c.u];
+      c.nt = tiles_of(c.ch);
+    }
+  };
+  auto advance = [&](Cur& c) {
+    if (++c.t >= c.nt) {
       c.t = 0;
       c.u += gridDim.x;
+      load(c);
     }
   };
 
   if (threadIdx.x >= kThreads) {
     // ---------------- producer warp (one elected lane issues the copies)
     if (threadIdx.x != kThreads) return;
-    TileCursor c{(int)blockIdx.x, 0};
+    Cur c{(int)blockIdx.x, 0, 0, {}};
+    load(c);
     int j = 0;
     for (; c.u < A.n_chunks; ++j, advance(c)) {
       const int st = j % kStages;
@@ -769,7 +783,7 @@ __global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs
         abort_flag = 1;
       }
       if (abort_flag) break;
-      const Chunk ch = A.chunks[c.u];
+      const Chunk& ch = c.ch;
       const int e0 = c.t * kTile;
       const int tlen = min(kTile, ch.len - e0);
       unsigned char* sbase = dyn + (size_t)st * stage_bytes;
@@ -797,12 +811,13 @@ __global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs
 
   // ---------------- consumer warps
   const int lane = threadIdx.x & 31;
-  TileCursor cons{(int)blockIdx.x, 0};
+  Cur cons{(int)blockIdx.x, 0, 0, {}};
+  load(cons);
   int k = 0;
   int cur_seg = -1;
   unsigned long long hi = 0, lo = 0;
   while (cons.u < A.n_chunks) {
-    const Chunk ch = A.chunks[cons.u];
+    const Chunk ch = cons.ch;
     if (cons.t == 0 && ch.seg != cur_seg) {
       build_server_tables_consumers(S, A, ch.seg);
       cur_seg = ch.seg;
@@ -856,7 +871,7 @@ __global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs
       if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with stage st
     }
     ++k;
-    const bool last_tile = cons.t == tiles_of(ch) - 1;
+    const bool last_tile = cons.t == cons.nt - 1;
     const int u_done = cons.u;
     advance(cons);
     if (last_tile) {  // chunk total among the consumers (fixed order)
