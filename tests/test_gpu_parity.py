@@ -393,6 +393,51 @@ def test_degenerate_inputs(dtype):
     p.close()
 
 
+def test_two_handles_on_two_streams():
+    """Two optimizers stepped in interleaved order on two non-default CUDA streams (their kernels
+    free to overlap) end bit-identical to the same schedules run alone on the default stream: a
+    handle owns all its state, and every call runs on the stream it is given."""
+    ws = [_tiny(numel=(70_001, 33), n_workers=4, grad_dtype=W.F16, warmup_steps=2, seed=181),
+          _tiny(numel=(50_000,), n_workers=16, grad_dtype=W.BF16, warmup_steps=2, seed=182)]
+    grads = [[[t.cuda() for t in W.GradSource(w, "cpu").grads(s)] for s in range(5)] for w in ws]
+
+    def make(w):
+        params = [p.cuda() for p in W.params(w, "cpu")]
+        return params, ob.OneBitAdam(params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr,
+                                     grad_dtype=W.TORCH_DTYPE[w.grad_dtype])
+
+    def schedule(opt, g, s, stream):
+        if s < 2:
+            opt.warmup_step(g[s], stream=stream)
+        else:
+            if s == 2:
+                opt.freeze_variance(stream=stream)
+            opt.compress_step(g[s], stream=stream)
+
+    alone = []
+    for w, g in zip(ws, grads):
+        params, opt = make(w)
+        for s in range(5):
+            schedule(opt, g, s, None)
+        torch.cuda.synchronize()
+        alone.append((torch.cat([p.cpu() for p in params]).numpy(), _state(opt, w.n_workers)))
+        opt.free()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    made = [make(w) for w in ws]
+    for s in range(5):
+        for k in (0, 1):
+            schedule(made[k][1], grads[k], s, streams[k])
+    torch.cuda.synchronize()
+    for k, w in enumerate(ws):
+        params, opt = made[k]
+        x = torch.cat([p.cpu() for p in params]).numpy()
+        assert np.array_equal(x.view(np.uint32), alone[k][0].view(np.uint32)), k
+        st = _state(opt, w.n_workers)
+        for key in st:
+            assert np.array_equal(st[key].view(np.uint8), alone[k][1][key].view(np.uint8)), (k, key)
+        opt.free()
+
+
 def test_timing_and_launch_counts():
     w = _tiny(numel=(50_000,), n_workers=4, warmup_steps=1)
     p = Pair(w)
