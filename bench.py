@@ -60,8 +60,8 @@ def measured_peak():
 
 def _kernel_source_hash(marker: str):
     """Hash of one kernel's source: the constants declared before it (the shared tuning constants
-    and those of the kernels it builds on) plus the kernel's own region (from its heading comment to
-    the next separator)."""
+    and those of the kernels it builds on) plus the code of the kernel's own region (from its heading
+    comment to the next separator), full-line comments left out."""
     import hashlib
 
     path = os.path.join(ROOT, "communication_compressed_optimizer_compress_gb300", "csrc", "onebit_kernels.cuh")
@@ -69,7 +69,8 @@ def _kernel_source_hash(marker: str):
     i = src.index(marker)
     consts = "\n".join(ln for ln in src[:i].splitlines() if ln.startswith("constexpr "))
     j = src.index("\n// " + "-" * 40, i)  # the next full-width section separator
-    return hashlib.sha256((consts + src[i:j]).encode()).hexdigest()[:16]
+    code = "\n".join(ln for ln in src[i:j].splitlines() if not ln.lstrip().startswith("//"))  # comments aside
+    return hashlib.sha256((consts + code).encode()).hexdigest()[:16]
 
 
 def traffic_from_profiles(name: str, marker: str, elems: int):

@@ -249,8 +249,8 @@ __device__ __forceinline__ float error_of(float c, float s) {  // c - s*sign(c),
 
 // ------------------------------------------------------------------------------------------------
 // K1: worker momentum + error feedback + 1-bit compression + norm partials.
-// One unit = (chunk, worker).  c_i = (b1*m + (1-b1)*g_i) + delta_i, delta_i rebuilt from the
-// previous c_i and s_i; writes c_i, its sign byte and the chunk's sum of c_i^2.
+// One unit = (worker-side chunk, worker).  c_i = (b1*m + (1-b1)*g_i) + delta_i, delta_i rebuilt
+// from the previous c_i and s_i; writes c_i, its sign byte and the chunk's sum of c_i^2.
 
 // Where the worker kernel's momentum comes from.
 enum MomentumSource : int {
