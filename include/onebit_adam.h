@@ -26,8 +26,9 @@
  * with no fused multiply-add; norms are accumulated in double and rounded once to fp32.
  *
  * Conventions used by every entry point:
- *   - Errors: every call returns a status and never aborts.  Argument and phase checks happen on
- *     the host before anything is enqueued; a failed check changes no state.  CUDA launch or copy
+ *   - Errors: every call returns a status and never aborts, and no C++ exception leaves it (a host
+ *     allocation that fails is ONEBIT_ERR_NOMEM).  Argument and phase checks happen on the host
+ *     before anything is enqueued; a failed check changes no state.  CUDA launch or copy
  *     failures return ONEBIT_ERR_CUDA (onebit_adam_last_error() gives the CUDA message).  A
  *     non-finite scale found on the device sets a sticky flag read by onebit_adam_get_status().
  *   - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Calls enqueue work and
