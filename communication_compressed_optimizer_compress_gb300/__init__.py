@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
             "onebit_adam_plan_worker_chunks": [cfgp, ctypes.POINTER(i64), i64, ctypes.POINTER(i64)],
             "onebit_adam_set_fault_injection": [vp, i32, i64],
             "onebit_adam_set_max_ctas": [vp, i32],
+            "onebit_adam_set_lr": [vp, ctypes.c_float],
             "onebit_adam_set_variance_monitor": [vp, i32],
             "onebit_adam_variance_norm": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)],
         }
@@ -293,6 +294,10 @@ class OneBitAdam:
         cnt = (ctypes.c_int64 * NUM_KERNELS)()
         _check(lib().onebit_adam_kernel_times(self.h, ms, cnt), "onebit_adam_kernel_times", self.h)
         return {KERNEL_NAMES[k]: (ms[k], cnt[k]) for k in range(NUM_KERNELS)}
+
+    def set_lr(self, lr: float):
+        """Learning rate for the following steps (for schedules; the method itself keeps it fixed)."""
+        _check(lib().onebit_adam_set_lr(self.h, float(lr)), "onebit_adam_set_lr", self.h)
 
     def set_max_ctas(self, max_ctas: int):
         """Cap the CTAs of every streaming launch (0: fill the GPU); results do not depend on it."""

@@ -1281,6 +1281,12 @@ onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, 
   }
 }
 
+onebit_status_t onebit_adam_set_lr(onebit_adam_t* h, float lr) {
+  if (!h || !std::isfinite(lr)) return ONEBIT_ERR_INVALID_ARG;
+  h->cfg.lr = lr;
+  return ONEBIT_OK;
+}
+
 onebit_status_t onebit_adam_set_max_ctas(onebit_adam_t* h, int32_t max_ctas) {
   if (!h || max_ctas < 0) return ONEBIT_ERR_INVALID_ARG;
   h->max_ctas = max_ctas;

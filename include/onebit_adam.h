@@ -213,6 +213,12 @@ onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launch
 onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enable);
 onebit_status_t onebit_adam_variance_norm(onebit_adam_t* h, double* norm, int64_t* step);
 
+/* Set the learning rate gamma used by the following steps (warm-up, compression and baseline).  The
+ * pages keep gamma constant; this serves the schedules training uses (warm-up ramps, decay).  The
+ * new value must be finite, else ONEBIT_ERR_INVALID_ARG.  A step captured in a CUDA graph keeps the
+ * gamma it was captured with. */
+onebit_status_t onebit_adam_set_lr(onebit_adam_t* h, float lr);
+
 /* Caps the CTAs that every streaming kernel launch of this handle uses (0, the default: as many as
  * fill the GPU).  No counterpart on the method's pages: it lets a caller leave SMs to work running
  * concurrently on other streams.  Results do not depend on it, bit for bit: every partial sum is

@@ -262,6 +262,10 @@ class OneBitAdamOracle:
         self.t = 0
         self.phase = "warmup"
 
+    def set_lr(self, lr):
+        """Learning rate of the following steps (the method keeps it fixed; schedules change it)."""
+        self.cfg.lr = float(lr)
+
     def _grad_ptrs(self, grads):
         if self.scale_block:  # cut each caller tensor's gradient into its blocks
             Tu, B = len(self.unumel), self.scale_block

@@ -438,6 +438,27 @@ def test_two_handles_on_two_streams():
         opt.free()
 
 
+def test_learning_rate_schedule():
+    """gamma changed before every step (a warm-up ramp, then decay) on both sides: parity holds
+    step by step, and the warm-up stays bit-exact."""
+    w = _tiny(numel=(70_001, 33), n_workers=4, grad_dtype=W.F16, warmup_steps=3, seed=191)
+    p = Pair(w)
+    lrs = [np.float32(v) for v in (1e-4, 5e-4, 1e-3, 8e-4, 4e-4, 2e-4, 1e-4)]
+    for s in range(3):
+        p.gpu.set_lr(lrs[s])
+        p.ora.set_lr(lrs[s])
+        p.warmup(check=False)
+        p.check_warmup(exact=True)
+    p.freeze()
+    for s in range(3, 7):
+        p.gpu.set_lr(lrs[s])
+        p.ora.set_lr(lrs[s])
+        p.compress()
+    with pytest.raises(ob.OneBitError):
+        p.gpu.set_lr(float("nan"))
+    p.close()
+
+
 def test_timing_and_launch_counts():
     w = _tiny(numel=(50_000,), n_workers=4, warmup_steps=1)
     p = Pair(w)
