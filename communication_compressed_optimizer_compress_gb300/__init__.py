@@ -280,6 +280,25 @@ class OneBitAdam:
         _check(lib().onebit_adam_import(self.h, int(what), int(worker), tensor.contiguous().data_ptr(),
                                         _stream_ptr(stream)), "onebit_adam_import", self.h)
 
+    def state_dict(self, stream=None):
+        """Everything a resume needs besides the parameters (which the caller owns): the step count
+        and phase, m, v (den after the freeze) and every error memory, in fp32 CUDA tensors."""
+        t, phase = self.get_step()
+        return {"t": t, "phase": phase,
+                "m": self.export_state(STATE_M, stream=stream),
+                "v": self.export_state(STATE_V, stream=stream),
+                "server_error": self.export_state(STATE_SERVER_ERROR, stream=stream),
+                "worker_error": [self.export_state(STATE_WORKER_ERROR, i, stream=stream) for i in range(self.n)]}
+
+    def load_state_dict(self, d, stream=None):
+        """Restore a state_dict() into this handle (same configuration): set_step, then the imports."""
+        self.set_step(d["t"], d["phase"], stream=stream)
+        self.import_state(STATE_M, d["m"], stream=stream)
+        self.import_state(STATE_V, d["v"], stream=stream)
+        self.import_state(STATE_SERVER_ERROR, d["server_error"], stream=stream)
+        for i, e in enumerate(d["worker_error"]):
+            self.import_state(STATE_WORKER_ERROR, e, i, stream=stream)
+
     def comm_bytes(self):
         c, f = ctypes.c_uint64(), ctypes.c_uint64()
         _check(lib().onebit_adam_comm_bytes(self.h, ctypes.byref(c), ctypes.byref(f)), "onebit_adam_comm_bytes")

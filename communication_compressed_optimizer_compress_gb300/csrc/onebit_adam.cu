@@ -1158,7 +1158,6 @@ onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worke
         return run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.v), st);
       case ONEBIT_STATE_WORKER_ERROR: {
         if (worker < 0 || worker >= P.n) return ONEBIT_ERR_INVALID_ARG;
-        if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
         float* ws_prev = last_wscale(h);  // what the next step reads as the previous scales
         if (h->werr_zero) {
           ONEBIT_CUDA(h, cudaMemsetAsync(h->at<float>(h->lay.c), 0, (size_t)P.n * P.Dp * 4, st));
@@ -1172,7 +1171,6 @@ onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worke
         return ONEBIT_OK;
       }
       case ONEBIT_STATE_SERVER_ERROR: {
-        if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
         if (!h->m_dense) {  // m is carried by the server scales about to be zeroed: materialise it
           if ((s = export_m(h, h->at<float>(h->lay.m), st))) return s;
           h->m_dense = true;

@@ -188,8 +188,9 @@ onebit_status_t onebit_adam_state_size(const onebit_adam_t* h, int32_t what, siz
 onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worker, void* dst, onebit_stream_t stream);
 
 /* Load state `what` (M, V, WORKER_ERROR, SERVER_ERROR) from device memory `src` on `stream`.
- * Importing an error in phase COMPRESS makes the next step use it exactly; importing M makes the
- * next compression step read this fp32 momentum. */
+ * An imported error is used exactly by the next step that reads errors: a compression step, or in
+ * phase WARMUP a gradient-compression baseline step (a freeze still resets the errors to zero).
+ * Importing M makes the next compression step read this fp32 momentum. */
 onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worker, const void* src, onebit_stream_t stream);
 
 /* Bytes one worker sends per compression step (sign words + one fp32 scale per tensor) and the

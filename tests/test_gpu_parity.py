@@ -459,6 +459,56 @@ def test_learning_rate_schedule():
     p.close()
 
 
+@pytest.mark.parametrize("phase", ["compress", "ec_adam"])
+def test_state_dict_round_trip(phase):
+    """state_dict() taken mid-run and loaded into a fresh handle resumes bit-identically: in the
+    compression stage, and in the warm-up phase between gradient-compression baseline steps, whose
+    error memories are part of the state."""
+    w = _tiny(numel=(70_001, 33), n_workers=3, grad_dtype=W.BF16, warmup_steps=10, seed=201)
+    src = W.GradSource(w, "cpu")
+    g = [[t.cuda() for t in src.grads(s)] for s in range(8)]
+
+    def step(opt, s):
+        if phase == "ec_adam":
+            opt.ec_adam_step(g[s])
+        elif s < 2:
+            opt.warmup_step(g[s])
+        else:
+            if s == 2:
+                opt.freeze_variance()
+            opt.compress_step(g[s])
+
+    def make(params):
+        return ob.OneBitAdam(params, w.n_workers, w.warmup_steps, w.beta1, w.beta2, w.eps, w.lr,
+                             grad_dtype=W.TORCH_DTYPE[w.grad_dtype])
+
+    params = [p.cuda() for p in W.params(w, "cpu")]
+    ref = make(params)
+    for s in range(4):
+        step(ref, s)
+    ckpt = ref.state_dict()
+    ckpt_x = [p.clone() for p in params]
+    for s in range(4, 8):
+        step(ref, s)
+    torch.cuda.synchronize()
+    want = _state(ref, w.n_workers)
+    want_x = torch.cat([p.cpu() for p in params]).numpy()
+
+    params2 = [x.clone() for x in ckpt_x]
+    opt = make(params2)
+    opt.load_state_dict(ckpt)
+    for s in range(4, 8):
+        step(opt, s)
+    torch.cuda.synchronize()
+    got = _state(opt, w.n_workers)
+    got_x = torch.cat([p.cpu() for p in params2]).numpy()
+    assert np.array_equal(got_x.view(np.uint32), want_x.view(np.uint32))
+    for k in want:
+        assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
+    opt.free()
+    ref.free()
+
+
 def test_timing_and_launch_counts():
     w = _tiny(numel=(50_000,), n_workers=4, warmup_steps=1)
     p = Pair(w)
