@@ -466,12 +466,25 @@ def main():
         opt.compress_step_host(host)  # first call allocates the library's staging buffer
         torch.cuda.synchronize()
 
+        probe_streams = [torch.cuda.Stream(device=dev) for _ in range(4)]
+
         def link_probe():
             """The host link at this moment: plain copies of this step's own host gradients into
-            device buffers of the same shapes (one stream, nothing else running), in GB/s."""
+            device buffers of the same shapes, cut the way the library cuts its staging copies
+            (64 MB pieces, round-robin over 4 streams) with nothing else running, in GB/s."""
             t0.record(stream)
+            for cs in probe_streams:
+                cs.wait_stream(stream)
+            r = 0
             for hb, db in zip(host, gsets[1]):
-                db.copy_(hb, non_blocking=True)
+                src, dst = hb.view(-1), db.view(-1)
+                piece = (64 << 20) // hb.element_size()
+                for a in range(0, src.numel(), piece):
+                    with torch.cuda.stream(probe_streams[r % 4]):
+                        dst[a:a + piece].copy_(src[a:a + piece], non_blocking=True)
+                    r += 1
+            for cs in probe_streams:
+                stream.wait_stream(cs)
             t1.record(stream)
             torch.cuda.synchronize()
             return h2d / (t0.elapsed_time(t1) / 1e3) / 1e9
