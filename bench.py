@@ -178,7 +178,7 @@ def barrier():
 def oracle_sample(w, seconds: float = 12.0, d_sample: int = 1 << 21):
     """Time the oracle (single-threaded C) on a bounded sample of the workload: the same worker
     count, gradient dtype and law on a flat buffer of d_sample parameters; one warm-up step, the
-    freeze, then compression steps until `seconds` of CPU time are spent.  Returns params/s."""
+    freeze, then compression steps until `seconds` of wall time are spent.  Returns params/s."""
     import numpy as np
 
     import oracle
