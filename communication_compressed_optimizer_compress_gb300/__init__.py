@@ -275,10 +275,12 @@ class OneBitAdam:
     def import_state(self, what, tensor, worker=0, stream=None):
         import torch
 
-        if tensor.dtype != torch.float32 or not tensor.is_cuda or tensor.numel() * 4 != self.state_size(what):
-            raise ValueError("import expects a contiguous fp32 CUDA tensor of state_size bytes")
-        _check(lib().onebit_adam_import(self.h, int(what), int(worker), tensor.contiguous().data_ptr(),
-                                        _stream_ptr(stream)), "onebit_adam_import", self.h)
+        # the copy is asynchronous on `stream`, so a temporary made here could be freed before it ran
+        if (tensor.dtype != torch.float32 or not tensor.is_contiguous() or tensor.device != self.params[0].device
+                or tensor.numel() * 4 != self.state_size(what)):
+            raise ValueError("import expects a contiguous fp32 tensor of state_size bytes on the parameters' device")
+        _check(lib().onebit_adam_import(self.h, int(what), int(worker), tensor.data_ptr(), _stream_ptr(stream)),
+               "onebit_adam_import", self.h)
 
     def state_dict(self, stream=None):
         """Everything a resume needs besides the parameters (which the caller owns): the step count

@@ -184,13 +184,15 @@ onebit_status_t onebit_adam_set_step(onebit_adam_t* h, int64_t t, int32_t phase,
 onebit_status_t onebit_adam_state_size(const onebit_adam_t* h, int32_t what, size_t* bytes);
 
 /* Copy state `what` (worker index for per-worker items, else ignored) into device memory `dst`
- * (onebit_adam_state_size() bytes) on `stream`.  Errors and the momentum are materialised in fp32. */
+ * (onebit_adam_state_size() bytes) on `stream`.  Errors and the momentum are materialised in fp32.
+ * `dst` holds the result once `stream` has passed the copy. */
 onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worker, void* dst, onebit_stream_t stream);
 
 /* Load state `what` (M, V, WORKER_ERROR, SERVER_ERROR) from device memory `src` on `stream`.
  * An imported error is used exactly by the next step that reads errors: a compression step, or in
  * phase WARMUP a gradient-compression baseline step (a freeze still resets the errors to zero).
- * Importing M makes the next compression step read this fp32 momentum. */
+ * Importing M makes the next compression step read this fp32 momentum.  The copy is enqueued on
+ * `stream`: `src` must stay valid and unchanged until `stream` has passed it. */
 onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worker, const void* src, onebit_stream_t stream);
 
 /* Bytes one worker sends per compression step (sign words + one fp32 scale per tensor) and the

@@ -496,6 +496,11 @@ def test_state_dict_round_trip(phase):
 
     params2 = [x.clone() for x in ckpt_x]
     opt = make(params2)
+    # the import copies asynchronously, so tensors it would have to copy first are refused
+    strided = torch.zeros(2 * ckpt["m"].numel(), device="cuda")[::2]
+    for bad in (strided, ckpt["m"].cpu()):
+        with pytest.raises(ValueError):
+            opt.import_state(ob.STATE_M, bad)
     opt.load_state_dict(ckpt)
     for s in range(4, 8):
         step(opt, s)
