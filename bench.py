@@ -19,6 +19,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -73,18 +74,31 @@ def _kernel_source_hash(marker: str):
     return hashlib.sha256((consts + code).encode()).hexdigest()[:16]
 
 
-def traffic_from_profiles(name: str, marker: str, elems: int):
+def traffic_from_profiles(name: str, n_workers: int, grad_bytes: int, elems: int):
     """DRAM bytes per launch of a kernel from its committed ncu summary (bytes per element there x
-    the elements of this launch), or None when the kernel's source changed since the capture."""
+    the elements of this launch).  None when no record was taken at this worker count and gradient
+    width, or when the kernel's source changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)[name]
-        if rec["source_sha256_16"] != _kernel_source_hash(marker):
+        if rec["n_workers"] != n_workers or rec["grad_bytes"] != grad_bytes:
+            return None
+        if rec["source_sha256_16"] != _kernel_source_hash(rec["marker"]):
             return None
         return rec["dram_bytes_per_elem"] * elems
     except Exception:
         return None
+
+
+def warmup_kernel(n: int, grad_bytes: int) -> str:
+    """The warm-up kernel the library launches for aligned buffers: the staged variant for 16-bit
+    gradients with kWarmStagedMin <= n <= kWarmStagedMax (constants read from the kernel source)."""
+    path = os.path.join(ROOT, "communication_compressed_optimizer_compress_gb300", "csrc", "onebit_kernels.cuh")
+    src = open(path).read()
+    lo = int(re.search(r"constexpr int kWarmStagedMin = (\d+);", src).group(1))
+    hi = int(re.search(r"constexpr int kWarmStagedMax = (\d+);", src).group(1))
+    return "k_warmup_staged" if grad_bytes == 2 and lo <= n <= hi else "k_warmup"
 
 
 class ClockSampler:
@@ -438,6 +452,8 @@ def main():
     step_gbs = w.d * ab["step"] / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = measured_peak()
     dom = "warmup" if args.step == "warmup" else "worker"
+    warm_kernel = warmup_kernel(w.n_workers, W.GRAD_BYTES[w.grad_dtype])
+    traffic_rec = {"compress": "k_worker", "ec_adam": "k_worker[ec_adam]", "warmup": warm_kernel}[args.step]
     dom_ms = kt[dom][0] / max(1, kt[dom][1])
     dom_gbs = w.d * ab[dom] / (dom_ms / 1e3) / 1e9 if dom_ms > 0 else None
     per_kernel = {}
@@ -526,11 +542,10 @@ def main():
             "roofline": None if dom_gbs is None else {"bound": "hbm",
                          "kernel": {"compress": "k_worker (momentum + error + sign pack + norm partials)",
                                     "ec_adam": "k_worker (gradient + error + sign pack + norm partials)",
-                                    "warmup": "k_warmup (worker mean + Adam)"}[args.step],
+                                    "warmup": f"{warm_kernel} (worker mean + Adam)"}[args.step],
                          "achieved": dom_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": dom_gbs / peak,
-                         "traffic": traffic_from_profiles("k_worker", "// K1: worker momentum", w.d)
-                         if args.step == "compress" else None,
+                         "traffic": traffic_from_profiles(traffic_rec, w.n_workers, W.GRAD_BYTES[w.grad_dtype], w.d),
                          "bytes_per_elem": ab[dom], "elems_per_launch": w.d},
             "kernels": per_kernel,
             "warmup_adam_ms_per_step": warm_ms,
