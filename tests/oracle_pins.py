@@ -684,4 +684,98 @@ def pin_ec_adam_error_feedback_telescopes(ora):
     assert np.max(np.abs(sum_srv + o.view("eps_srv") - sum_avg)) <= 1e-6 * np.abs(sum_avg).max() * steps
 
 
+def _brute_rms(vals):
+    """||v||_2 / sqrt(len) from the correctly rounded sum of the exact squares (math.fsum), taken in
+    double and rounded once to fp32; 0 for an empty range."""
+    if not vals:
+        return np.float32(0.0)
+    return np.float32(math.sqrt(math.fsum(float(v) * float(v) for v in vals) / len(vals)))
+
+
+def pin_brute_force_compression_steps_small_d(ora):
+    """Several compression steps on d <= 64, restated here element by element in scalar fp32 from
+    the method's steps (worker momentum, error compensation, sign + rms scale per tensor, ordered
+    server average, server error, per-shard recompression, broadcast, preconditioned update), with
+    shards of 32*ceil(L/(32n)) and norms from exactly rounded sums.  Every state word must equal the
+    oracle's after every step: ragged lists with empty tensors, n in {1, 2, 3, 5}, zero gradients
+    (sign(0) = +1) and fp16 gradients."""
+    cases = [([64], 1, F32), ([33, 0, 31], 2, F32), ([5, 32, 27], 3, F16), ([1, 17, 40], 5, F32), ([64], 3, F32)]
+    for case, (numel, n, dtype) in enumerate(cases):
+        rng = np.random.default_rng(300 + case)
+        D, T = sum(numel), len(numel)
+        offs = np.concatenate([[0], np.cumsum(numel)]).astype(int)
+        b1, lr = np.float32(0.9), np.float32(1e-2)
+        omb1 = np.float32(np.float32(1.0) - b1)
+        x = [np.float32(v) for v in rng.standard_normal(D) * 0.02]
+        den = [np.float32(v) for v in rng.uniform(1e-3, 1e-1, D)]
+        m = [np.float32(v) for v in rng.standard_normal(D) * 1e-3]
+        m[: D // 4] = [np.float32(0.0)] * (D // 4)
+        delta = [[np.float32(0.0)] * D for _ in range(n)]
+        eps = [np.float32(0.0)] * D
+        o = _compress_ready(ora, numel, n, np.array(x, np.float32), np.array(den, np.float32),
+                            np.array(m, np.float32), beta1=float(b1), lr=float(lr), grad_dtype=dtype)
+        for step in range(4):
+            flats = []
+            for i in range(n):
+                f = (rng.standard_normal(D) * 10 ** rng.uniform(-4, -2)).astype(np.float32)
+                if step == 0:
+                    f[: D // 4] = 0.0  # with m = 0 there: c = 0, a bit of 1 and a lossless zero
+                flats.append(f.astype(np.float16) if dtype == F16 else f)
+            o.compress_step([f[offs[k]: offs[k + 1]] for f in flats for k in range(T)])
+
+            # worker i: m_i = b1*m + (1-b1)*g_i, c_i = m_i + delta_i, then sign + scale per tensor
+            wscale = np.zeros((n, T), np.float32)
+            msg = [[None] * D for _ in range(n)]
+            wbits = [[0] * D for _ in range(n)]
+            for i in range(n):
+                c = [np.float32(b1 * m[p] + omb1 * np.float32(flats[i][p])) for p in range(D)]
+                c = [np.float32(c[p] + delta[i][p]) for p in range(D)]
+                for k in range(T):
+                    s = _brute_rms(c[offs[k]: offs[k + 1]])
+                    wscale[i, k] = s
+                    for p in range(offs[k], offs[k + 1]):
+                        bit = c[p] >= 0
+                        wbits[i][p] = int(bit)
+                        msg[i][p] = s if bit else -s
+                        delta[i][p] = np.float32(c[p] - s) if bit else np.float32(c[p] + s)
+            # server: ordered sum of the messages, / n, + server error; recompress per shard
+            a = []
+            for p in range(D):
+                acc = np.float32(0.0)
+                for i in range(n):
+                    acc = np.float32(acc + msg[i][p])
+                a.append(np.float32(np.float32(acc / np.float32(n)) + eps[p]))
+            sscale = np.zeros((T, n), np.float32)
+            sbits = [0] * D
+            for k, L in enumerate(numel):
+                S_k = 32 * -(-L // (32 * n))
+                for j in range(n):
+                    lo, hi = offs[k] + min(j * S_k, L), offs[k] + min((j + 1) * S_k, L)
+                    S = _brute_rms(a[lo:hi])
+                    sscale[k, j] = S
+                    for p in range(lo, hi):
+                        bit = a[p] >= 0
+                        sbits[p] = int(bit)
+                        eps[p] = np.float32(a[p] - S) if bit else np.float32(a[p] + S)
+                        m[p] = S if bit else -S
+            x = [np.float32(x[p] - np.float32(lr * np.float32(m[p] / den[p]))) for p in range(D)]
+
+            def words(bits):
+                out = []
+                for k, L in enumerate(numel):
+                    for w0 in range(0, L, 32):
+                        out.append(sum(bits[offs[k] + e] << (e - w0) for e in range(w0, min(w0 + 32, L))))
+                return np.array(out, np.uint32)
+
+            where = f"case {case} step {step}"
+            assert np.array_equal(o.wscale, wscale), where
+            assert np.array_equal(o.sscale, sscale), where
+            for i in range(n):
+                assert np.array_equal(o.view("wbits")[i], words(wbits[i])), where
+                assert np.array_equal(o.view("delta")[i].view(np.uint32), np.array(delta[i], np.float32).view(np.uint32)), where
+            assert np.array_equal(o.view("sbits"), words(sbits)), where
+            for name, want in (("eps_srv", eps), ("m", m), ("x", x)):
+                assert np.array_equal(o.view(name).view(np.uint32), np.array(want, np.float32).view(np.uint32)), (where, name)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
