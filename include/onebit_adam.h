@@ -29,8 +29,11 @@
  *   - Errors: every call returns a status and never aborts, and no C++ exception leaves it (a host
  *     allocation that fails is ONEBIT_ERR_NOMEM).  Argument and phase checks happen on the host
  *     before anything is enqueued; a failed check changes no state.  CUDA launch or copy
- *     failures return ONEBIT_ERR_CUDA (onebit_adam_last_error() gives the CUDA message).  A
- *     non-finite scale found on the device sets a sticky flag read by onebit_adam_get_status().
+ *     failures return ONEBIT_ERR_CUDA (onebit_adam_last_error() gives the CUDA message).  When a
+ *     step call fails that way after some of its kernels were enqueued, the step count does not
+ *     advance and the parameters and optimizer state are unspecified: resume from a checkpoint
+ *     (onebit_adam_set_step + onebit_adam_import).  A non-finite scale found on the device sets a
+ *     sticky flag read by onebit_adam_get_status().
  *   - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Calls enqueue work and
  *     return without synchronising, except where stated.  All calls on one handle must be ordered
  *     on one stream (or synchronised by the caller): the handle's state is updated in stream order.
