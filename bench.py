@@ -74,21 +74,29 @@ def _kernel_source_hash(marker: str):
     return hashlib.sha256((consts + code).encode()).hexdigest()[:16]
 
 
-def traffic_from_profiles(name: str, n_workers: int, grad_bytes: int, elems: int):
-    """DRAM bytes per launch of a kernel from its committed ncu summary (bytes per element there x
-    the elements of this launch).  None when no record was taken at this worker count and gradient
-    width, or when the kernel's source changed since the capture."""
+def traffic_from_profiles(kernel: str, step: str, w, scale_block: int = 0):
+    """DRAM bytes per launch of `kernel` in a `step` of workload `w`, from the committed ncu records
+    (bytes per element there x the elements of this launch).  None when no record was taken on this
+    shape (worker count, gradient width, number of tensors, scale block), when the kernel's source
+    changed since the capture, or when the record does not scale to a full launch: at the capture's
+    size the L2 absorbed more than 2% of the kernel's bytes (the previous kernel's output, or this
+    kernel's last writes), and a share that large does not grow with the element count."""
+    from communication_compressed_optimizer_compress_gb300 import workloads as W
+
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)[name]
-        if rec["n_workers"] != n_workers or rec["grad_bytes"] != grad_bytes:
-            return None
-        if rec["source_sha256_16"] != _kernel_source_hash(rec["marker"]):
-            return None
-        return rec["dram_bytes_per_elem"] * elems
+            recs = json.load(f)
     except Exception:
         return None
+    for rec in recs.values():
+        if (rec["kernel"], rec["step"], rec["n_workers"], rec["grad_bytes"], rec["n_tensors"], rec["scale_block"]) != \
+                (kernel, step, w.n_workers, W.GRAD_BYTES[w.grad_dtype], w.n_tensors, scale_block):
+            continue
+        if not rec["scales_to_launch"] or rec["source_sha256_16"] != _kernel_source_hash(rec["marker"]):
+            return None
+        return rec["dram_bytes_per_elem"] * w.d
+    return None
 
 
 def warmup_kernel(n: int, grad_bytes: int) -> str:
@@ -453,7 +461,9 @@ def main():
     peak, peak_kind = measured_peak()
     dom = "warmup" if args.step == "warmup" else "worker"
     warm_kernel = warmup_kernel(w.n_workers, W.GRAD_BYTES[w.grad_dtype])
-    traffic_rec = {"compress": "k_worker", "ec_adam": "k_worker[ec_adam]", "warmup": warm_kernel}[args.step]
+    # the kernel behind each timing bucket (the server's staged variant on the shapes it has records for)
+    bucket_kernel = {"warmup": warm_kernel, "worker": "k_worker", "server": "k_server_staged", "update": "k_update",
+                     "ec_update": "k_ec_adam_update"}
     dom_ms = kt[dom][0] / max(1, kt[dom][1])
     dom_gbs = w.d * ab[dom] / (dom_ms / 1e3) / 1e9 if dom_ms > 0 else None
     per_kernel = {}
@@ -466,6 +476,8 @@ def main():
         if name in ab:
             entry["gbs"] = w.d * ab[name] / (avg / 1e3) / 1e9
             entry["bytes_per_elem"] = ab[name]
+        if name in bucket_kernel:
+            entry["traffic"] = traffic_from_profiles(bucket_kernel[name], args.step, w, args.scale_block)
         per_kernel[name] = entry
 
     # ---- end to end through the C ABI with host gradient buffers (H2D copies inside the timing)
@@ -545,7 +557,7 @@ def main():
                                     "warmup": f"{warm_kernel} (worker mean + Adam)"}[args.step],
                          "achieved": dom_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": dom_gbs / peak,
-                         "traffic": traffic_from_profiles(traffic_rec, w.n_workers, W.GRAD_BYTES[w.grad_dtype], w.d),
+                         "traffic": traffic_from_profiles(bucket_kernel[dom], args.step, w, args.scale_block),
                          "bytes_per_elem": ab[dom], "elems_per_launch": w.d},
             "kernels": per_kernel,
             "warmup_adam_ms_per_step": warm_ms,

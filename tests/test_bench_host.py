@@ -18,34 +18,50 @@ def _records():
 
 
 def test_traffic_records_are_complete():
+    keys = set()
     for name, rec in _records().items():
-        for key in ("dram_bytes_per_elem", "n_workers", "grad_bytes", "step", "marker", "source_sha256_16",
-                    "captured_on", "summary"):
+        for key in ("kernel", "step", "n_workers", "grad_bytes", "n_tensors", "scale_block", "dram_bytes_per_elem",
+                    "scales_to_launch", "marker", "source_sha256_16", "captured_on", "summary"):
             assert key in rec, (name, key)
+        shape = (rec["kernel"], rec["step"], rec["n_workers"], rec["grad_bytes"], rec["n_tensors"], rec["scale_block"])
+        assert shape not in keys, name  # one record per kernel, step and shape
+        keys.add(shape)
         assert os.path.isfile(os.path.join(ROOT, rec["summary"])), rec["summary"]
         assert rec["step"] in ("compress", "warmup", "ec_adam")
         # traffic is a measurement of the algorithmic bytes: never far above, a little below when
-        # the previous kernel's output is still in L2
+        # the previous kernel's output (or this one's last writes) are still in L2
         alg = bench.algorithmic_bytes(rec["n_workers"], rec["grad_bytes"], rec["step"])
-        key = {"k_worker": "worker", "k_worker[ec_adam]": "worker", "k_server_staged": "server",
-               "k_warmup_staged": "warmup"}[name]
-        assert 0.75 * alg[key] <= rec["dram_bytes_per_elem"] <= 1.05 * alg[key], (name, alg[key])
+        bucket = {"k_worker": "worker", "k_server_staged": "server", "k_warmup_staged": "warmup", "k_warmup": "warmup",
+                  "k_update": "update", "k_ec_adam_update": "ec_update"}[rec["kernel"]]
+        assert 0.75 * alg[bucket] <= rec["dram_bytes_per_elem"] <= 1.05 * alg[bucket], (name, alg[bucket])
+        # only a record whose capture lost at most 2% to L2 is scaled to a full launch
+        assert rec["scales_to_launch"] == (rec["dram_bytes_per_elem"] >= 0.98 * alg[bucket]), name
 
 
 def test_traffic_lookup_matches_workload_and_source(monkeypatch):
-    recs = _records()
-    rec = recs["k_worker"]
-    d = 340_000_000
+    from communication_compressed_optimizer_compress_gb300 import workloads as W
+
+    w = W.WORKLOADS["bert_large"]
+    rec = next(r for r in _records().values() if r["kernel"] == "k_worker" and r["step"] == "compress")
+    assert (rec["n_workers"], rec["grad_bytes"], rec["n_tensors"]) == (w.n_workers, W.GRAD_BYTES[w.grad_dtype], 1)
     live = bench._kernel_source_hash(rec["marker"]) == rec["source_sha256_16"]
-    got = bench.traffic_from_profiles("k_worker", rec["n_workers"], rec["grad_bytes"], d)
-    assert got == (rec["dram_bytes_per_elem"] * d if live else None)
-    # another worker count or gradient width has no record: null, never the n=16 figure
-    assert bench.traffic_from_profiles("k_worker", rec["n_workers"] // 2, rec["grad_bytes"], d) is None
-    assert bench.traffic_from_profiles("k_worker", rec["n_workers"], 4, d) is None
-    assert bench.traffic_from_profiles("no_such_kernel", 16, 2, d) is None
+    got = bench.traffic_from_profiles("k_worker", "compress", w)
+    assert got == (rec["dram_bytes_per_elem"] * w.d if live else None)
+    # another shape has no record: null, never the figure of a different configuration
+    assert bench.traffic_from_profiles("k_worker", "compress", w.with_(n_workers=8)) is None
+    assert bench.traffic_from_profiles("k_worker", "compress", w.with_(grad_dtype=W.F32)) is None
+    assert bench.traffic_from_profiles("k_worker", "compress", w.with_(numel=(1000, 2000))) is None
+    assert bench.traffic_from_profiles("k_worker", "compress", w, scale_block=65536) is None
+    assert bench.traffic_from_profiles("k_worker", "warmup", w) is None
+    assert bench.traffic_from_profiles("no_such_kernel", "compress", w) is None
+    # a record that does not scale to a full launch is never scaled
+    for rec in _records().values():
+        if not rec["scales_to_launch"]:
+            shape = w.with_(n_workers=rec["n_workers"], grad_dtype={2: W.F16, 4: W.F32}[rec["grad_bytes"]])
+            assert bench.traffic_from_profiles(rec["kernel"], rec["step"], shape) is None, rec["kernel"]
     # a kernel whose source changed since the capture reads as null
     monkeypatch.setattr(bench, "_kernel_source_hash", lambda marker: "0" * 16)
-    assert bench.traffic_from_profiles("k_worker", rec["n_workers"], rec["grad_bytes"], d) is None
+    assert bench.traffic_from_profiles("k_worker", "compress", w) is None
 
 
 def test_algorithmic_bytes_closed_forms():
