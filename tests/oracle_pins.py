@@ -692,52 +692,100 @@ def _brute_rms(vals):
     return np.float32(math.sqrt(math.fsum(float(v) * float(v) for v in vals) / len(vals)))
 
 
-def pin_brute_force_compression_steps_small_d(ora):
-    """Several compression steps on d <= 64, restated here element by element in scalar fp32 from
-    the method's steps (worker momentum, error compensation, sign + rms scale per tensor, ordered
-    server average, server error, per-shard recompression, broadcast, preconditioned update), with
-    shards of 32*ceil(L/(32n)) and norms from exactly rounded sums.  Every state word must equal the
-    oracle's after every step: ragged lists with empty tensors, n in {1, 2, 3, 5}, zero gradients
-    (sign(0) = +1) and fp16 gradients."""
-    cases = [([64], 1, F32), ([33, 0, 31], 2, F32), ([5, 32, 27], 3, F16), ([1, 17, 40], 5, F32), ([64], 3, F32)]
-    for case, (numel, n, dtype) in enumerate(cases):
+def pin_brute_force_whole_algorithm_small_d(ora):
+    """The whole method on tiny inputs, restated here element by element in scalar fp32 from its
+    steps.  Warm-up Adam runs on the ordered mean of the worker gradients, with or without
+    Kingma-Ba correction.  The freeze gives den = sqrt(v) + eps.  Each compression step then runs
+    worker momentum, error compensation, sign + rms scale per tensor, the ordered server average,
+    the server error, per-shard recompression, the broadcast and the preconditioned update.
+    Shards are 32*ceil(L/(32n)) and norms come from exactly rounded sums.  Every state word must
+    equal the oracle's after every step.  Cases: the ragged list {1, 5, 32, 33} at
+    n in {1, 2, 3, 4, 8}, an empty tensor, a single 64-element tensor, zero gradients
+    (sign(0) = +1), and fp32, fp16 and bf16 gradients."""
+    cases = [([64], 1, F32, False), ([1, 5, 32, 33], 2, F32, False), ([1, 5, 32, 33], 3, F16, True),
+             ([1, 5, 32, 33], 4, BF16, False), ([1, 5, 32, 33], 8, F32, False), ([33, 0, 31], 5, F32, True),
+             ([64], 3, F32, False)]
+    T_w, steps = 2, 4
+    for case, (numel, n, dtype, bc) in enumerate(cases):
         rng = np.random.default_rng(300 + case)
         D, T = sum(numel), len(numel)
         offs = np.concatenate([[0], np.cumsum(numel)]).astype(int)
-        b1, lr = np.float32(0.9), np.float32(1e-2)
-        omb1 = np.float32(np.float32(1.0) - b1)
-        x = [np.float32(v) for v in rng.standard_normal(D) * 0.02]
-        den = [np.float32(v) for v in rng.uniform(1e-3, 1e-1, D)]
-        m = [np.float32(v) for v in rng.standard_normal(D) * 1e-3]
-        m[: D // 4] = [np.float32(0.0)] * (D // 4)
+        b1, b2, eps_adam, lr = np.float32(0.9), np.float32(0.999), np.float32(1e-8), np.float32(1e-2)
+        one = np.float32(1.0)
+        omb1, omb2 = np.float32(one - b1), np.float32(one - b2)
+        x0 = (rng.standard_normal(D) * 0.02).astype(np.float32)
+        x = list(x0)
+        m = [np.float32(0.0)] * D
+        v = [np.float32(0.0)] * D
+        o = ora.optimizer(numel, n, x0, beta1=float(b1), beta2=float(b2), eps=float(eps_adam), lr=float(lr),
+                          grad_dtype=dtype, bias_correction=bc)
+
+        def draw(zero_head):
+            flats, vals = [], []
+            for _ in range(n):
+                f = (rng.standard_normal(D) * 10 ** rng.uniform(-4, -2)).astype(np.float32)
+                if zero_head:
+                    f[: D // 4] = 0.0
+                if dtype == F16:
+                    f = f.astype(np.float16)
+                    vals.append([np.float32(e) for e in f])
+                elif dtype == BF16:
+                    f = (f.view(np.uint32) >> 16).astype(np.uint16)  # truncated to bf16 bits
+                    vals.append([(np.uint32(e) << np.uint32(16)).view(np.float32) for e in f])
+                else:
+                    vals.append(list(f))
+                flats.append(f)
+            return [f[offs[k]: offs[k + 1]] for f in flats for k in range(T)], vals
+
+        def check(name, want, where):
+            got = o.view(name)
+            assert np.array_equal(got.view(np.uint32), np.array(want, np.float32).view(np.uint32)), (where, name)
+
+        # warm-up: Adam on the ordered mean of the n gradients
+        for t in range(1, T_w + 1):
+            grads, g = draw(False)
+            o.warmup_step(grads)
+            bc1 = np.float32(1.0 - float(b1) ** t)
+            bc2 = np.float32(1.0 - float(b2) ** t)
+            for p in range(D):
+                acc = np.float32(0.0)
+                for i in range(n):
+                    acc = np.float32(acc + g[i][p])
+                gm = np.float32(acc / np.float32(n))
+                m[p] = np.float32(np.float32(b1 * m[p]) + np.float32(omb1 * gm))
+                v[p] = np.float32(np.float32(b2 * v[p]) + np.float32(omb2 * np.float32(gm * gm)))
+                mh, vh = (np.float32(m[p] / bc1), np.float32(v[p] / bc2)) if bc else (m[p], v[p])
+                x[p] = np.float32(x[p] - np.float32(lr * np.float32(mh / np.float32(np.sqrt(vh) + eps_adam))))
+            for name, want in (("x", x), ("m", m), ("v", v)):
+                check(name, want, f"case {case} warm-up {t}")
+
+        # freeze: den = sqrt(v) + eps (v bias-corrected at t = T_w when correction is on)
+        o.freeze()
+        bc2 = np.float32(1.0 - float(b2) ** T_w)
+        den = [np.float32(np.sqrt(np.float32(v[p] / bc2) if bc else v[p]) + eps_adam) for p in range(D)]
+        check("den", den, f"case {case} freeze")
         delta = [[np.float32(0.0)] * D for _ in range(n)]
         eps = [np.float32(0.0)] * D
-        o = _compress_ready(ora, numel, n, np.array(x, np.float32), np.array(den, np.float32),
-                            np.array(m, np.float32), beta1=float(b1), lr=float(lr), grad_dtype=dtype)
-        for step in range(4):
-            flats = []
-            for i in range(n):
-                f = (rng.standard_normal(D) * 10 ** rng.uniform(-4, -2)).astype(np.float32)
-                if step == 0:
-                    f[: D // 4] = 0.0  # with m = 0 there: c = 0, a bit of 1 and a lossless zero
-                flats.append(f.astype(np.float16) if dtype == F16 else f)
-            o.compress_step([f[offs[k]: offs[k + 1]] for f in flats for k in range(T)])
+
+        for step in range(steps):
+            grads, g = draw(step == 0)
+            o.compress_step(grads)
 
             # worker i: m_i = b1*m + (1-b1)*g_i, c_i = m_i + delta_i, then sign + scale per tensor
             wscale = np.zeros((n, T), np.float32)
             msg = [[None] * D for _ in range(n)]
             wbits = [[0] * D for _ in range(n)]
             for i in range(n):
-                c = [np.float32(b1 * m[p] + omb1 * np.float32(flats[i][p])) for p in range(D)]
+                c = [np.float32(np.float32(b1 * m[p]) + np.float32(omb1 * g[i][p])) for p in range(D)]
                 c = [np.float32(c[p] + delta[i][p]) for p in range(D)]
                 for k in range(T):
-                    s = _brute_rms(c[offs[k]: offs[k + 1]])
-                    wscale[i, k] = s
+                    sc = _brute_rms(c[offs[k]: offs[k + 1]])
+                    wscale[i, k] = sc
                     for p in range(offs[k], offs[k + 1]):
                         bit = c[p] >= 0
                         wbits[i][p] = int(bit)
-                        msg[i][p] = s if bit else -s
-                        delta[i][p] = np.float32(c[p] - s) if bit else np.float32(c[p] + s)
+                        msg[i][p] = sc if bit else -sc
+                        delta[i][p] = np.float32(c[p] - sc) if bit else np.float32(c[p] + sc)
             # server: ordered sum of the messages, / n, + server error; recompress per shard
             a = []
             for p in range(D):
@@ -767,15 +815,16 @@ def pin_brute_force_compression_steps_small_d(ora):
                         out.append(sum(bits[offs[k] + e] << (e - w0) for e in range(w0, min(w0 + 32, L))))
                 return np.array(out, np.uint32)
 
-            where = f"case {case} step {step}"
+            where = f"case {case} compression step {step}"
             assert np.array_equal(o.wscale, wscale), where
             assert np.array_equal(o.sscale, sscale), where
             for i in range(n):
                 assert np.array_equal(o.view("wbits")[i], words(wbits[i])), where
-                assert np.array_equal(o.view("delta")[i].view(np.uint32), np.array(delta[i], np.float32).view(np.uint32)), where
+                got = o.view("delta")[i].view(np.uint32)
+                assert np.array_equal(got, np.array(delta[i], np.float32).view(np.uint32)), where
             assert np.array_equal(o.view("sbits"), words(sbits)), where
             for name, want in (("eps_srv", eps), ("m", m), ("x", x)):
-                assert np.array_equal(o.view(name).view(np.uint32), np.array(want, np.float32).view(np.uint32)), (where, name)
+                check(name, want, where)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
