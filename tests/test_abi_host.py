@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import communication_compressed_optimizer_compress_gb300 as ob
@@ -72,73 +73,42 @@ def test_null_arguments_return_status():
 SHAPES = [[1], [5, 0, 33, 200], [65536 * 3 + 17], [1 << 20], [1000] * 7, [110_000_000], [1, 1, 1]]
 
 
-@pytest.mark.parametrize("numel", SHAPES, ids=lambda v: f"T{len(v)}_{sum(v)}")
-@pytest.mark.parametrize("n", [1, 3, 8, 16])
-def test_chunk_plan(numel, n):
-    """Chunks tile every tensor exactly once, never cross a server shard (the oracle's shard rule),
-    start on a 32-element boundary, hold at most 65536 elements, and the padded offsets keep every
-    tensor 32-element aligned."""
-    rows = ob.plan_chunks(ob.make_config(numel, n))
-    by_tensor = {k: [] for k in range(len(numel))}
-    for (k, j, start, length, off) in rows:
-        by_tensor[k].append((j, start, length, off))
-        assert 1 <= length <= 65536 and start % 32 == 0 and off % 32 == 0
-    pad_off = 0
-    for k, L in enumerate(numel):
-        ch = by_tensor[k]
-        pos = 0
-        for (j, start, length, off) in ch:
-            assert start == pos
-            lo, hi = oracle.shard(L, n, j)
-            assert lo <= start and start + length <= hi
-            assert off == pad_off + start
-            pos += length
-        assert pos == L
-        pad_off += (L + 31) // 32 * 32
-
-
-@pytest.mark.parametrize("numel,n,block", [([224, 0, 96], 2, 64), ([5000, 37], 20, 32), ([1 << 20], 4, 4096),
-                                            ([65536 * 3 + 17, 5], 3, 96), ([100], 4, 1 << 20)])
-def test_chunk_plan_scale_blocks(numel, n, block):
-    """With a scale block, the plan's segments are the blocks of the oracle's blocking rule: chunks
-    tile every block once, never cross that block's server shards, and keep the caller's padded
-    element offsets (blocks are multiples of 32, so only a tensor's last block can be ragged)."""
-    blocks = oracle.scale_blocks(numel, block)
+def _check_server_plan(numel, n, block=0):
+    """Server-side chunks tile every segment (a tensor, or a scale block of one) exactly once, never
+    cross a server shard (the oracle's shard rule), start on a 32-element boundary, hold at most
+    65536 elements, and keep the caller's padded element offsets."""
+    segs = oracle.scale_blocks(numel, block)
     rows = ob.plan_chunks(ob.make_config(numel, n, scale_block=block))
-    by_block = {b: [] for b in range(len(blocks))}
-    for (b, j, start, length, off) in rows:
-        by_block[b].append((j, start, length, off))
+    by_seg = {k: [] for k in range(len(segs))}
+    for (k, j, start, length, off) in rows:
+        by_seg[k].append((j, start, length, off))
+        assert 1 <= length <= 65536 and start % 32 == 0 and off % 32 == 0
     pad_starts, pad_off = [], 0
     for L in numel:
-        pad_starts.extend(pad_off + s for s in (range(0, L, block) if L else [0]))
+        pad_starts.extend(pad_off + s for s in (range(0, L, block) if (L and block) else [0]))
         pad_off += (L + 31) // 32 * 32
-    assert len(pad_starts) == len(blocks)
-    for b, L in enumerate(blocks):
+    assert len(pad_starts) == len(segs)
+    for k, L in enumerate(segs):
         pos = 0
-        for (j, start, length, off) in by_block[b]:
+        for (j, start, length, off) in by_seg[k]:
             assert start == pos
             lo, hi = oracle.shard(L, n, j)
             assert lo <= start and start + length <= hi
-            assert off == pad_starts[b] + start
+            assert off == pad_starts[k] + start
             pos += length
         assert pos == L
+    return rows
 
 
-WORKER_PLANS = [([1 << 20], 4, 0), ([1000], 16, 0), ([5, 0, 33, 200], 4, 0), ([340_000_000], 16, 0),
-                ([224, 0, 96], 3, 96), ([1 << 20], 16, 65536), ([70_001, 33, 0, 5], 3, 96), ([5000], 20, 32)]
-
-
-@pytest.mark.parametrize("numel,n,block", WORKER_PLANS, ids=[f"{sum(a)}_n{b}_B{c}" for a, b, c in WORKER_PLANS])
-def test_worker_chunk_plan(numel, n, block):
+def _check_worker_plan(numel, n, block=0):
     """Worker chunks tile every segment once, start on a 32-element boundary, hold at most one chunk
     length; a chunk that spans shards holds whole shards (its first shard and the recorded shard
     length follow the oracle's shard rule); where shards are at least a chunk long the worker table
     equals the server-side table."""
-    import oracle as _o
     cfg = ob.make_config(numel, n, scale_block=block)
     rows = ob.plan_worker_chunks(cfg)
     server = ob.plan_chunks(cfg)
-    segs = _o.scale_blocks(numel, block)
+    segs = oracle.scale_blocks(numel, block)
     want = -(-sum(numel) // 1216)
     clen = min(65536, max(4096, -(-want // 4096) * 4096))  # the chunk-length rule
     by_seg = {k: [] for k in range(len(segs))}
@@ -161,6 +131,59 @@ def test_worker_chunk_plan(numel, n, block):
         assert pos == L
         if per >= clen:
             assert [r[:5] for r in by_seg[k]] == [r for r in server if r[0] == k]
+    return rows
+
+
+@pytest.mark.parametrize("numel", SHAPES, ids=lambda v: f"T{len(v)}_{sum(v)}")
+@pytest.mark.parametrize("n", [1, 3, 8, 16])
+def test_chunk_plan(numel, n):
+    """The server-side table on fixed shapes (see _check_server_plan)."""
+    _check_server_plan(numel, n)
+
+
+def _random_plan_configs(count, seed):
+    """Seeded random lists: empty, tiny, ragged and multi-chunk tensors, worker counts 1..256, and
+    per-tensor or per-block scales."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        T = int(rng.integers(1, 41))
+        kind = rng.choice(5, size=T, p=[0.05, 0.2, 0.35, 0.35, 0.05])
+        lo = np.array([0, 1, 65, 5000, 1_000_000])[kind]
+        hi = np.array([1, 65, 5000, 300_000, 3_000_000])[kind]
+        numel = [int(rng.integers(a, b)) for a, b in zip(lo, hi)]
+        if not sum(numel):  # a list with no element at all is refused by design
+            numel[-1] = 1
+        n = int(rng.choice([1, 2, 3, 5, 7, 8, 13, 16, 17, 31, 64, 128, 200, 256]))
+        block = 0 if rng.random() < 0.6 else 32 * int(rng.integers(1, 4097))
+        out.append((numel, n, block))
+    return out
+
+
+@pytest.mark.parametrize("numel,n,block", _random_plan_configs(200, 2024),
+                         ids=lambda v: None if not isinstance(v, list) else f"T{len(v)}")
+def test_random_plans(numel, n, block):
+    """Both tables on seeded random configurations, against the oracle's shard and blocking rules."""
+    _check_server_plan(numel, n, block)
+    _check_worker_plan(numel, n, block)
+
+
+@pytest.mark.parametrize("numel,n,block", [([224, 0, 96], 2, 64), ([5000, 37], 20, 32), ([1 << 20], 4, 4096),
+                                            ([65536 * 3 + 17, 5], 3, 96), ([100], 4, 1 << 20)])
+def test_chunk_plan_scale_blocks(numel, n, block):
+    """With a scale block, the plan's segments are the blocks of the oracle's blocking rule (blocks
+    are multiples of 32, so only a tensor's last block can be ragged); see _check_server_plan."""
+    _check_server_plan(numel, n, block)
+
+
+WORKER_PLANS = [([1 << 20], 4, 0), ([1000], 16, 0), ([5, 0, 33, 200], 4, 0), ([340_000_000], 16, 0),
+                ([224, 0, 96], 3, 96), ([1 << 20], 16, 65536), ([70_001, 33, 0, 5], 3, 96), ([5000], 20, 32)]
+
+
+@pytest.mark.parametrize("numel,n,block", WORKER_PLANS, ids=[f"{sum(a)}_n{b}_B{c}" for a, b, c in WORKER_PLANS])
+def test_worker_chunk_plan(numel, n, block):
+    """The worker table on fixed shapes (see _check_worker_plan)."""
+    _check_worker_plan(numel, n, block)
 
 
 def test_oversized_plans_are_refused_before_they_are_built():
