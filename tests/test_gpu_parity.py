@@ -639,6 +639,39 @@ def test_scale_blocks(numel, n, dtype, block):
     p.close()
 
 
+def _random_parity_configs(count, seed):
+    """Seeded random lists for the parity sweep: empty, tiny, ragged and multi-chunk tensors, worker
+    counts across every server path, all gradient dtypes, per-tensor or per-block scales; a few
+    hundred thousand elements at most, so that the oracle keeps up."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        T = int(rng.integers(1, 13))
+        kind = rng.choice(4, size=T, p=[0.1, 0.3, 0.35, 0.25])
+        lo = np.array([0, 1, 65, 5000])[kind]
+        hi = np.array([1, 65, 5000, 60_000])[kind]
+        numel = [int(rng.integers(a, b)) for a, b in zip(lo, hi)]
+        if not sum(numel):
+            numel[-1] = 1
+        n = int(rng.choice([1, 2, 3, 5, 8, 13, 16, 17, 20, 33, 64, 129]))
+        dtype = int(rng.choice([W.F32, W.F16, W.BF16]))
+        block = 0 if rng.random() < 0.6 else 32 * int(rng.integers(1, 513))
+        out.append((tuple(numel), n, dtype, block, int(rng.integers(1 << 30))))
+    return out
+
+
+@pytest.mark.parametrize("numel,n,dtype,block,seed", _random_parity_configs(12, 7),
+                         ids=[f"r{i}" for i in range(12)])
+def test_random_configs(numel, n, dtype, block, seed):
+    """The CUDA path against the oracle on seeded random parameter lists: warm-up, freeze and
+    compression steps compared after every step, as in the fixed cases."""
+    w = _tiny(numel=numel, n_workers=n, grad_dtype=dtype, warmup_steps=2, compress_steps=3, seed=seed)
+    p = Pair(w, scale_block=block)
+    st = p.run()
+    assert st.scales_exact >= 0.99 * st.scales, st
+    p.close()
+
+
 def test_cuda_graph_replay_equals_eager():
     """A compression step enqueues kernels only (no host synchronisation or allocation), so a pair
     of steady-state steps (one full cycle of the double-buffered scales) can be captured in a CUDA
