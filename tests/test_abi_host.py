@@ -221,3 +221,24 @@ def test_comm_bytes_volume_reduction_closed_form():
     numel = [340_000_000]
     compressed = sum(((L + 31) // 32) * 4 + 4 for L in numel)
     assert abs(compressed / (4 * numel[0]) - 1 / 32) < 1e-6
+
+
+def test_missing_library_raises_instead_of_falling_back(monkeypatch):
+    """Without the built library every entry point raises at once: there is no CPU path."""
+    pkg = ob
+    monkeypatch.setattr(pkg, "_lib", None)
+    monkeypatch.setattr(pkg, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libonebit_adam.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        pkg.lib()
+    with pytest.raises(RuntimeError, match="missing"):
+        pkg.workspace_size(pkg.make_config([10], 2))
+
+
+def test_binding_refuses_host_or_non_fp32_parameters():
+    """The optimizer takes contiguous fp32 CUDA tensors only; anything else is refused before the
+    library is called."""
+    import torch
+
+    for bad in (torch.zeros(64), torch.zeros(64, dtype=torch.float64), torch.zeros(8, 8).t()):
+        with pytest.raises(ValueError, match="fp32 CUDA"):
+            ob.OneBitAdam([bad], 2, 1)
