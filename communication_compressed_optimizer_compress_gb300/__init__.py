@@ -114,6 +114,8 @@ def _check(status: int, where: str, handle=None):
         detail = ""
         if handle:
             detail = lib().onebit_adam_last_error(handle).decode()
+        elif where == "onebit_adam_init":  # a failed init leaves its message on the thread
+            detail = lib().onebit_adam_last_error(None).decode()
         raise OneBitError(status, where, detail)
 
 

@@ -326,6 +326,10 @@ onebit_status_t cuda_fail(onebit_adam* h, cudaError_t e, const char* where) {
   return ONEBIT_ERR_CUDA;
 }
 
+// The CUDA message of the last onebit_adam_init that failed on this thread: its handle is gone, so
+// onebit_adam_last_error(NULL) returns this.
+thread_local std::string t_init_error;
+
 #define ONEBIT_CUDA(h, call)                                  \
   do {                                                        \
     cudaError_t e_ = (call);                                  \
@@ -772,7 +776,7 @@ const char* onebit_adam_error_string(onebit_status_t s) {
   return "unknown status";
 }
 
-const char* onebit_adam_last_error(const onebit_adam_t* h) { return h ? h->last_error.c_str() : ""; }
+const char* onebit_adam_last_error(const onebit_adam_t* h) { return h ? h->last_error.c_str() : t_init_error.c_str(); }
 
 onebit_status_t onebit_adam_workspace_size(const onebit_adam_config_t* cfg, size_t* bytes) {
   return guarded([&]() -> onebit_status_t {
@@ -849,6 +853,7 @@ onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* 
       onebit_adam* h;
       bool cuda;  // the handle holds CUDA resources: free it through onebit_adam_free
       ~Release() {
+        if (h) t_init_error = h->last_error;
         if (h && cuda) onebit_adam_free(h);
         else delete h;
       }

@@ -291,7 +291,10 @@ onebit_status_t onebit_worker_compress_noalloc(const float* m, const void* grad,
 
 /* Static description of a status code. */
 const char* onebit_adam_error_string(onebit_status_t status);
-/* Message of the last CUDA failure seen by this handle ("" if none). */
+/* Message of the last CUDA failure seen by this handle ("" if none).  With h = NULL: the message of
+ * the last onebit_adam_init that failed on the calling thread ("" if none), since a failed init
+ * returns no handle.  The string stays valid until the next call on the same handle (or, for
+ * NULL, the next onebit_adam_init on this thread). */
 const char* onebit_adam_last_error(const onebit_adam_t* h);
 
 #ifdef __cplusplus

@@ -242,3 +242,21 @@ def test_binding_refuses_host_or_non_fp32_parameters():
     for bad in (torch.zeros(64), torch.zeros(64, dtype=torch.float64), torch.zeros(8, 8).t()):
         with pytest.raises(ValueError, match="fp32 CUDA"):
             ob.OneBitAdam([bad], 2, 1)
+
+
+def test_failed_init_keeps_its_message_without_a_handle():
+    """On a host with no CUDA device, init fails with ONEBIT_ERR_CUDA, returns no handle, and the
+    CUDA message is available from onebit_adam_last_error(NULL) (a failed init has no handle)."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("needs a host without a CUDA device")
+    L = ob.lib()
+    cfg = ob.make_config([1024], 2)
+    ptrs = (ctypes.c_void_p * 1)(0x1000)  # never dereferenced: there is no device to reach
+    h = ctypes.c_void_p()
+    assert L.onebit_adam_init(ctypes.byref(cfg), ptrs, None, 0, None, ctypes.byref(h)) == ob.ERR_CUDA
+    assert not h.value
+    assert "cudaGetDevice" in L.onebit_adam_last_error(None).decode()
+    with pytest.raises(ob.OneBitError, match="cudaGetDevice"):
+        ob._check(ob.ERR_CUDA, "onebit_adam_init")
