@@ -260,3 +260,25 @@ def test_failed_init_keeps_its_message_without_a_handle():
     assert "cudaGetDevice" in L.onebit_adam_last_error(None).decode()
     with pytest.raises(ob.OneBitError, match="cudaGetDevice"):
         ob._check(ob.ERR_CUDA, "onebit_adam_init")
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/onebit_adam.h is a C header: it compiles as C99 and as C++ with no CUDA or torch
+    header, and a C program can take the address of every entry point it declares."""
+    import shutil
+    import subprocess
+
+    hdr = os.path.join(ROOT, "include", "onebit_adam.h")
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(onebit_\w+)\(", open(hdr).read(), re.M)
+    assert len(names) >= 20
+    src = tmp_path / "use.c"
+    src.write_text('#include "onebit_adam.h"\n'
+                   "typedef void (*entry_t)(void);\n"
+                   "entry_t table[] = {\n" + ",\n".join(f"  (entry_t){n}" for n in names) + "\n};\n")
+    for cc, std in (("gcc", "-std=c99"), ("g++", "-std=c++17")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not available")
+        lang = ["-x", "c++"] if cc == "g++" else []
+        r = subprocess.run([cc, *lang, std, "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
+                            "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
