@@ -499,9 +499,11 @@ onebit_status_t run_warmup_m(onebit_adam* h, const StepArgs& A, bool vec, cudaSt
     }
   }
   auto pick = [&](auto kern) { return launch(h, ONEBIT_K_WARMUP, kern, grid_for(h, (const void*)kern, kThreads, C), kThreads, st, A); };
-  if (A.n <= 4 && sizeof(GT) == 2) {  // 16-bit gradients, all in one small batch (measured slower for fp32)
-    if (bc) return vec ? pick(k_warmup<GT, true, true, MON, true>) : pick(k_warmup<GT, true, false, MON, true>);
-    return vec ? pick(k_warmup<GT, false, true, MON, true>) : pick(k_warmup<GT, false, false, MON, true>);
+  if constexpr (sizeof(GT) == 2) {  // 16-bit gradients, all in one small batch (measured slower for fp32)
+    if (A.n <= 4) {
+      if (bc) return vec ? pick(k_warmup<GT, true, true, MON, true>) : pick(k_warmup<GT, true, false, MON, true>);
+      return vec ? pick(k_warmup<GT, false, true, MON, true>) : pick(k_warmup<GT, false, false, MON, true>);
+    }
   }
   if (bc) return vec ? pick(k_warmup<GT, true, true, MON, false>) : pick(k_warmup<GT, true, false, MON, false>);
   return vec ? pick(k_warmup<GT, false, true, MON, false>) : pick(k_warmup<GT, false, false, MON, false>);
