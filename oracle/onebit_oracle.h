@@ -17,8 +17,8 @@
  *        recompression, broadcast of m_{t+1}).
  *   [P2] "1-bit Adam (Two-Stage Preconditioner-Frozen Error-Compensated Adam)" (AIMech curated page):
  *        summary formulas v_t = b2 v + (1-b2) g^2, m_t = b1 m + (1-b1) g, V = diag(sqrt(v_Tw)+eps),
- *        x_t = x_{t-1} - gamma V^{-1} m_hat_t; mechanism "gather-then-broadcast" with worker error
- *        memory delta^(i) and server shard error memory epsilon.
+ *        x_t = x_{t-1} - gamma V^{-1} m_hat_t; a "gather-then-broadcast" exchange in which every
+ *        worker keeps an error memory delta^(i) and every server shard keeps one, epsilon.
  *   [P4] "1-bit Adam" (codewithpapers method page): scale = |compensated| / |quantized|.
  *
  * Precision.  The pages do not fix a precision.  State (x, m, v/den, worker and server errors) is

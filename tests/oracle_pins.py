@@ -349,8 +349,8 @@ def pin_compress_golden_n2(ora):
 def _momentum_sgd_case(ora, n, identical):
     """Equal-magnitude momenta with a common sign pattern are compressed losslessly at the workers
     and at the server, so the compression stage reduces to momentum SGD with the coordinate-wise
-    learning rate lr / (sqrt(v) + eps) (Sec. 3.3: with constant variance Adam is momentum SGD with a
-    coordinate-dependent learning rate)."""
+    learning rate lr / (sqrt(v) + eps) (Sec. 3.3: once v is held fixed, each Adam step is a momentum
+    step whose step size differs per coordinate)."""
     rng = np.random.default_rng(9 + n)
     d, steps = 96, 6
     sig = np.where(rng.random(d) < 0.5, -1.0, 1.0)
