@@ -282,3 +282,42 @@ def test_header_is_plain_c(tmp_path):
         r = subprocess.run([cc, *lang, std, "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
                             "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def _kernel_constant(name):
+    src = open(os.path.join(ROOT, "communication_compressed_optimizer_compress_gb300", "csrc", "onebit_kernels.cuh")).read()
+    m = re.search(r"constexpr int %s = ([^;]+);" % name, src)
+    return m.group(1)
+
+
+@pytest.mark.parametrize("numel,n,block", _random_plan_configs(200, 2024)[::4] + [([340_000_000], 16, 0),
+                                                                                  ([1 << 20, 5, 33], 128, 0)],
+                         ids=lambda v: None if not isinstance(v, list) else f"T{len(v)}")
+def test_staged_server_copy_windows_stay_in_bounds(numel, n, block):
+    """The staged server's bulk copies, recomputed on the host from the plan and the kernel's own
+    constants, for every tile of every chunk.  Each worker's sign bytes are copied as a window
+    widened to 16-byte boundaries, and each tile's a values as whole 32-element words.  Both must
+    stay inside the worker's sign row (stride Wr words) and the padded state, meet the bulk-copy
+    rules (16-byte aligned addresses, sizes in multiples of 16), and fit the stage's row slot."""
+    kTile = int(_kernel_constant("kTile"))
+    expr = _kernel_constant("kRowBytes").replace("kTile", str(kTile))
+    assert re.fullmatch(r"[0-9+*/ ()]+", expr), expr
+    kRowBytes = int(eval(expr.replace("/", "//"), {"__builtins__": {}}))
+    rows = ob.plan_chunks(ob.make_config(numel, n, scale_block=block))
+    Dp = sum((L + 31) // 32 * 32 for L in numel)
+    Wp = Dp // 32
+    Wr = (Wp + 3) // 4 * 4
+    for (_, _, _, length, off) in rows:
+        for e0 in range(0, length, kTile):
+            tlen = min(kTile, length - e0)
+            # a: ceil(tlen / 32) words of 32 floats from element off + e0
+            a0, abytes = (off + e0) * 4, (tlen + 31) // 32 * 32 * 4
+            assert a0 % 16 == 0 and abytes % 16 == 0 and (off + e0) + abytes // 4 <= Dp
+            assert abytes <= kTile * 4
+            # every worker's sign bytes, widened to a 16-byte window inside its row
+            byte0, nb = (off + e0) >> 3, (tlen + 7) // 8
+            wlo = byte0 & ~15
+            wlen = ((byte0 & 15) + nb + 15) & ~15
+            assert wlo % 16 == 0 and wlen % 16 == 0 and (Wr * 4) % 16 == 0
+            assert wlo + wlen <= Wr * 4
+            assert wlen <= kRowBytes and (byte0 & 15) + nb <= wlen
