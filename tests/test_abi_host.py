@@ -321,3 +321,47 @@ def test_staged_server_copy_windows_stay_in_bounds(numel, n, block):
             assert wlo % 16 == 0 and wlen % 16 == 0 and (Wr * 4) % 16 == 0
             assert wlo + wlen <= Wr * 4
             assert wlen <= kRowBytes and (byte0 & 15) + nb <= wlen
+
+
+def test_binding_constants_and_config_layout_match_the_header(tmp_path):
+    """The binding restates the header's enums and its config struct for ctypes.  A C program built
+    against the header prints the values, the struct's size and every field's offset; they must
+    equal the binding's."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    enums = {
+        "ONEBIT_OK": ob.OK, "ONEBIT_ERR_INVALID_ARG": ob.ERR_INVALID_ARG, "ONEBIT_ERR_PHASE": ob.ERR_PHASE,
+        "ONEBIT_ERR_CUDA": ob.ERR_CUDA, "ONEBIT_ERR_NOMEM": ob.ERR_NOMEM, "ONEBIT_ERR_WORKSPACE": ob.ERR_WORKSPACE,
+        "ONEBIT_ERR_NONFINITE": ob.ERR_NONFINITE, "ONEBIT_ERR_UNSUPPORTED": ob.ERR_UNSUPPORTED,
+        "ONEBIT_F32": ob.F32, "ONEBIT_F16": ob.F16, "ONEBIT_BF16": ob.BF16,
+        "ONEBIT_PHASE_WARMUP": ob.PHASE_WARMUP, "ONEBIT_PHASE_COMPRESS": ob.PHASE_COMPRESS,
+        "ONEBIT_STATE_M": ob.STATE_M, "ONEBIT_STATE_V": ob.STATE_V, "ONEBIT_STATE_WORKER_ERROR": ob.STATE_WORKER_ERROR,
+        "ONEBIT_STATE_SERVER_ERROR": ob.STATE_SERVER_ERROR, "ONEBIT_STATE_WORKER_BITS": ob.STATE_WORKER_BITS,
+        "ONEBIT_STATE_SERVER_BITS": ob.STATE_SERVER_BITS, "ONEBIT_STATE_WORKER_SCALES": ob.STATE_WORKER_SCALES,
+        "ONEBIT_STATE_SERVER_SCALES": ob.STATE_SERVER_SCALES,
+        "ONEBIT_FAULT_NONE": ob.FAULT_NONE, "ONEBIT_FAULT_STALL_COPIES": ob.FAULT_STALL_COPIES,
+        "ONEBIT_FAULT_FAIL_ALLOC": ob.FAULT_FAIL_ALLOC, "ONEBIT_NUM_KERNELS": ob.NUM_KERNELS,
+    }
+    kernels = ["WARMUP", "FREEZE", "WORKER", "WORKER_SCALE", "SERVER", "SERVER_SCALE", "UPDATE", "EXPORT", "EC_UPDATE"]
+    for k, name in enumerate(kernels):
+        enums[f"ONEBIT_K_{name}"] = ob.KERNEL_NAMES.index(name.lower())
+    fields = [f[0] for f in ob.Config._fields_]
+    lines = [f'  printf("{e} %d\\n", (int){e});' for e in enums]
+    lines.append('  printf("sizeof %zu\\n", sizeof(onebit_adam_config_t));')
+    lines += [f'  printf("{f} %zu\\n", offsetof(onebit_adam_config_t, {f}));' for f in fields]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "onebit_adam.h"\nint main(void) {\n'
+                   + "\n".join(lines) + "\n  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    r = subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True).stdout.splitlines())
+    for e, v in enums.items():
+        assert int(got[e]) == v, e
+    assert int(got["sizeof"]) == ctypes.sizeof(ob.Config)
+    for f in fields:
+        assert int(got[f]) == getattr(ob.Config, f).offset, f
