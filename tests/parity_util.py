@@ -52,6 +52,24 @@ def _close(name, got, want, mask=None, rtol=RTOL, atol=ATOL):
                              f"gpu {got[idx]} oracle {want[idx]}")
 
 
+def _close_t(name, got, want, mask=None, rtol=RTOL, atol=ATOL):
+    """_close on device tensors (fp64); rtol may be a tensor of the same shape as got."""
+    got = got.reshape(-1).double()
+    want = want.reshape(-1).double().to(got.device)
+    if torch.is_tensor(rtol):
+        rtol = rtol.reshape(-1).to(got.device)
+    if mask is not None:
+        got, want = got[mask], want[mask]
+        if torch.is_tensor(rtol):
+            rtol = rtol[mask]
+    bad = ~((got - want).abs() <= atol + rtol * want.abs())
+    bad |= torch.isnan(got) != torch.isnan(want)
+    if bool(bad.any()):
+        idx = torch.nonzero(bad)[:5].flatten()
+        raise AssertionError(f"{name}: {int(bad.sum())} of {bad.numel()} differ, e.g. at {idx.tolist()}: "
+                             f"gpu {got[idx].tolist()} oracle {want[idx].tolist()}")
+
+
 def _bits(words, D, offs, woffs, numel):
     """Unpack sign words (tensor-wise word layout) into a bool vector of the D elements."""
     words = np.asarray(words).view(np.uint32)
@@ -68,11 +86,14 @@ def _bits(words, D, offs, woffs, numel):
 class Pair:
     """A CUDA optimizer and an oracle optimizer stepped in lock-free parallel on the same inputs."""
 
-    def __init__(self, w: W.Workload, device="cuda:0", bias_correction=False, misalign=False, scale_block=0):
+    def __init__(self, w: W.Workload, device="cuda:0", bias_correction=False, misalign=False, scale_block=0,
+                 gen_device="cpu"):
         self.w = w
         self.dev = torch.device(device)
-        self.src = W.GradSource(w, "cpu")
-        x0 = W.params(w, "cpu")
+        # the seeded inputs are drawn on `gen_device` (the device is faster for the large cases); both
+        # sides get the same values: the CUDA path the tensors, the oracle their host copies
+        self.src = W.GradSource(w, gen_device)
+        x0 = [p.cpu() for p in W.params(w, gen_device)]
         self.misalign = misalign
         if misalign:
             # parameters that start 4 bytes into an allocation: the kernels must take the scalar path
@@ -94,7 +115,6 @@ class Pair:
         self.offs = np.concatenate([[0], np.cumsum(self.numel)]).astype(np.int64)
         self.woffs = np.concatenate([[0], np.cumsum([(L + 31) // 32 for L in self.numel])]).astype(np.int64)
         self.step_idx = 0
-        self.excl_w = np.zeros((w.n_workers, self.D), bool)
         self.excl_s = np.zeros(self.D, bool)
         self.stats = Stats()
 
@@ -161,79 +181,123 @@ class Pair:
         _close("m (warm-up)", gm, self.ora.view("m"))
         _close("v (warm-up)", gv, self.ora.view("v"))
 
+    def _index(self):
+        """Element -> (sign word, bit, segment, server shard) tables on the device, built once."""
+        if getattr(self, "_idx", None) is None:
+            dev, n = self.dev, self.w.n_workers
+            D, T = self.D, len(self.numel)
+            word = torch.empty(D, dtype=torch.int64, device=dev)
+            bit = torch.empty(D, dtype=torch.int32, device=dev)
+            seg = torch.empty(D, dtype=torch.int64, device=dev)
+            shard = torch.empty(D, dtype=torch.int64, device=dev)
+            for k, L in enumerate(self.numel):
+                if L == 0:
+                    continue
+                a, b = int(self.offs[k]), int(self.offs[k + 1])
+                e = torch.arange(L, device=dev, dtype=torch.int64)
+                word[a:b] = int(self.woffs[k]) + e // 32
+                bit[a:b] = (e % 32).to(torch.int32)
+                seg[a:b] = k
+                per = 32 * -(-L // (32 * n))
+                shard[a:b] = k * n + e // per
+            self._idx = (word, bit, seg, shard)
+        return self._idx
+
+    def _unpack(self, words):
+        """Sign words (tensor-wise word layout, any 32-bit dtype) -> bool per element, on the device."""
+        word, bit, _, _ = self._index()
+        if not torch.is_tensor(words):
+            words = torch.from_numpy(np.ascontiguousarray(words).view(np.int32))
+        w = words.to(self.dev).view(torch.int32)
+        return ((w[word] >> bit) & 1).bool()
+
+    def _dev(self, a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+
     def check_compress(self, ec=False):
+        """The parity protocol (module docstring), evaluated in fp64 on the device."""
         torch.cuda.synchronize()
         assert self.gpu.get_status() == ob.OK
-        w, o, n = self.w, self.ora, self.w.n_workers
+        o, n, dev = self.ora, self.w.n_workers, self.dev
+        T = len(self.numel)
         st = self.stats
         st.steps += 1
         st.coords += self.D
-        gws = self.gpu.export_state(ob.STATE_WORKER_SCALES).cpu().numpy().reshape(n, -1)
-        gss = self.gpu.export_state(ob.STATE_SERVER_SCALES).cpu().numpy().reshape(-1, n)
-        seg_of = np.repeat(np.arange(len(self.numel)), self.numel)
+        _, _, seg, shard = self._index()
+        numel_t = torch.tensor(self.numel, dtype=torch.float64, device=dev)
+        gws = self.gpu.export_state(ob.STATE_WORKER_SCALES).reshape(n, T).double()
+        gss = self.gpu.export_state(ob.STATE_SERVER_SCALES).reshape(T, n).double()
+        ows = self._dev(o.wscale).reshape(n, T).double()
+        oss = self._dev(o.sscale).reshape(T, n).double()
         # Coordinates excluded at an earlier step stay excluded everywhere: once the two sides
         # carry different error memories or a different m there, every later value at that
         # coordinate may differ.
-        G = self.excl_s.copy()
-        band_w = np.zeros((n, self.D), bool)
+        G = self._dev(self.excl_s)
+        band_any = torch.zeros(self.D, dtype=torch.bool, device=dev)
+        n_band_w = 0
         # ---- workers
         for i in range(n):
-            ob_bits = _bits(o.view("wbits")[i], self.D, self.offs, self.woffs, self.numel)
-            s_el = o.wscale[i][seg_of].astype(np.float64) if self.D else np.zeros(0)
-            c_ora = o.view("delta")[i].astype(np.float64) + np.where(ob_bits, s_el, -s_el)
-            band_w[i] = np.abs(c_ora) < BAND * s_el
-            keep = ~(G | band_w[i])
-            gw = self.gpu.export_state(ob.STATE_WORKER_BITS, i).cpu().numpy()
-            g_bits = _bits(gw, self.D, self.offs, self.woffs, self.numel)
-            if not np.array_equal(g_bits[keep], ob_bits[keep]):
-                bad = np.flatnonzero((g_bits != ob_bits) & keep)[:5]
-                raise AssertionError(f"worker {i}: sign bits differ at {bad}")
-            if keep.all():  # full words, padding bits included
-                assert np.array_equal(gw.view(np.uint32), o.view("wbits")[i])
-            gd = self.gpu.export_state(ob.STATE_WORKER_ERROR, i).cpu().numpy()
-            _close(f"worker {i} error", gd, o.view("delta")[i], keep)
-            for k, L in enumerate(self.numel):
-                nex = int((~keep[self.offs[k]: self.offs[k + 1]]).sum())
-                rt = 3e-7 + (8.0 * nex / L if L else 0.0)
-                _close(f"worker {i} scale of tensor {k}", gws[i, k], o.wscale[i, k], rtol=rt, atol=0)
-                st.scales += 1
-                st.scales_exact += int(np.float32(gws[i, k]) == o.wscale[i, k])
-        self.excl_w |= band_w
-        st.excluded_worker += int(band_w.sum())
+            ob_bits = self._unpack(o.view("wbits")[i])
+            s_el = ows[i][seg]
+            d_ora = self._dev(o.view("delta")[i]).double()
+            c_ora = d_ora + torch.where(ob_bits, s_el, -s_el)
+            band = c_ora.abs() < BAND * s_el
+            keep = ~(G | band)
+            gw = self.gpu.export_state(ob.STATE_WORKER_BITS, i)
+            g_bits = self._unpack(gw)
+            bad = (g_bits != ob_bits) & keep
+            if bool(bad.any()):
+                raise AssertionError(f"worker {i}: sign bits differ at {torch.nonzero(bad)[:5].flatten().tolist()}")
+            if bool(keep.all()):  # full words, padding bits included
+                assert torch.equal(gw.view(torch.int32).cpu(), torch.from_numpy(
+                    np.ascontiguousarray(o.view("wbits")[i]).view(np.int32)))
+            gd = self.gpu.export_state(ob.STATE_WORKER_ERROR, i)
+            _close_t(f"worker {i} error", gd, d_ora, keep)
+            nex = torch.zeros(T, dtype=torch.float64, device=dev).index_add_(0, seg, (~keep).double())
+            rt = 3e-7 + torch.where(numel_t > 0, 8.0 * nex / numel_t.clamp(min=1), torch.zeros_like(nex))
+            _close_t(f"worker {i} scales", gws[i], ows[i], rtol=rt, atol=0.0)
+            st.scales += T
+            st.scales_exact += int((gws[i].float() == ows[i].float()).sum())
+            band_any |= band
+            n_band_w += int(band.sum())
+        st.excluded_worker += n_band_w
         st.worker_draws += n * self.D
         # ---- server
-        sb_ora = _bits(o.view("sbits"), self.D, self.offs, self.woffs, self.numel)
-        S_el = np.zeros(self.D)
-        for k, L in enumerate(self.numel):
-            for j in range(n):
-                lo, hi = oracle.shard(L, n, j)
-                S_el[self.offs[k] + lo: self.offs[k] + hi] = o.sscale[k, j]
-        a_ora = o.view("eps_srv").astype(np.float64) + np.where(sb_ora, S_el, -S_el)
-        band_s = np.abs(a_ora) < BAND * S_el
-        self.excl_s = G | band_w.any(axis=0) | band_s
-        keep = ~self.excl_s
-        gsb = self.gpu.export_state(ob.STATE_SERVER_BITS).cpu().numpy()
-        g_sbits = _bits(gsb, self.D, self.offs, self.woffs, self.numel)
-        if not np.array_equal(g_sbits[keep], sb_ora[keep]):
-            bad = np.flatnonzero((g_sbits != sb_ora) & keep)[:5]
-            raise AssertionError(f"server sign bits differ at {bad}")
-        if keep.all():
-            assert np.array_equal(gsb.view(np.uint32), o.view("sbits"))
-        st.bit_words_compared += gsb.size * (n + 1)
-        _close("server error", self.gpu.export_state(ob.STATE_SERVER_ERROR).cpu().numpy(), o.view("eps_srv"), keep)
-        _close("m", self.gpu.export_state(ob.STATE_M).cpu().numpy(), o.view("m"), keep)
-        _close("x", self.x(), o.view("x"), keep)
+        sb_ora = self._unpack(o.view("sbits"))
+        S_el = oss.reshape(-1)[shard]
+        e_ora = self._dev(o.view("eps_srv")).double()
+        a_ora = e_ora + torch.where(sb_ora, S_el, -S_el)
+        band_s = a_ora.abs() < BAND * S_el
+        excl = G | band_any | band_s
+        keep = ~excl
+        gsb = self.gpu.export_state(ob.STATE_SERVER_BITS)
+        g_sbits = self._unpack(gsb)
+        bad = (g_sbits != sb_ora) & keep
+        if bool(bad.any()):
+            raise AssertionError(f"server sign bits differ at {torch.nonzero(bad)[:5].flatten().tolist()}")
+        if bool(keep.all()):
+            assert torch.equal(gsb.view(torch.int32).cpu(), torch.from_numpy(
+                np.ascontiguousarray(o.view("sbits")).view(np.int32)))
+        st.bit_words_compared += gsb.numel() * (n + 1)
+        _close_t("server error", self.gpu.export_state(ob.STATE_SERVER_ERROR), e_ora, keep)
+        _close_t("m", self.gpu.export_state(ob.STATE_M), self._dev(o.view("m")), keep)
+        _close_t("x", self._x_dev(), self._dev(o.view("x")), keep)
         if ec:
-            _close("v", self.gpu.export_state(ob.STATE_V).cpu().numpy(), o.view("v"), keep)
-        for k, L in enumerate(self.numel):
-            for j in range(n):
-                lo, hi = oracle.shard(L, n, j)
-                nex = int(self.excl_s[self.offs[k] + lo: self.offs[k] + hi].sum())
-                rt = 3e-7 + (8.0 * nex / (hi - lo) if hi > lo else 0.0)
-                _close(f"server scale ({k},{j})", gss[k, j], o.sscale[k, j], rtol=rt, atol=0)
-                st.scales += 1
-                st.scales_exact += int(np.float32(gss[k, j]) == o.sscale[k, j])
-        st.excluded_server = int(self.excl_s.sum())
+            _close_t("v", self.gpu.export_state(ob.STATE_V), self._dev(o.view("v")), keep)
+        lens = torch.tensor([oracle.shard(L, n, j)[1] - oracle.shard(L, n, j)[0]
+                             for L in self.numel for j in range(n)], dtype=torch.float64, device=dev)
+        nex = torch.zeros(T * n, dtype=torch.float64, device=dev).index_add_(0, shard, excl.double())
+        rt = 3e-7 + torch.where(lens > 0, 8.0 * nex / lens.clamp(min=1), torch.zeros_like(nex))
+        _close_t("server scales", gss.reshape(-1), oss.reshape(-1), rtol=rt, atol=0.0)
+        st.scales += T * n
+        st.scales_exact += int((gss.float() == oss.float()).sum())
+        self.excl_s = excl.cpu().numpy()
+        st.excluded_server = int(excl.sum())
+
+    def _x_dev(self):
+        if self.D == 0:
+            return torch.zeros(0, device=self.dev)
+        return torch.cat([p.detach().reshape(-1) for p in self.params])
 
     def run(self, warm=None, comp=None):
         warm = self.w.warmup_steps if warm is None else warm
