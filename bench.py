@@ -197,6 +197,49 @@ def barrier():
 
 # ---------------------------------------------------------------------------------------- oracle
 
+def host_cpu():
+    """The host's core count and CPU model name (lscpu's "Model name", else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith(("model name", "cpu model")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return {"nproc": os.cpu_count(), "model": model}
+
+
+class pinned_to_core0:
+    """Run the enclosed host work on core 0 alone (the single-threaded oracle timing protocol)."""
+
+    def __enter__(self):
+        self.prev = None
+        try:
+            self.prev = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, {0})
+            self.pinned = True
+        except Exception:
+            self.pinned = False
+        return self
+
+    def __exit__(self, *a):
+        if self.prev is not None:
+            try:
+                os.sched_setaffinity(0, self.prev)
+            except Exception:
+                pass
+
+
 def oracle_sample(w, seconds: float = 12.0, d_sample: int = 1 << 21):
     """Time the oracle (single-threaded C) on a bounded sample of the workload: the same worker
     count, gradient dtype and law on a flat buffer of d_sample parameters; one warm-up step, the
@@ -215,19 +258,23 @@ def oracle_sample(w, seconds: float = 12.0, d_sample: int = 1 << 21):
     o.warmup_step(sets[0])
     o.freeze()
     times = []
-    t_all = time.perf_counter()
-    k = 0
-    while True:
-        t0 = time.perf_counter()
-        o.compress_step(sets[k % 2])
-        times.append(time.perf_counter() - t0)
-        k += 1
-        if time.perf_counter() - t_all > seconds and k >= 1:
-            break
+    with pinned_to_core0() as pin:
+        t_all = time.perf_counter()
+        k = 0
+        while True:
+            t0 = time.perf_counter()
+            o.compress_step(sets[k % 2])
+            times.append(time.perf_counter() - t0)
+            k += 1
+            if time.perf_counter() - t_all > seconds and k >= 1:
+                break
     per = statistics.median(times)
+    cpu = host_cpu()
     return {"value": d_sample / per, "unit": "params/s", "cores": 1, "kind": "oracle",
-            "sample": f"{ws.name} law, flat d={d_sample}, n={ws.n_workers}, "
-                      f"{W.DTYPE_NAME[ws.grad_dtype]} grads, {k} compression steps (median), single thread",
+            "sample": f"{ws.name} law, flat d={d_sample} (a sample of the d={w.d} workload), n={ws.n_workers}, "
+                      f"{W.DTYPE_NAME[ws.grad_dtype]} grads, {k} compression steps (median), single thread"
+                      f"{' pinned to core 0' if pin.pinned else ''}",
+            "d_sample": d_sample, "pinned_core0": pin.pinned, "host_nproc": cpu["nproc"], "host_cpu": cpu["model"],
             "s_per_step": per, "steps": k}
 
 
@@ -270,26 +317,128 @@ def run_reference(args, w):
     if d != ws.d:
         ws, o, sets = make(d)
         o.compress_step(sets[0])
-    for s in range(1, Wm):
-        o.compress_step(sets[s % 2])
-    t0 = time.perf_counter()
-    for s in range(K):
-        o.compress_step(sets[(Wm + s) % 2])
-    total = time.perf_counter() - t0
+    with pinned_to_core0() as pin:
+        for s in range(1, Wm):
+            o.compress_step(sets[s % 2])
+        t0 = time.perf_counter()
+        for s in range(K):
+            o.compress_step(sets[(Wm + s) % 2])
+        total = time.perf_counter() - t0
     value = d * K / total
     ab = algorithmic_bytes(w.n_workers, W.GRAD_BYTES[w.grad_dtype])
-    sample = (f"{ws.name} law, flat d={d}, n={ws.n_workers}, {W.DTYPE_NAME[ws.grad_dtype]} grads, "
-              f"{Wm} untimed + {K} timed compression steps, single thread")
+    cpu = host_cpu()
+    sample = (f"{ws.name} law, flat d={d} (a sample of the d={w.d} workload), n={ws.n_workers}, "
+              f"{W.DTYPE_NAME[ws.grad_dtype]} grads, {Wm} untimed + {K} timed compression steps, single thread"
+              f"{' pinned to core 0' if pin.pinned else ''}")
+    config = workload_config(w, args)
+    config["d_sample"] = d  # the elements each timed oracle step processes; value = d_sample / step time
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": total / K * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(w, args),
+        "config": config,
         "step_gbs": value * ab["step"] / 1e9,
-        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "d_sample": d, "pinned_core0": pin.pinned, "host_nproc": cpu["nproc"],
+                         "host_cpu": cpu["model"]},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_exchange(args, w):
+    """The multi-GPU form: rank r of N simulates workers r*n/N .. (r+1)*n/N-1 and serves the same
+    shards; a step is compress_begin, an all-to-all of the packed messages, compress_serve, an
+    all-gather of the servers' results, compress_end.  value = d * steps / (slowest rank's time): the
+    parameters one step updates, with the n workers' work spread over the N GPUs (strong scaling)."""
+    import torch
+    import torch.distributed as dist
+
+    import communication_compressed_optimizer_compress_gb300 as ob
+    from communication_compressed_optimizer_compress_gb300 import dist as D
+    from communication_compressed_optimizer_compress_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    n = w.n_workers
+    if n % world:
+        raise SystemExit(f"--exchange needs the worker count ({n}) to be a multiple of the GPU count ({world})")
+    nl, T = n // world, w.n_tensors
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    ob.lib()
+    params = [p.to(dev) for p in W.params(w, dev)]
+    src = W.GradSource(w, dev)
+    gsets = []
+    for s_ in range(2):  # this rank's workers' gradients only
+        g = src.grads(s_)
+        gsets.append(g[rank * nl * T:(rank + 1) * nl * T])
+        del g
+    opt = D.RankOneBitAdam(params, n, w.warmup_steps, rank, world,
+                           transport=D.DeviceTransport() if world > 1 else D.LocalTransport(),
+                           beta1=w.beta1, beta2=w.beta2, eps=w.eps, lr=w.lr, grad_dtype=W.TORCH_DTYPE[w.grad_dtype])
+    stream = torch.cuda.current_stream()
+    for s_ in range(w.warmup_steps):
+        opt.warmup_step(gsets[s_ % 2])
+    opt.freeze_variance()
+    for s_ in range(max(3, args.warmup)):
+        opt.compress_step(gsets[s_ % 2])
+    torch.cuda.synchronize()
+    assert opt.get_status() == ob.OK
+    opt.set_timing(True)
+    opt.kernel_times()
+    launches0 = opt.launch_count()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t0.record(stream)
+        for s_ in range(args.steps):
+            opt.compress_step(gsets[s_ % 2])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = t0.elapsed_time(t1)
+    max_ms = dist_max(ms, dev)
+    kt = opt.kernel_times()
+    launches = opt.launch_count() - launches0
+    opt.set_timing(False)
+    status = opt.get_status()
+    gb = W.GRAD_BYTES[w.grad_dtype]
+    ab_w = algorithmic_bytes(nl, gb)["worker"]           # this rank's workers, every element
+    ab_s = algorithmic_bytes(n, gb)["server"] / world    # every worker's bits, this rank's shards
+    ab_u = algorithmic_bytes(n, gb)["update"]            # the full replica
+    ms_per_step = max_ms / args.steps
+    wk_ms = kt["worker"][0] / max(1, kt["worker"][1])
+    wk_gbs = w.d * ab_w / (wk_ms / 1e3) / 1e9 if wk_ms > 0 else None
+    peak, peak_kind = measured_peak()
+    per_kernel = {name: {"avg_ms": v[0] / max(1, v[1]), "launches": v[1]} for name, v in kt.items() if v[1]}
+    if rank == 0:
+        cfg = workload_config(w, args)
+        cfg["parallelism"] = (f"multi-GPU form: {n} workers over {world} GPU(s) ({nl} per GPU); compressed "
+                              f"all-to-all + all-gather ({'NCCL' if world > 1 else 'none at one GPU'})")
+        line = {
+            "metric": METRIC, "value": w.d * args.steps / (max_ms / 1e3), "unit": "params/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
+            "step_gbs_per_gpu": w.d * (ab_w + ab_s + ab_u) / (ms_per_step / 1e3) / 1e9,
+            "exchange_bytes_per_step_per_gpu": opt.exchange_bytes(),
+            "roofline": None if wk_gbs is None else {
+                "bound": "hbm", "kernel": "k_worker (this GPU's workers)", "achieved": wk_gbs, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": wk_gbs / peak, "traffic": None,
+                "bytes_per_elem": ab_w, "elems_per_launch": w.d},
+            "kernels": per_kernel, "gpu_launches": launches, "clocks": clk.summary(),
+            "status": ob.error_string(status), "e2e": None, "cpu_baseline": None,
+            "note": "one GPU: the split step with nothing to exchange" if world == 1 else None,
+        }
+        print(json.dumps(line), flush=True)
+    opt.free()
+    if world > 1:
+        dist.destroy_process_group()
     return 0
 
 
@@ -334,6 +483,10 @@ def main():
     ap.add_argument("--scale-block", type=int, default=0,
                     help="per-block scale granularity: every block of this many elements (a multiple of 32) "
                          "gets its own worker scales and server shards; 0 = per tensor")
+    ap.add_argument("--exchange", action="store_true",
+                    help="the multi-GPU form: the n workers split over the ranks (n/N per GPU), the compressed "
+                         "messages exchanged with an NCCL all-to-all and all-gather between the library's split "
+                         "step calls; at one GPU the split step with nothing to exchange")
     args = ap.parse_args()
     if args.graph and args.steps % 2:
         args.steps += 1
@@ -349,6 +502,8 @@ def main():
         w = w.with_(n_workers=args.n)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.exchange:
+        return run_exchange(args, w)
 
     import torch
     import torch.distributed as dist
@@ -528,19 +683,25 @@ def main():
         e2e_ms = dist_max(t0.elapsed_time(t1), dev)
         link_after = link_probe()
         link_gbs = max(link_before, link_after)
+        moved = h2d / (e2e_ms / e2e_steps / 1e3) / 1e9
         e2e = {"value": world * w.d * e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 4,
                "ms_per_step": e2e_ms / e2e_steps,
                "link_h2d_gbs": link_gbs,
                "link_h2d_gbs_before_after": [link_before, link_after],
-               "frac_of_link": h2d / (e2e_ms / e2e_steps / 1e3) / 1e9 / link_gbs,
-               "path": "onebit_adam_compress_step_host (pinned host grads) + D2H of the server scales"}
+               "frac_of_link": moved / link_gbs,
+               "frac_of_link_before_after": [moved / link_before, moved / link_after],
+               "params_on_device": True,
+               "path": "onebit_adam_compress_step_host (pinned host grads copied in by the library) + D2H of "
+                       "the server scales; the updated parameters and the optimizer state stay in HBM, as in a "
+                       "training loop, so only the scales come back"}
         del host
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.step == "compress":
         cb = oracle_sample(w)
-        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "d_sample", "pinned_core0", "host_nproc",
+                                  "host_cpu")}
 
     if rank == 0:
         line = {

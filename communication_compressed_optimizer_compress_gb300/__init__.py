@@ -20,7 +20,7 @@ PHASE_WARMUP, PHASE_COMPRESS = 0, 1
  STATE_WORKER_SCALES, STATE_SERVER_SCALES) = range(8)
 FAULT_NONE, FAULT_STALL_COPIES, FAULT_FAIL_ALLOC = 0, 1, 2
 KERNEL_NAMES = ["warmup", "freeze", "worker", "worker_scale", "server", "server_scale", "update", "export",
-                "ec_update"]
+                "ec_update", "exchange"]
 NUM_KERNELS = len(KERNEL_NAMES)
 
 
@@ -92,6 +92,7 @@ def lib() -> ctypes.CDLL:
             "onebit_adam_set_lr": [vp, ctypes.c_float],
             "onebit_adam_set_variance_monitor": [vp, i32],
             "onebit_adam_variance_norm": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)],
+            "onebit_adam_set_auto_freeze": [vp, ctypes.c_double],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -336,25 +337,24 @@ class OneBitAdam:
                self.h)
         return v.value, t.value
 
-    def warmup_until_stable(self, grads_fn, tol: float, max_steps: int | None = None, stream=None):
-        """Warm-up steps until the variance norm's relative change per step falls to `tol` or below
-        (|n_t - n_{t-1}| <= tol * n_{t-1}), or until the configured T_w; then freeze the variance.
-        grads_fn(t) returns the gradients of warm-up step t (0-based).  Returns the steps taken."""
-        self.set_variance_monitor(True)
-        t0, _ = self.get_step()
-        limit = int(self.cfg.warmup_steps) if max_steps is None else min(int(max_steps), int(self.cfg.warmup_steps))
-        prev = None
-        taken = 0
-        while t0 + taken < limit:
-            self.warmup_step(grads_fn(t0 + taken), stream)
-            taken += 1
-            cur, _ = self.variance_norm()
-            if prev is not None and abs(cur - prev) <= tol * prev:
-                break
-            prev = cur
-        self.set_variance_monitor(False)
-        self.freeze_variance(stream)
-        return taken
+    def set_auto_freeze(self, tol: float):
+        """The library's automatic freeze (0 turns it off): see onebit_adam_set_auto_freeze."""
+        _check(lib().onebit_adam_set_auto_freeze(self.h, float(tol)), "onebit_adam_set_auto_freeze", self.h)
+
+    def warmup_until_stable(self, grads_fn, tol: float, stream=None):
+        """Warm-up steps with the library's automatic freeze on until the library freezes the
+        variance (its norm's relative change per step at most `tol`, or T_w reached).  grads_fn(t)
+        returns the gradients of warm-up step t (0-based).  Returns the steps taken."""
+        t0, phase = self.get_step()
+        t = t0
+        self.set_auto_freeze(tol)
+        try:
+            while phase == PHASE_WARMUP:
+                self.warmup_step(grads_fn(t), stream)
+                t, phase = self.get_step()
+        finally:
+            self.set_auto_freeze(0.0)
+        return t - t0
 
     def set_fault_injection(self, kind: int, value: int = 0):
         _check(lib().onebit_adam_set_fault_injection(self.h, int(kind), int(value)),

@@ -55,6 +55,16 @@ struct Plan {
   int32_t max_wseg_count = 0, max_shard_count = 0;
   bool worker_spans = false;  // some worker chunk holds several shards
   bool contig = false;        // server kernels walk contiguous runs (see make_plan)
+  // Multi-GPU form (make_rank_plan): rank `rank` of `world` holds the nl = n/world workers
+  // w0 .. w0+nl-1 (w0 = rank*nl) and serves shards w0 .. w0+nl-1 of every segment.  One GPU
+  // simulating all n workers is rank 0 of 1.
+  int rank = 0, world = 1, nl = 0, w0 = 0;
+  bool ranked = false;              // created by onebit_adam_init_rank: the exchange calls are legal
+  std::vector<Chunk> schunks;       // this rank's server-side chunks (its shards), in plan order
+  std::vector<Range> sshard_ranges; // [T*n] their ranges within schunks (count 0 for other ranks' shards)
+  int64_t xsend = 0, xbcast = 0;    // words per exchange block: all-to-all, all-gather
+  std::vector<XRange> xr[4];        // exchange copies of the four stages (see make_rank_plan)
+  std::vector<int64_t> xrows[4];    // the same copies as host rows (onebit_adam_plan_exchange)
 };
 
 // Server shard j of a tensor of L elements: [j*S, min((j+1)*S, L)), S = 32*ceil(L/(32n)).
@@ -196,12 +206,116 @@ onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
   P->contig = P->T > 1 && table * (int64_t)P->chunks.size() * 20 > P->D;
   P->Wp = off / 32;
   P->Wr = (P->Wp + 3) / 4 * 4;
+  P->nl = P->n;  // one GPU simulating every worker; make_rank_plan() narrows it
+  return ONEBIT_OK;
+}
+
+// Words of segment k's sign words that hold the shards of rank q: [lo, hi) in the segment's word
+// space (shard boundaries are multiples of 32 inside a segment; the last word may hold padding bits).
+void rank_words(const Plan& P, int k, int q, int64_t* lo, int64_t* hi) {
+  int64_t a, b, c, d;
+  shard_bounds(P.numel[k], P.n, q * P.nl, &a, &b);
+  shard_bounds(P.numel[k], P.n, (q + 1) * P.nl - 1, &c, &d);
+  *lo = a / 32;
+  *hi = d > a ? (d + 31) / 32 : a / 32;
+}
+
+// The multi-GPU form's partition and exchange copies.  Regions: 0 worker sign rows (row = worker,
+// word in the padded word layout), 1 worker scales (row = worker, column = segment), 2 server sign
+// words (row 0), 3 server scales (row = segment, column = shard), 4 the caller's exchange buffer
+// (row = block, i.e. rank).  Stages:
+//   0 (begin)  pack, into block q of the all-to-all send buffer, every local worker's scales and the
+//              sign words of rank q's shards: per local worker il, T scales then the words, segment
+//              by segment (worker il's part of block q starts at il*(T + Wq), Wq = words of q's shards);
+//   1 (serve)  unpack block p of the received buffer into the rows of rank p's workers;
+//   2 (serve)  pack this rank's server scales (segment-major, nl per segment) and the server sign
+//              words of its shards into its all-gather block;
+//   3 (end)    unpack every other rank's all-gather block into the server scales and sign words.
+// A rank's own block is never copied: its data is already in place.
+onebit_status_t make_rank_plan(Plan* P, int rank, int world) {
+  P->rank = rank;
+  P->world = world;
+  P->nl = P->n / world;
+  P->w0 = rank * P->nl;
+  const int T = P->T, n = P->n, nl = P->nl;
+  // this rank's server-side chunks, with shard ranges relative to them
+  P->schunks.clear();
+  P->sshard_ranges.assign((size_t)T * n, Range{0, 0, 0});
+  for (int k = 0; k < T; ++k)
+    for (int j = 0; j < n; ++j) {
+      const Range g = P->shard_ranges[(size_t)k * n + j];
+      Range r{(int32_t)P->schunks.size(), 0, g.len};
+      if (j >= P->w0 && j < P->w0 + nl) {
+        P->schunks.insert(P->schunks.end(), P->chunks.begin() + g.first, P->chunks.begin() + g.first + g.count);
+        r.count = g.count;
+      }
+      P->sshard_ranges[(size_t)k * n + j] = r;
+    }
+  // words of each rank's shards, per segment, and their prefix sums
+  std::vector<int64_t> wlo((size_t)world * T), whi((size_t)world * T), cum((size_t)world * (T + 1), 0);
+  int64_t wmax = 0;
+  for (int q = 0; q < world; ++q) {
+    for (int k = 0; k < T; ++k) {
+      rank_words(*P, k, q, &wlo[(size_t)q * T + k], &whi[(size_t)q * T + k]);
+      cum[(size_t)q * (T + 1) + k + 1] = cum[(size_t)q * (T + 1) + k] + whi[(size_t)q * T + k] - wlo[(size_t)q * T + k];
+    }
+    wmax = std::max(wmax, cum[(size_t)q * (T + 1) + T]);
+  }
+  P->xsend = (int64_t)nl * (T + wmax);
+  P->xbcast = (int64_t)T * nl + wmax;
+  for (int st = 0; st < 4; ++st) {
+    P->xr[st].clear();
+    P->xrows[st].clear();
+  }
+  const int64_t row_stride[5] = {P->Wr, T, 0, n, 0};
+  auto add = [&](int st, int sreg, int64_t srow, int64_t soff, int dreg, int64_t drow, int64_t doff, int64_t len) {
+    if (len <= 0) return;
+    const int64_t block = st < 2 ? P->xsend : P->xbcast;
+    const int64_t s0 = (sreg == 4 ? srow * block : srow * row_stride[sreg]) + soff;
+    const int64_t d0 = (dreg == 4 ? drow * block : drow * row_stride[dreg]) + doff;
+    const int64_t r[8] = {st, sreg, srow, soff, dreg, drow, doff, len};
+    P->xrows[st].insert(P->xrows[st].end(), r, r + 8);
+    for (int64_t o = 0; o < len; o += kXPiece)
+      P->xr[st].push_back(XRange{s0 + o, d0 + o, (int32_t)std::min<int64_t>(kXPiece, len - o), (int16_t)sreg,
+                                 (int16_t)dreg});
+  };
+  auto seg_word = [&](int k) { return P->seg_off[k] / 32; };
+  const int64_t Wme = cum[(size_t)rank * (T + 1) + T];
+  for (int q = 0; q < world; ++q) {
+    if (q == rank) continue;
+    const int64_t Wq = cum[(size_t)q * (T + 1) + T];
+    for (int il = 0; il < nl; ++il) {
+      const int w = P->w0 + il;  // stage 0: this rank's worker w, for rank q's shards
+      add(0, 1, w, 0, 4, q, (int64_t)il * (T + Wq), T);
+      for (int k = 0; k < T; ++k)
+        add(0, 0, w, seg_word(k) + wlo[(size_t)q * T + k], 4, q, (int64_t)il * (T + Wq) + T + cum[(size_t)q * (T + 1) + k],
+            whi[(size_t)q * T + k] - wlo[(size_t)q * T + k]);
+      const int wp = q * nl + il;  // stage 1: rank q's worker wp, for this rank's shards
+      add(1, 4, q, (int64_t)il * (T + Wme), 1, wp, 0, T);
+      for (int k = 0; k < T; ++k)
+        add(1, 4, q, (int64_t)il * (T + Wme) + T + cum[(size_t)rank * (T + 1) + k], 0, wp,
+            seg_word(k) + wlo[(size_t)rank * T + k], whi[(size_t)rank * T + k] - wlo[(size_t)rank * T + k]);
+    }
+    // stage 3: rank q's server scales and sign words
+    for (int k = 0; k < T; ++k) add(3, 4, q, (int64_t)k * nl, 3, k, (int64_t)q * nl, nl);
+    for (int k = 0; k < T; ++k)
+      add(3, 4, q, (int64_t)T * nl + cum[(size_t)q * (T + 1) + k], 2, 0, seg_word(k) + wlo[(size_t)q * T + k],
+          whi[(size_t)q * T + k] - wlo[(size_t)q * T + k]);
+  }
+  if (world > 1) {  // stage 2: this rank's block of the all-gather
+    for (int k = 0; k < T; ++k) add(2, 3, k, P->w0, 4, 0, (int64_t)k * nl, nl);
+    for (int k = 0; k < T; ++k)
+      add(2, 2, 0, seg_word(k) + wlo[(size_t)rank * T + k], 4, 0, (int64_t)T * nl + cum[(size_t)rank * (T + 1) + k],
+          whi[(size_t)rank * T + k] - wlo[(size_t)rank * T + k]);
+  }
+  for (int st = 0; st < 4; ++st)
+    if (P->xr[st].size() > (size_t)INT32_MAX) return ONEBIT_ERR_UNSUPPORTED;
   return ONEBIT_OK;
 }
 
 struct Layout {
   size_t m, v, a, c, wbits, sbits, wscale, sscale, wpart, spart, chunks, seg_ranges, shard_ranges, wchunks,
-      wseg_ranges, gptr, pptr, status, total;
+      wseg_ranges, schunks, sshard_ranges, xr[4], gptr, pptr, status, total;
 };
 
 Layout make_layout(const Plan& P) {
@@ -212,22 +326,26 @@ Layout make_layout(const Plan& P) {
     o = align_up(o + std::max<size_t>(bytes, 1), kAlign);
     return at;
   };
-  const size_t n = P.n, T = P.T, C = P.chunks.size();
+  const size_t n = P.n, nl = P.nl, T = P.T, C = P.chunks.size();
   L.m = take(P.Dp * 4);
   L.v = take(P.Dp * 4);
   L.a = take(P.Dp * 4);
-  L.c = take(n * P.Dp * 4);
+  L.c = take(nl * P.Dp * 4);  // only this rank's workers keep c
   L.wbits = take(n * P.Wr * 4);
   L.sbits = take(P.Wp * 4);
   L.wscale = take(2 * n * T * 4);
   L.sscale = take(2 * n * T * 4);
-  L.wpart = take(n * P.wchunks.size() * 8);
+  L.wpart = take(nl * P.wchunks.size() * 8);
   L.spart = take(C * 8);
+  // host-built tables, uploaded together (chunks .. xr[3])
   L.chunks = take(C * sizeof(Chunk));
   L.seg_ranges = take(T * sizeof(Range));
   L.shard_ranges = take(T * n * sizeof(Range));
   L.wchunks = take(P.wchunks.size() * sizeof(Chunk));
   L.wseg_ranges = take(T * sizeof(Range));
+  L.schunks = take(P.schunks.size() * sizeof(Chunk));
+  L.sshard_ranges = take(P.sshard_ranges.size() * sizeof(Range));
+  for (int st = 0; st < 4; ++st) L.xr[st] = take(P.xr[st].size() * sizeof(XRange));
   L.gptr = take(kPtrRing * n * T * sizeof(void*));
   L.pptr = take(T * sizeof(void*));
   L.status = take(256);
@@ -287,7 +405,12 @@ struct onebit_adam {
   double* vnorm_host = nullptr;  // pinned
   cudaEvent_t ev_vnorm = nullptr;
   int64_t vnorm_step = 0;
+  // automatic freeze: tolerance on the norm's relative change per step (0: off), last norm seen
+  double auto_tol = 0.0;
+  bool auto_have_prev = false;
+  double auto_prev = 0.0;
   std::string last_error;
+  int xstage = 0;  // multi-GPU form: 0 idle, 1 after compress_begin, 2 after compress_serve
 
   template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
 };
@@ -324,6 +447,25 @@ bool refuse_alloc(onebit_adam* h) {
 onebit_status_t cuda_fail(onebit_adam* h, cudaError_t e, const char* where) {
   if (h) h->last_error = std::string(where) + ": " + cudaGetErrorString(e);
   return ONEBIT_ERR_CUDA;
+}
+
+// The pinned host slot (and its event) that receives the variance norm of monitored warm-up steps.
+onebit_status_t ensure_vnorm_slot(onebit_adam* h) {
+  if (h->vnorm_host) return ONEBIT_OK;
+  if (refuse_alloc(h) ||
+      cudaHostAlloc(reinterpret_cast<void**>(&h->vnorm_host), sizeof(double), cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    h->vnorm_host = nullptr;
+    return ONEBIT_ERR_NOMEM;
+  }
+  *h->vnorm_host = 0.0;
+  if (cudaEventCreateWithFlags(&h->ev_vnorm, cudaEventDisableTiming) != cudaSuccess) {
+    const cudaError_t e = cudaGetLastError();
+    cudaFreeHost(h->vnorm_host);
+    h->vnorm_host = nullptr;
+    return cuda_fail(h, e, "cudaEventCreateWithFlags");
+  }
+  return ONEBIT_OK;
 }
 
 // The CUDA message of the last onebit_adam_init that failed on this thread: its handle is gone, so
@@ -432,23 +574,33 @@ StepArgs base_args(onebit_adam* h) {
   A.bc1 = 1.0f;
   A.bc2 = 1.0f;
   A.stall_tx = h->stall_tx;
+  A.nl = P.nl;
+  A.w0 = P.w0;
   return A;
+}
+
+// The server kernels of the multi-GPU form run over this rank's shards only.
+void narrow_to_own_shards(const onebit_adam* h, StepArgs* A) {
+  if (!h->plan.ranked) return;
+  A->chunks = h->at<Chunk>(h->lay.schunks);
+  A->n_chunks = (int32_t)h->plan.schunks.size();
+  A->shard_ranges = h->at<Range>(h->lay.sshard_ranges);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Upload (or reuse) the [n*T] gradient pointer table; reports whether every gradient pointer allows
 // the vector loads of the kernels.
-onebit_status_t bind_grads(onebit_adam* h, const void* const* grads, cudaStream_t stream, const void* const** dev,
-                           bool* vec) {
+onebit_status_t bind_grads(onebit_adam* h, const void* const* grads, int nw, cudaStream_t stream,
+                           const void* const** dev, bool* vec) {
   const Plan& P = h->plan;
-  const size_t cnt = (size_t)P.n * P.T;
+  const size_t cnt = (size_t)nw * P.T;  // nw: the workers whose gradients are passed (n, or a rank's nl)
   const size_t gb = h->cfg.grad_dtype == ONEBIT_F32 ? 4 : 2;
-  for (size_t q = 0; q < (size_t)P.n * P.Tu; ++q)
+  for (size_t q = 0; q < (size_t)nw * P.Tu; ++q)
     if (!grads[q] && P.unumel[q % P.Tu] > 0) return ONEBIT_ERR_INVALID_ARG;
   if (P.split) {  // one pointer per segment: its caller tensor's pointer advanced to the block
     h->gexp.resize(cnt);
-    for (int i = 0; i < P.n; ++i)
+    for (int i = 0; i < nw; ++i)
       for (int k = 0; k < P.Tu; ++k) {
         const uint8_t* g = static_cast<const uint8_t*>(grads[(size_t)i * P.Tu + k]);
         for (int v = P.ufirst[k]; v < P.ufirst[k + 1]; ++v)
@@ -509,14 +661,17 @@ onebit_status_t run_warmup_m(onebit_adam* h, const StepArgs& A, bool vec, cudaSt
   return vec ? pick(k_warmup<GT, false, true, MON, false>) : pick(k_warmup<GT, false, false, MON, false>);
 }
 
+// warm-up steps compute the variance norm for the monitor and for the automatic freeze
+bool monitored(const onebit_adam* h) { return h->vmon || h->auto_tol > 0.0; }
+
 template <typename GT>
 onebit_status_t run_warmup(onebit_adam* h, StepArgs A, bool vec, cudaStream_t st) {
-  return h->vmon ? run_warmup_m<GT, true>(h, A, vec, st) : run_warmup_m<GT, false>(h, A, vec, st);
+  return monitored(h) ? run_warmup_m<GT, true>(h, A, vec, st) : run_warmup_m<GT, false>(h, A, vec, st);
 }
 
 template <typename GT, int DM, bool HE>
 onebit_status_t run_worker_v(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
-  const int64_t units = (int64_t)A.n_wchunks * A.n;
+  const int64_t units = (int64_t)A.n_wchunks * A.nl;
   if (vec) {
     auto k = k_worker<GT, DM, HE, true>;
     return launch(h, ONEBIT_K_WORKER, k, grid_for(h, (const void*)k, kThreads, units), kThreads, st, A);
@@ -564,12 +719,46 @@ onebit_status_t run_server(onebit_adam* h, const StepArgs& A, cudaStream_t st) {
   return h->serr_zero ? run_server_v<false>(h, A, st) : run_server_v<true>(h, A, st);
 }
 
+// den = sqrt(v) + eps in place (v / (1 - b2^t) first with bias correction); the compression stage
+// starts from zero errors and the dense warm-up momentum.
+onebit_status_t do_freeze(onebit_adam* h, cudaStream_t st) {
+  const int64_t groups = h->plan.Dp / 8;
+  const float bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)h->t));
+  float* v = h->at<float>(h->lay.v);
+  auto go = [&](auto kern) -> onebit_status_t {
+    TimedLaunch tl{ONEBIT_K_FREEZE, nullptr, nullptr};
+    if (h->timing) {
+      tl.start = take_event(h);
+      tl.stop = take_event(h);
+      if (tl.start) cudaEventRecord(tl.start, st);
+    }
+    const int grid = grid_for(h, (const void*)kern, kThreads, (groups + kThreads - 1) / kThreads);
+    kern<<<grid, kThreads, 0, st>>>(v, groups, bc2, h->cfg.eps);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(h, e, "freeze launch");
+    ++h->launches;
+    if (h->timing && tl.start && tl.stop) {
+      cudaEventRecord(tl.stop, st);
+      h->timed.push_back(tl);
+    }
+    return ONEBIT_OK;
+  };
+  const onebit_status_t s = h->cfg.bias_correction ? go(k_freeze<true>) : go(k_freeze<false>);
+  if (s) return s;
+  h->phase = ONEBIT_PHASE_COMPRESS;
+  h->m_dense = true;
+  h->werr_zero = true;
+  h->serr_zero = true;
+  h->auto_have_prev = false;
+  return ONEBIT_OK;
+}
+
 onebit_status_t do_warmup(onebit_adam* h, const void* const* grads, cudaStream_t st) {
   if (h->phase != ONEBIT_PHASE_WARMUP) return ONEBIT_ERR_PHASE;
   if (h->t >= h->cfg.warmup_steps) return ONEBIT_ERR_PHASE;
   StepArgs A = base_args(h);
   bool vec = false;
-  onebit_status_t s = bind_grads(h, grads, st, &A.gptr, &vec);
+  onebit_status_t s = bind_grads(h, grads, h->plan.n, st, &A.gptr, &vec);  // every worker's gradient
   if (s) return s;
   const int64_t t = h->t + 1;
   A.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, (double)t));
@@ -582,7 +771,7 @@ onebit_status_t do_warmup(onebit_adam* h, const void* const* grads, cudaStream_t
   }
   if (s) return s;
   h->t = t;
-  if (h->vmon) {  // ||v_t|| from the chunk partials, then to the pinned host slot
+  if (monitored(h)) {  // ||v_t|| from the chunk partials, then to the pinned host slot
     double* slot = reinterpret_cast<double*>(h->ws + h->lay.status + 64);
     k_variance_norm<<<1, kScaleThreads, 0, st>>>(h->at<double>(h->lay.spart), A.n_chunks, slot);
     cudaError_t e = cudaGetLastError();
@@ -592,16 +781,25 @@ onebit_status_t do_warmup(onebit_adam* h, const void* const* grads, cudaStream_t
     ONEBIT_CUDA(h, cudaEventRecord(h->ev_vnorm, st));
     h->vnorm_step = t;
   }
+  if (h->auto_tol > 0.0) {
+    // the automatic freeze: the variance norm's relative change per step against the tolerance
+    ONEBIT_CUDA(h, cudaEventSynchronize(h->ev_vnorm));
+    const double cur = *h->vnorm_host;
+    const bool stable = h->auto_have_prev && std::fabs(cur - h->auto_prev) <= h->auto_tol * h->auto_prev;
+    h->auto_prev = cur;
+    h->auto_have_prev = true;
+    if (stable || t >= h->cfg.warmup_steps) return do_freeze(h, st);
+  }
   return ONEBIT_OK;
 }
 
 // One compression-stage step, or (ec_adam) one step of the gradient-compression baseline: the
 // same worker/server compression of g_i + delta_i, then Adam on the broadcast.
-onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream_t st, bool ec_adam = false) {
-  if (h->phase != (ec_adam ? ONEBIT_PHASE_WARMUP : ONEBIT_PHASE_COMPRESS)) return ONEBIT_ERR_PHASE;
+// The worker half of a step: K1 for the handle's workers (all n, or a rank's nl) and their scales.
+onebit_status_t run_worker_half(onebit_adam* h, const void* const* grads, cudaStream_t st, bool ec_adam) {
   StepArgs A = base_args(h);
   bool vec = false;
-  onebit_status_t s = bind_grads(h, grads, st, &A.gptr, &vec);
+  onebit_status_t s = bind_grads(h, grads, h->plan.nl, st, &A.gptr, &vec);
   if (s) return s;
   switch (h->cfg.grad_dtype) {
     case ONEBIT_F32: s = run_worker<float>(h, A, vec, st, ec_adam); break;
@@ -609,20 +807,48 @@ onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream
     default: s = run_worker<__nv_bfloat16>(h, A, vec, st, ec_adam); break;
   }
   if (s) return s;
-  const int nt = h->plan.n * h->plan.T;
+  // partials outside the exact range of the fast squares are summed again in double (a scan otherwise)
+  const int64_t parts = (int64_t)h->plan.nl * h->plan.wchunks.size();
+  s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_exact,
+             grid_for(h, (const void*)k_worker_exact, kThreads, (parts + kThreads - 1) / kThreads), kThreads, st, A);
+  if (s) return s;
+  const int nt = h->plan.nl * h->plan.T;
   // many short ranges: one warp per scale; otherwise one CTA per scale
   constexpr int kPerCta = kScaleThreads / 32;
   if (h->plan.max_wseg_count <= kWarpScaleMax)
-    s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale_warp, (nt + kPerCta - 1) / kPerCta, kScaleThreads, st, A);
-  else
-    s = launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale, nt, kScaleThreads, st, A);
+    return launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale_warp, (nt + kPerCta - 1) / kPerCta, kScaleThreads, st, A);
+  return launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale, nt, kScaleThreads, st, A);
+}
+
+// The server half: K2 over the handle's shards (all, or a rank's own) and the shard scales.
+onebit_status_t run_server_half(onebit_adam* h, cudaStream_t st) {
+  StepArgs A = base_args(h);
+  narrow_to_own_shards(h, &A);
+  onebit_status_t s = run_server(h, A, st);
   if (s) return s;
-  if ((s = run_server(h, A, st))) return s;
+  const int nt = h->plan.n * h->plan.T;
+  constexpr int kPerCta = kScaleThreads / 32;
   if (h->plan.max_shard_count <= kWarpScaleMax)
-    s = launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale_warp, (nt + kPerCta - 1) / kPerCta, kScaleThreads, st, A);
-  else
-    s = launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale, nt, kScaleThreads, st, A);
+    return launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale_warp, (nt + kPerCta - 1) / kPerCta, kScaleThreads, st, A);
+  return launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale, nt, kScaleThreads, st, A);
+}
+
+// The step's bookkeeping once its last kernel is enqueued.
+void finish_step(onebit_adam* h, bool ec_adam) {
+  h->compress_steps += 1;
+  h->t += 1;
+  if (!ec_adam) h->m_dense = false;  // the baseline keeps Adam's own fp32 momentum
+  h->werr_zero = false;
+  h->serr_zero = false;
+}
+
+onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream_t st, bool ec_adam = false) {
+  if (h->phase != (ec_adam ? ONEBIT_PHASE_WARMUP : ONEBIT_PHASE_COMPRESS) || h->xstage) return ONEBIT_ERR_PHASE;
+  if (h->plan.world > 1) return ONEBIT_ERR_UNSUPPORTED;  // a rank's step needs the exchange (begin/serve/end)
+  onebit_status_t s = run_worker_half(h, grads, st, ec_adam);
   if (s) return s;
+  if ((s = run_server_half(h, st))) return s;
+  StepArgs A = base_args(h);
   if (ec_adam) {
     const int64_t t = h->t + 1;
     A.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, (double)t));
@@ -641,20 +867,82 @@ onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream
     s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
   }
   if (s) return s;
-  h->compress_steps += 1;
-  h->t += 1;
-  if (!ec_adam) h->m_dense = false;  // the baseline keeps Adam's own fp32 momentum
-  h->werr_zero = false;
-  h->serr_zero = false;
+  finish_step(h, ec_adam);
+  return ONEBIT_OK;
+}
+
+// ---- the multi-GPU form: the compression step split at the exchange
+
+onebit_status_t run_exchange_copy(onebit_adam* h, int stage, const void* buf, cudaStream_t st) {
+  const size_t cnt = h->plan.xr[stage].size();
+  if (!cnt) return ONEBIT_OK;
+  XArgs X{};
+  X.r = h->at<XRange>(h->lay.xr[stage]);
+  X.n = (int32_t)cnt;
+  const size_t nt = (size_t)h->plan.n * h->plan.T;
+  const int cur = (int)(h->compress_steps & 1);
+  X.base[0] = h->at<uint32_t>(h->lay.wbits);
+  X.base[1] = reinterpret_cast<uint32_t*>(h->at<float>(h->lay.wscale) + cur * nt);
+  X.base[2] = h->at<uint32_t>(h->lay.sbits);
+  X.base[3] = reinterpret_cast<uint32_t*>(h->at<float>(h->lay.sscale) + cur * nt);
+  X.base[4] = const_cast<uint32_t*>(static_cast<const uint32_t*>(buf));
+  return launch(h, ONEBIT_K_EXCHANGE, k_exchange_copy, grid_for(h, (const void*)k_exchange_copy, kThreads, X.n),
+                kThreads, st, X);
+}
+
+onebit_status_t do_begin(onebit_adam* h, const void* const* grads, void* send, cudaStream_t st) {
+  if (!h->plan.ranked) return ONEBIT_ERR_UNSUPPORTED;
+  if (h->phase != ONEBIT_PHASE_COMPRESS || h->xstage != 0) return ONEBIT_ERR_PHASE;
+  if (h->plan.world > 1 && !send) return ONEBIT_ERR_INVALID_ARG;
+  onebit_status_t s = run_worker_half(h, grads, st, false);
+  if (s) return s;
+  if ((s = run_exchange_copy(h, 0, send, st))) return s;
+  h->xstage = 1;
+  return ONEBIT_OK;
+}
+
+onebit_status_t do_serve(onebit_adam* h, const void* recv, void* bcast, cudaStream_t st) {
+  if (!h->plan.ranked) return ONEBIT_ERR_UNSUPPORTED;
+  if (h->xstage != 1) return ONEBIT_ERR_PHASE;
+  if (h->plan.world > 1 && (!recv || !bcast)) return ONEBIT_ERR_INVALID_ARG;
+  onebit_status_t s = run_exchange_copy(h, 1, recv, st);
+  if (s) return s;
+  if ((s = run_server_half(h, st))) return s;
+  if ((s = run_exchange_copy(h, 2, bcast, st))) return s;
+  h->xstage = 2;
+  return ONEBIT_OK;
+}
+
+onebit_status_t do_end(onebit_adam* h, const void* gathered, cudaStream_t st) {
+  if (!h->plan.ranked) return ONEBIT_ERR_UNSUPPORTED;
+  if (h->xstage != 2) return ONEBIT_ERR_PHASE;
+  if (h->plan.world > 1 && !gathered) return ONEBIT_ERR_INVALID_ARG;
+  onebit_status_t s = run_exchange_copy(h, 3, gathered, st);
+  if (s) return s;
+  StepArgs A = base_args(h);
+  if (h->params_aligned) {
+    auto k = k_update<true>;
+    s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+  } else {
+    auto k = k_update<false>;
+    s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+  }
+  if (s) return s;
+  finish_step(h, false);
+  h->xstage = 0;
   return ONEBIT_OK;
 }
 
 // Export kinds on the padded state, written into the caller's unpadded buffer.
 onebit_status_t run_export(onebit_adam* h, int kind, const float* src, const uint32_t* bits, const float* scales,
-                           int seg_mul, int shard_mul, float* dst, cudaStream_t st) {
+                           int seg_mul, int shard_mul, float* dst, cudaStream_t st, bool own_shards = false) {
   ExportArgs X{};
   X.chunks = h->at<Chunk>(h->lay.chunks);
   X.n_chunks = (int32_t)h->plan.chunks.size();
+  if (own_shards && h->plan.ranked) {  // a rank's server state covers its own shards only
+    X.chunks = h->at<Chunk>(h->lay.schunks);
+    X.n_chunks = (int32_t)h->plan.schunks.size();
+  }
   X.kind = kind;
   X.scale_seg_mul = seg_mul;
   X.scale_shard_mul = shard_mul;
@@ -758,6 +1046,21 @@ onebit_status_t guarded(F&& body) noexcept {
   }
 }
 
+// The plan of a handle: one GPU simulating every worker (rank 0 of 1, ranked = false), or rank `rank`
+// of `world` in the multi-GPU form (n a multiple of world; ranked = true, also for world = 1).
+onebit_status_t plan_for(const onebit_adam_config_t* cfg, int rank, int world, bool ranked, Plan* P) {
+  onebit_status_t s = check_config(cfg);
+  if (s) return s;
+  if (world < 1 || rank < 0 || rank >= world || cfg->n_workers % world != 0) return ONEBIT_ERR_INVALID_ARG;
+  if ((s = make_plan(cfg, P))) return s;
+  P->ranked = ranked;
+  if (ranked) return make_rank_plan(P, rank, world);
+  return ONEBIT_OK;
+}
+
+onebit_status_t init_handle(const onebit_adam_config_t* cfg, int rank, int world, bool ranked, float* const* params,
+                            void* workspace, size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out);
+
 }  // namespace
 
 // =================================================================================== C ABI
@@ -781,13 +1084,35 @@ const char* onebit_adam_error_string(onebit_status_t s) {
 const char* onebit_adam_last_error(const onebit_adam_t* h) { return h ? h->last_error.c_str() : t_init_error.c_str(); }
 
 onebit_status_t onebit_adam_workspace_size(const onebit_adam_config_t* cfg, size_t* bytes) {
+  return onebit_adam_workspace_size_rank(cfg, 0, 1, bytes);
+}
+
+onebit_status_t onebit_adam_workspace_size_rank(const onebit_adam_config_t* cfg, int32_t rank, int32_t world,
+                                                size_t* bytes) {
   return guarded([&]() -> onebit_status_t {
     if (!bytes) return ONEBIT_ERR_INVALID_ARG;
-    onebit_status_t s = check_config(cfg);
-    if (s) return s;
     Plan P;
-    if ((s = make_plan(cfg, &P))) return s;
+    onebit_status_t s = plan_for(cfg, rank, world, world > 1, &P);
+    if (s) return s;
     *bytes = make_layout(P).total;
+    return ONEBIT_OK;
+  });
+}
+
+onebit_status_t onebit_adam_plan_exchange(const onebit_adam_config_t* cfg, int32_t rank, int32_t world, int64_t* rows,
+                                          int64_t cap, int64_t* count, int64_t* send_block, int64_t* bcast_block) {
+  return guarded([&]() -> onebit_status_t {
+    if (!count || !send_block || !bcast_block || (cap > 0 && !rows)) return ONEBIT_ERR_INVALID_ARG;
+    Plan P;
+    onebit_status_t s = plan_for(cfg, rank, world, true, &P);
+    if (s) return s;
+    int64_t q = 0;
+    for (int st = 0; st < 4; ++st)
+      for (size_t r = 0; r < P.xrows[st].size(); r += 8, ++q)
+        if (q < cap) std::copy(P.xrows[st].begin() + r, P.xrows[st].begin() + r + 8, rows + q * 8);
+    *count = q;
+    *send_block = P.xsend;
+    *bcast_block = P.xbcast;
     return ONEBIT_OK;
   });
 }
@@ -836,6 +1161,57 @@ onebit_status_t onebit_adam_plan_worker_chunks(const onebit_adam_config_t* cfg, 
 
 onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* params, void* workspace,
                                  size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out) {
+  return init_handle(cfg, 0, 1, false, params, workspace, workspace_bytes, stream, out);
+}
+
+onebit_status_t onebit_adam_init_rank(const onebit_adam_config_t* cfg, int32_t rank, int32_t world,
+                                      float* const* params, void* workspace, size_t workspace_bytes,
+                                      onebit_stream_t stream, onebit_adam_t** out) {
+  return init_handle(cfg, rank, world, true, params, workspace, workspace_bytes, stream, out);
+}
+
+onebit_status_t onebit_adam_exchange_words(const onebit_adam_t* h, int64_t* send_block, int64_t* bcast_block) {
+  if (!h || !send_block || !bcast_block) return ONEBIT_ERR_INVALID_ARG;
+  *send_block = h->plan.xsend;
+  *bcast_block = h->plan.xbcast;
+  return ONEBIT_OK;
+}
+
+onebit_status_t onebit_adam_compress_begin(onebit_adam_t* h, const void* const* grads, uint32_t* send,
+                                           onebit_stream_t stream) {
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_compress_begin");
+    if (!h || !grads) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    return do_begin(h, grads, send, as_stream(stream));
+  });
+}
+
+onebit_status_t onebit_adam_compress_serve(onebit_adam_t* h, const uint32_t* recv, uint32_t* bcast,
+                                           onebit_stream_t stream) {
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_compress_serve");
+    if (!h) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    return do_serve(h, recv, bcast, as_stream(stream));
+  });
+}
+
+onebit_status_t onebit_adam_compress_end(onebit_adam_t* h, const uint32_t* gathered, onebit_stream_t stream) {
+  return guarded([&]() -> onebit_status_t {
+    NvtxRange trace("onebit_adam_compress_end");
+    if (!h) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    return do_end(h, gathered, as_stream(stream));
+  });
+}
+
+}  // extern "C"
+
+namespace {
+
+onebit_status_t init_handle(const onebit_adam_config_t* cfg, int rank, int world, bool ranked, float* const* params,
+                            void* workspace, size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out) {
   return guarded([&]() -> onebit_status_t {
     NvtxRange trace("onebit_adam_init");
     if (!out || !params) return ONEBIT_ERR_INVALID_ARG;
@@ -847,7 +1223,7 @@ onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* 
     if (workspace && !aligned(workspace, kAlign)) return ONEBIT_ERR_WORKSPACE;
 
     Plan plan;  // built before the handle, so that a failure here leaves nothing to release
-    if ((s = make_plan(cfg, &plan))) return s;
+    if ((s = plan_for(cfg, rank, world, ranked, &plan))) return s;
     onebit_adam* h = new (std::nothrow) onebit_adam();
     if (!h) return ONEBIT_ERR_NOMEM;
     // from here on every exit but success releases the handle (an exception included)
@@ -900,6 +1276,11 @@ onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* 
                 (size_t)P.T * P.n * sizeof(Range));
     std::memcpy(tables.data() + (h->lay.wchunks - h->lay.chunks), P.wchunks.data(), P.wchunks.size() * sizeof(Chunk));
     std::memcpy(tables.data() + (h->lay.wseg_ranges - h->lay.chunks), P.wseg_ranges.data(), P.T * sizeof(Range));
+    std::memcpy(tables.data() + (h->lay.schunks - h->lay.chunks), P.schunks.data(), P.schunks.size() * sizeof(Chunk));
+    std::memcpy(tables.data() + (h->lay.sshard_ranges - h->lay.chunks), P.sshard_ranges.data(),
+                P.sshard_ranges.size() * sizeof(Range));
+    for (int st = 0; st < 4; ++st)
+      std::memcpy(tables.data() + (h->lay.xr[st] - h->lay.chunks), P.xr[st].data(), P.xr[st].size() * sizeof(XRange));
     if (cudaMemcpyAsync(h->ws + h->lay.chunks, tables.data(), tables.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
       return cuda_fail(h, cudaGetLastError(), "upload tables");
     if (cudaMemcpyAsync(h->ws + h->lay.pptr, h->params.data(), P.T * sizeof(float*), cudaMemcpyHostToDevice, st) !=
@@ -913,6 +1294,10 @@ onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* 
     return ONEBIT_OK;
   });
 }
+
+}  // namespace
+
+extern "C" {
 
 onebit_status_t onebit_adam_free(onebit_adam_t* h) {
   return guarded([&]() -> onebit_status_t {
@@ -1005,36 +1390,7 @@ onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t st
     if (!h) return ONEBIT_ERR_INVALID_ARG;
     if (h->phase != ONEBIT_PHASE_WARMUP || h->t < 1) return ONEBIT_ERR_PHASE;
     DeviceGuard g(h->device);
-    cudaStream_t st = as_stream(stream);
-    const int64_t groups = h->plan.Dp / 8;
-    const float bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)h->t));
-    float* v = h->at<float>(h->lay.v);
-    onebit_status_t s;
-    auto go = [&](auto kern) -> onebit_status_t {
-      TimedLaunch tl{ONEBIT_K_FREEZE, nullptr, nullptr};
-      if (h->timing) {
-        tl.start = take_event(h);
-        tl.stop = take_event(h);
-        if (tl.start) cudaEventRecord(tl.start, st);
-      }
-      const int grid = grid_for(h, (const void*)kern, kThreads, (groups + kThreads - 1) / kThreads);
-      kern<<<grid, kThreads, 0, st>>>(v, groups, bc2, h->cfg.eps);
-      cudaError_t e = cudaGetLastError();
-      if (e != cudaSuccess) return cuda_fail(h, e, "freeze launch");
-      ++h->launches;
-      if (h->timing && tl.start && tl.stop) {
-        cudaEventRecord(tl.stop, st);
-        h->timed.push_back(tl);
-      }
-      return ONEBIT_OK;
-    };
-    s = h->cfg.bias_correction ? go(k_freeze<true>) : go(k_freeze<false>);
-    if (s) return s;
-    h->phase = ONEBIT_PHASE_COMPRESS;
-    h->m_dense = true;
-    h->werr_zero = true;
-    h->serr_zero = true;
-    return ONEBIT_OK;
+    return do_freeze(h, as_stream(stream));
   });
 }
 
@@ -1086,6 +1442,7 @@ onebit_status_t onebit_adam_set_step(onebit_adam_t* h, int64_t t, int32_t phase,
     (void)stream;
     h->t = t;
     h->phase = phase;
+    h->xstage = 0;  // a resumed handle starts outside any exchange
     return ONEBIT_OK;
   });
 }
@@ -1113,6 +1470,8 @@ onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worke
     const Plan& P = h->plan;
     const bool per_worker = what == ONEBIT_STATE_WORKER_ERROR || what == ONEBIT_STATE_WORKER_BITS;
     if (per_worker && (worker < 0 || worker >= P.n)) return ONEBIT_ERR_INVALID_ARG;
+    // a rank keeps the errors of its own workers only
+    if (what == ONEBIT_STATE_WORKER_ERROR && (worker < P.w0 || worker >= P.w0 + P.nl)) return ONEBIT_ERR_INVALID_ARG;
     DeviceGuard g(h->device);
     cudaStream_t st = as_stream(stream);
     float* out = static_cast<float*>(dst);
@@ -1122,12 +1481,18 @@ onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worke
       case ONEBIT_STATE_WORKER_ERROR:
         if (h->werr_zero)
           return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
-        return run_export(h, kExportSignedErr, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, nullptr,
+        return run_export(h, kExportSignedErr, h->at<float>(h->lay.c) + (size_t)(worker - P.w0) * P.Dp, nullptr,
                           last_wscale(h) + (size_t)worker * P.T, 1, 0, out, st);
-      case ONEBIT_STATE_SERVER_ERROR:
+      case ONEBIT_STATE_SERVER_ERROR: {
         if (h->serr_zero)
           return run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
-        return run_export(h, kExportSignedErr, h->at<float>(h->lay.a), nullptr, last_sscale(h), P.n, 1, out, st);
+        if (P.world > 1) {  // other ranks' shards read 0
+          const onebit_status_t s = run_export(h, kExportZero, nullptr, nullptr, nullptr, 0, 0, out, st);
+          if (s) return s;
+        }
+        return run_export(h, kExportSignedErr, h->at<float>(h->lay.a), nullptr, last_sscale(h), P.n, 1, out, st,
+                          true);
+      }
       case ONEBIT_STATE_WORKER_BITS:
         ONEBIT_CUDA(h, cudaMemcpyAsync(dst, h->at<uint32_t>(h->lay.wbits) + (size_t)worker * P.Wr, P.Wp * 4,
                                        cudaMemcpyDeviceToDevice, st));
@@ -1164,15 +1529,16 @@ onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worke
       case ONEBIT_STATE_V:
         return run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.v), st);
       case ONEBIT_STATE_WORKER_ERROR: {
-        if (worker < 0 || worker >= P.n) return ONEBIT_ERR_INVALID_ARG;
+        if (worker < P.w0 || worker >= P.w0 + P.nl) return ONEBIT_ERR_INVALID_ARG;  // this rank's workers only
         float* ws_prev = last_wscale(h);  // what the next step reads as the previous scales
         if (h->werr_zero) {
-          ONEBIT_CUDA(h, cudaMemsetAsync(h->at<float>(h->lay.c), 0, (size_t)P.n * P.Dp * 4, st));
+          ONEBIT_CUDA(h, cudaMemsetAsync(h->at<float>(h->lay.c), 0, (size_t)P.nl * P.Dp * 4, st));
           ONEBIT_CUDA(h, cudaMemsetAsync(ws_prev, 0, nt * 4, st));
           h->werr_zero = false;
         }
         // store delta as c with a zero scale: the next step rebuilds c - 0*sign(c) = delta exactly
-        if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.c) + (size_t)worker * P.Dp, st)))
+        if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0,
+                            h->at<float>(h->lay.c) + (size_t)(worker - P.w0) * P.Dp, st)))
           return s;
         ONEBIT_CUDA(h, cudaMemsetAsync(ws_prev + (size_t)worker * P.T, 0, (size_t)P.T * 4, st));
         return ONEBIT_OK;
@@ -1182,8 +1548,9 @@ onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worke
           if ((s = export_m(h, h->at<float>(h->lay.m), st))) return s;
           h->m_dense = true;
         }
-        // store eps as a with a zero scale: the next step rebuilds a - 0*sign(a) = eps exactly
-        if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.a), st))) return s;
+        // store eps as a with a zero scale: the next step rebuilds a - 0*sign(a) = eps exactly (a rank
+        // keeps the errors of its own shards only)
+        if ((s = run_export(h, kImportCopy, in, nullptr, nullptr, 0, 0, h->at<float>(h->lay.a), st, true))) return s;
         ONEBIT_CUDA(h, cudaMemsetAsync(last_sscale(h), 0, nt * 4, st));
         h->serr_zero = false;
         return ONEBIT_OK;
@@ -1240,17 +1607,25 @@ onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enabl
   return guarded([&]() -> onebit_status_t {
     if (!h) return ONEBIT_ERR_INVALID_ARG;
     DeviceGuard g(h->device);
-    if (enable && !h->vnorm_host) {
-      if (refuse_alloc(h) ||
-          cudaHostAlloc(reinterpret_cast<void**>(&h->vnorm_host), sizeof(double), cudaHostAllocDefault) != cudaSuccess) {
-        cudaGetLastError();
-        h->vnorm_host = nullptr;
-        return ONEBIT_ERR_NOMEM;
-      }
-      *h->vnorm_host = 0.0;
-      ONEBIT_CUDA(h, cudaEventCreateWithFlags(&h->ev_vnorm, cudaEventDisableTiming));
+    if (enable) {
+      const onebit_status_t s = ensure_vnorm_slot(h);
+      if (s) return s;
     }
     h->vmon = enable != 0;
+    return ONEBIT_OK;
+  });
+}
+
+onebit_status_t onebit_adam_set_auto_freeze(onebit_adam_t* h, double tol) {
+  return guarded([&]() -> onebit_status_t {
+    if (!h || !std::isfinite(tol) || tol < 0.0) return ONEBIT_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (tol > 0.0) {
+      const onebit_status_t s = ensure_vnorm_slot(h);
+      if (s) return s;
+    }
+    h->auto_tol = tol;
+    h->auto_have_prev = false;
     return ONEBIT_OK;
   });
 }

@@ -97,6 +97,8 @@ struct StepArgs {
   int32_t n_wchunks;
   int32_t contig;            // the register server kernel walks contiguous runs (many short tensors)
   int64_t D;                 // elements (unpadded)
+  int32_t nl;                // workers whose momentum this launch compresses (all n, or one rank's share)
+  int32_t w0;                // the first of them: global workers w0 .. w0+nl-1 (c, wpart and gptr rows 0..nl-1)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -181,23 +183,28 @@ __device__ __forceinline__ double block_sum(double v, double* red) {
   return r;  // valid in thread 0
 }
 
+// The same fixed-order reduction, its result returned to every thread (red: NT/32 + 1 slots).
+template <int NT>
+__device__ __forceinline__ double block_sum_all(double v, double* red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    double r = lane < NT / 32 ? red[lane] : 0.0;
+    r = warp_sum(r);
+    if (lane == 0) red[NT / 32] = r;
+  }
+  __syncthreads();
+  return red[NT / 32];
+}
+
 // Sum of squares without rounding error at the element level: c*c = p + pe exactly (FMA), p is
 // added to the running fp32 sum with an exact two-sum, and the two error terms are collected in a
 // second fp32 word.  (hi, lo) carries ~44 bits; it is promoted to double once per work unit.  This
 // keeps the scales equal to a double-precision evaluation (1 ulp at most, almost always 0) without
-// using the GPU's slow fp64 pipe per element.
-__device__ __forceinline__ void add_square(float& hi, float& lo, float c) {
-  const float p = __fmul_rn(c, c);
-  const float pe = __fmaf_rn(c, c, -p);
-  const float s = __fadd_rn(hi, p);
-  const float bb = __fsub_rn(s, hi);
-  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
-  hi = s;
-  lo = __fadd_rn(lo, __fadd_rn(err, pe));
-}
-
-// The same exact-square accumulation for two elements at once with Blackwell's packed fp32x2
-// arithmetic: (hi, lo) hold two independent (hi, lo) accumulators, one per half.
+// using the GPU's slow fp64 pipe per element.  Written with Blackwell's packed fp32x2 arithmetic for
+// two elements at once: (hi, lo) hold two independent (hi, lo) accumulators, one per half.
 __device__ __forceinline__ void add_square2(unsigned long long& hi, unsigned long long& lo, float c0, float c1) {
   asm("{\n\t.reg .b64 c, p, np, pe, s, bb, t, u, e;\n\t"
       "mov.b64 c, {%2, %3};\n\t"
@@ -219,6 +226,52 @@ __device__ __forceinline__ void add_square2(unsigned long long& hi, unsigned lon
 __device__ __forceinline__ double square_total(unsigned long long hi, unsigned long long lo) {
   return ((double)__uint_as_float((uint32_t)hi) + (double)__uint_as_float((uint32_t)(hi >> 32))) +
          ((double)__uint_as_float((uint32_t)lo) + (double)__uint_as_float((uint32_t)(lo >> 32)));
+}
+
+// Range of the fp32-pair accumulation.  Each square is exact for |c| >= 2^-51 (below that its
+// rounding residual falls off fp32's subnormal grid, and below 2^-75 the square itself is lost), and
+// a thread's running sum cannot overflow while the unit's total stays far below 2^128.  A unit whose
+// total lies outside [kSquaresLo, kSquaresHi) -- all of its values tiny, values near overflow, or a
+// non-finite value -- is summed again from its stored values in double, where every square is
+// exact, so the scales follow the exact sum at any magnitude.  Inside the range, squares that lost
+// bits (each below 2^-102, at most 2^16 of them in a unit) move a total of at least 2^-56 by less
+// than 2^-30 of itself.  Normal workloads never leave the range: the check costs one comparison per
+// unit.
+constexpr double kSquaresLo = 0x1p-56;
+constexpr double kSquaresHi = 0x1p100;
+__device__ __forceinline__ bool squares_inexact(double tot) { return !(tot >= kSquaresLo && tot < kSquaresHi); }
+
+// This thread's share (elements tid, tid + nt, ...) of the sum of squares of v[0, len) in double,
+// read through L2 (the values were written by other threads of the block before a barrier).
+__device__ __forceinline__ double squares_fp64(const float* v, int len, int tid, int nt) {
+  double s = 0.0;
+  for (int e = tid; e < len; e += nt) {
+    const double x = (double)__ldcg(v + e);
+    s = __dadd_rn(s, __dmul_rn(x, x));
+  }
+  return s;
+}
+
+// The rare fp64 path: warp 0 sums the unit's stored values again (a fixed order: lane l takes
+// elements l, l + 32, ...) and the block receives the total through red[NT/32 + 1].
+template <int NT>
+__device__ __forceinline__ double unit_squares_fp64(const float* v, int len, double* red) {
+  if (threadIdx.x < 32) {
+    const double s = warp_sum(squares_fp64(v, len, threadIdx.x, 32));
+    if (threadIdx.x == 0) red[NT / 32 + 1] = s;
+  }
+  __syncthreads();
+  return red[NT / 32 + 1];
+}
+
+// A unit's sum of squares for the whole block (every thread calls it and receives the result): the
+// fp32-pair total, or the fp64 sum of the unit's stored values v[0, len) when that total is outside
+// the exact range.  red: NT/32 + 2 slots.
+template <int NT>
+__device__ __forceinline__ double unit_squares(unsigned long long hi, unsigned long long lo, const float* v, int len,
+                                               double* red) {
+  const double tot = block_sum_all<NT>(square_total(hi, lo), red);
+  return squares_inexact(tot) ? unit_squares_fp64<NT>(v, len, red) : tot;
 }
 
 // Transpose of an 8x8 bit matrix held in a 64-bit word (bit 8r+c -> bit 8c+r), by three rounds of
@@ -265,13 +318,14 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
   constexpr bool DENSE_M = MSRC == kMomDense;
   constexpr bool BITS = MSRC == kMomBits || MSRC == kMomBitsShards;
   __shared__ double red[kThreads / 32];
-  const int64_t n_units = (int64_t)A.n_wchunks * A.n;
+  const int64_t n_units = (int64_t)A.n_wchunks * A.nl;
   for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int ci = (int)(u / A.n);
-    const int i = (int)(u - (int64_t)ci * A.n);
+    const int ci = (int)(u / A.nl);
+    const int il = (int)(u - (int64_t)ci * A.nl);  // local worker; global worker i
+    const int i = A.w0 + il;
     const Chunk ch = A.wchunks[ci];
-    const GT* __restrict__ g = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start;
-    float* __restrict__ c = A.c + (int64_t)i * A.Dp + ch.off;
+    const GT* __restrict__ g = static_cast<const GT*>(A.gptr[(int64_t)il * A.T + ch.seg]) + ch.start;
+    float* __restrict__ c = A.c + (int64_t)il * A.Dp + ch.off;
     uint8_t* __restrict__ wb = reinterpret_cast<uint8_t*>(A.wbits + (int64_t)i * A.Wr) + (ch.off >> 3);
     const uint8_t* __restrict__ sb = reinterpret_cast<const uint8_t*>(A.sbits) + (ch.off >> 3);
     const float* __restrict__ md = A.m + ch.off;
@@ -365,7 +419,34 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       wb[ng] = (uint8_t)byte;
     }
     const double tot = block_sum<kThreads>(square_total(hi, lo), red);
-    if (threadIdx.x == 0) A.wpart[(int64_t)i * A.n_wchunks + ci] = tot;
+    if (threadIdx.x == 0) A.wpart[(int64_t)il * A.n_wchunks + ci] = tot;
+  }
+}
+
+// Exact-range repair of the worker partials.  A unit whose fast total lies outside the exact range of
+// the fp32-pair squares (all its values tiny, or near overflow) is summed again in double from its
+// stored c.  One thread per unit scans the partials; the units found are recomputed by the whole
+// block, each in a fixed order, so the result does not depend on which block finds them.  Kept out of
+// k_worker, whose streaming loop stays free of this rare code.
+static __global__ void __launch_bounds__(kThreads) k_worker_exact(const StepArgs A) {
+  __shared__ double red[kThreads / 32 + 2];
+  __shared__ int n_found;
+  __shared__ int found[kThreads];
+  const int64_t n_parts = (int64_t)A.nl * A.n_wchunks;  // partial il*n_wchunks + ci: local worker il, chunk ci
+  for (int64_t base = (int64_t)blockIdx.x * kThreads; base < n_parts; base += (int64_t)gridDim.x * kThreads) {
+    if (threadIdx.x == 0) n_found = 0;
+    __syncthreads();
+    const int64_t q = base + threadIdx.x;
+    if (q < n_parts && squares_inexact(__ldcg(A.wpart + q))) found[atomicAdd(&n_found, 1)] = threadIdx.x;
+    __syncthreads();
+    for (int f = 0; f < n_found; ++f) {
+      const int64_t qq = base + found[f];
+      const int il = (int)(qq / A.n_wchunks), ci = (int)(qq - (int64_t)il * A.n_wchunks);
+      const Chunk ch = A.wchunks[ci];
+      const double tot = unit_squares_fp64<kThreads>(A.c + (int64_t)il * A.Dp + ch.off, ch.len, red);
+      if (threadIdx.x == 0) A.wpart[qq] = tot;
+    }
+    __syncthreads();
   }
 }
 
@@ -386,11 +467,12 @@ __device__ __forceinline__ float finish_scale(const double* part, const Range r,
   return s;
 }
 
+// one scale per (local worker, tensor): item = il*T + k, written to global worker w0 + il
 static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale(const StepArgs A) {
   __shared__ double red[kScaleThreads / 32];
-  const int i = blockIdx.x / A.T, k = blockIdx.x % A.T;
-  const float s = finish_scale(A.wpart + (int64_t)i * A.n_wchunks, A.wseg_ranges[k], A.status, red);
-  if (threadIdx.x == 0) A.wscale_cur[blockIdx.x] = s;
+  const int il = blockIdx.x / A.T, k = blockIdx.x % A.T;
+  const float s = finish_scale(A.wpart + (int64_t)il * A.n_wchunks, A.wseg_ranges[k], A.status, red);
+  if (threadIdx.x == 0) A.wscale_cur[(int64_t)A.w0 * A.T + blockIdx.x] = s;
 }
 
 static __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const StepArgs A) {
@@ -418,10 +500,10 @@ __device__ __forceinline__ float finish_scale_warp(const double* part, const Ran
 
 static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale_warp(const StepArgs A) {
   const int item = blockIdx.x * (kScaleThreads / 32) + (threadIdx.x >> 5);
-  if (item >= A.n * A.T) return;  // the whole warp
-  const int i = item / A.T, k = item % A.T;
-  const float s = finish_scale_warp(A.wpart + (int64_t)i * A.n_wchunks, A.wseg_ranges[k], A.status);
-  if ((threadIdx.x & 31) == 0) A.wscale_cur[item] = s;
+  if (item >= A.nl * A.T) return;  // the whole warp
+  const int il = item / A.T, k = item % A.T;
+  const float s = finish_scale_warp(A.wpart + (int64_t)il * A.n_wchunks, A.wseg_ranges[k], A.status);
+  if ((threadIdx.x & 31) == 0) A.wscale_cur[(int64_t)A.w0 * A.T + item] = s;
 }
 
 static __global__ void __launch_bounds__(kScaleThreads) k_server_scale_warp(const StepArgs A) {
@@ -451,7 +533,7 @@ struct ServerTables {
   float ssc[kMaxWorkers];
   float lut[1 << kLutBits];
   float4 quad[16 * 32];  // [pattern of workers 12..15][lane]
-  double red[kThreads / 32];
+  double red[kThreads / 32 + 2];
 };
 
 // Rebuild the tables for tensor `seg` (block-wide; every thread calls it).
@@ -622,7 +704,7 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
       store_a(a, e, cnt, out);
       sb[gi] = (uint8_t)byte;
     }
-    const double tot = block_sum<kThreads>(square_total(hi, lo), S.red);
+    const double tot = unit_squares<kThreads>(hi, lo, a, ch.len, S.red);
     if (threadIdx.x == 0) A.spart[u] = tot;
   }
 }
@@ -687,6 +769,24 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 }
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory"); }
 
+// The consumer warps' fixed-order sum of one double per consumer thread, left in red[kConsumerWarps]
+// (red: kConsumerWarps + 1 slots at least).  *redo is set when that total lies outside the exact range of the
+// fp32-pair squares and the block has not aborted.
+__device__ __forceinline__ void consumers_total(double v, double* red, int* redo, const volatile int* abort) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  consumers_sync();
+  if (threadIdx.x < 32) {
+    double r = threadIdx.x < kConsumerWarps ? red[threadIdx.x] : 0.0;
+    r = warp_sum(r);
+    if (threadIdx.x == 0) {
+      red[kConsumerWarps] = r;
+      *redo = squares_inexact(r) && !*abort;
+    }
+  }
+  consumers_sync();
+}
+
 struct TileCursor {  // position in this block's sequence of (unit, tile)
   int u, t;
 };
@@ -732,6 +832,7 @@ template <bool HAS_ERR>
 __global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs A) {
   __shared__ ServerTables S;
   __shared__ volatile int abort_flag;
+  __shared__ int redo_squares;  // the chunk's sum of squares is taken again in double
   extern __shared__ __align__(128) unsigned char dyn[];
   const int n = A.n;
   const size_t stage_bytes = server_stage_bytes(n);
@@ -875,15 +976,13 @@ __global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs
     const int u_done = cons.u;
     advance(cons);
     if (last_tile) {  // chunk total among the consumers (fixed order)
-      double v = warp_sum(square_total(hi, lo));
-      if (lane == 0) S.red[threadIdx.x >> 5] = v;
-      consumers_sync();
-      if (threadIdx.x < 32) {
-        double r = lane < kConsumerWarps ? S.red[lane] : 0.0;
-        r = warp_sum(r);
-        if (threadIdx.x == 0 && !abort_flag) A.spart[u_done] = r;
+      consumers_total(square_total(hi, lo), S.red, &redo_squares, &abort_flag);
+      if (redo_squares && threadIdx.x < 32) {  // outside the exact range: warp 0 sums the chunk again in double
+        const Chunk cd = A.chunks[u_done];  // reloaded: keeping the descriptor live costs registers
+        const double r = warp_sum(squares_fp64(A.a + cd.off, cd.len, threadIdx.x, 32));
+        if (threadIdx.x == 0) S.red[kConsumerWarps] = r;
       }
-      consumers_sync();
+      if (threadIdx.x == 0 && !abort_flag) A.spart[u_done] = S.red[kConsumerWarps];
       hi = lo = 0;
     }
   }
@@ -1053,7 +1152,7 @@ template <typename GT, bool BC, bool VEC, bool MON, bool SMALL>
 __global__ void __launch_bounds__(kThreads, SMALL ? 3 : 2) k_warmup(const StepArgs A) {
   constexpr int B = SMALL ? 4 : (sizeof(GT) == 4 ? 8 : 16);
   __shared__ const GT* gsm[kMaxWorkers];
-  __shared__ double red[kThreads / 32];
+  __shared__ double red[kThreads / 32 + 2];
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
     unsigned long long vhi = 0, vlo = 0;
     const Chunk ch = A.chunks[u];
@@ -1141,7 +1240,7 @@ __global__ void __launch_bounds__(kThreads, SMALL ? 3 : 2) k_warmup(const StepAr
       }
     }
     if (MON) {
-      const double tot = block_sum<kThreads>(square_total(vhi, vlo), red);
+      const double tot = unit_squares<kThreads>(vhi, vlo, v, ch.len, red);
       if (threadIdx.x == 0) A.spart[u] = tot;
     }
   }
@@ -1163,8 +1262,9 @@ __host__ __device__ constexpr size_t warmup_dyn_smem(int n) { return kWStages * 
 
 template <typename GT, bool BC, bool MON>
 __global__ void __launch_bounds__(kStagedThreads) k_warmup_staged(const StepArgs A) {
-  __shared__ double red[kConsumerWarps];
+  __shared__ double red[kConsumerWarps + 2];
   __shared__ volatile int abort_flag;
+  __shared__ int redo_squares;  // the chunk's sum of squares is taken again in double
   extern __shared__ __align__(128) unsigned char dyn[];
   const int n = A.n;
   const size_t stage_bytes = warmup_stage_bytes(n);
@@ -1311,15 +1411,13 @@ __global__ void __launch_bounds__(kStagedThreads) k_warmup_staged(const StepArgs
     const int u_done = cons.u;
     advance(cons);
     if (MON && last_tile) {  // chunk total of v^2 among the consumers (fixed order)
-      double t = warp_sum(square_total(vhi, vlo));
-      if (lane == 0) red[threadIdx.x >> 5] = t;
-      consumers_sync();
-      if (threadIdx.x < 32) {
-        double r = lane < kConsumerWarps ? red[lane] : 0.0;
-        r = warp_sum(r);
-        if (threadIdx.x == 0 && !abort_flag) A.spart[u_done] = r;
+      consumers_total(square_total(vhi, vlo), red, &redo_squares, &abort_flag);
+      if (redo_squares && threadIdx.x < 32) {  // outside the exact range: warp 0 sums the chunk again in double
+        const Chunk cd = A.chunks[u_done];
+        const double r = warp_sum(squares_fp64(A.v + cd.off, cd.len, threadIdx.x, 32));
+        if (threadIdx.x == 0) red[kConsumerWarps] = r;
       }
-      consumers_sync();
+      if (threadIdx.x == 0 && !abort_flag) A.spart[u_done] = red[kConsumerWarps];
       vhi = vlo = 0;
     }
   }
@@ -1346,6 +1444,35 @@ __global__ void __launch_bounds__(kThreads) k_freeze(float* v, int64_t n_groups,
 #pragma unroll
     for (int q = 0; q < 8; ++q) r[q] = __fadd_rn(__fsqrt_rn(BC ? __fdiv_rn(r[q], bc2) : r[q]), eps);
     st8(v + gi * 8, r);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Exchange copies of the multi-GPU form: word ranges between this rank's state and the caller's
+// exchange buffers (the messages each peer's servers need, and this rank's share of the broadcast).
+// Regions: 0 worker sign rows, 1 current worker scales, 2 server sign words, 3 current server scales,
+// 4 the caller's exchange buffer.  Offsets and lengths are in 32-bit words (scales are copied bit for
+// bit).
+
+struct XRange {
+  int64_t src, dst;  // word offsets within the source and destination regions
+  int32_t len;       // words, <= kXPiece
+  int16_t sreg, dreg;
+};
+constexpr int kXPiece = 8192;  // longer ranges are cut into pieces of this many words
+
+struct XArgs {
+  const XRange* r;
+  int32_t n;
+  uint32_t* base[5];
+};
+
+static __global__ void __launch_bounds__(kThreads) k_exchange_copy(const XArgs X) {
+  for (int q = blockIdx.x; q < X.n; q += gridDim.x) {
+    const XRange r = X.r[q];
+    const uint32_t* s = X.base[r.sreg] + r.src;
+    uint32_t* d = X.base[r.dreg] + r.dst;
+    for (int e = threadIdx.x; e < r.len; e += kThreads) d[e] = s[e];
   }
 }
 

@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kThreads) k_vec_worker(const float* __restrict
                                                          const float* err_in, float b1, float omb1, int64_t len,
                                                          int n_chunks, uint8_t* __restrict__ bits, float* c,
                                                          double* part) {
-  __shared__ double red[kThreads / 32];
+  __shared__ double red[kThreads / 32 + 2];
   for (int ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const int64_t base = (int64_t)ci * kChunk;
     const int clen = (int)(len - base < kChunk ? len - base : kChunk);
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) k_vec_worker(const float* __restrict
       const int64_t used = (len + 7) >> 3, words = (len + 31) >> 5;
       for (int64_t b = used; b < words * 4; ++b) bits[b] = 0;
     }
-    const double tot = block_sum<kThreads>(square_total(hi, lo), red);
+    const double tot = unit_squares<kThreads>(hi, lo, cc, clen, red);
     if (threadIdx.x == 0) part[ci] = tot;
   }
 }
@@ -208,12 +208,24 @@ extern "C" onebit_status_t onebit_worker_compress_noalloc(const float* m, const 
   if (len < 1 || len > ONEBIT_NOALLOC_MAX_LEN) return ONEBIT_ERR_INVALID_ARG;
   if (grad_dtype < ONEBIT_F32 || grad_dtype > ONEBIT_BF16) return ONEBIT_ERR_INVALID_ARG;
   if (!(beta1 >= 0.0f && beta1 < 1.0f)) return ONEBIT_ERR_INVALID_ARG;
-  if (err_in && err_in != err_out) {
-    // an error input that partly overlaps the output would be read after it is overwritten
-    const char* a0 = reinterpret_cast<const char*>(err_in);
-    const char* b0 = reinterpret_cast<const char*>(err_out);
-    const int64_t bytes = len * 4;
-    if (a0 < b0 + bytes && b0 < a0 + bytes) return ONEBIT_ERR_INVALID_ARG;
+  {
+    // Every output must be disjoint from every input and from the other outputs (the kernels read
+    // the inputs through the read-only cache while the outputs are written), except that err_in may
+    // be exactly err_out (updated in place: each element is read before it is written).
+    struct Span {
+      const char* p;
+      int64_t bytes;
+    };
+    auto span = [](const void* q, int64_t bytes) { return Span{static_cast<const char*>(q), q ? bytes : 0}; };
+    auto overlap = [](Span a, Span b) { return a.bytes > 0 && b.bytes > 0 && a.p < b.p + b.bytes && b.p < a.p + a.bytes; };
+    const int64_t gb = grad_dtype == ONEBIT_F32 ? 4 : 2;
+    const Span in_m = span(m, len * 4), in_g = span(grad, len * gb);
+    const Span in_e = span(err_in == err_out ? nullptr : err_in, len * 4);
+    const Span out_b = span(bits_out, ((len + 31) / 32) * 4), out_s = span(scale_out, 4), out_e = span(err_out, len * 4);
+    for (const Span o : {out_b, out_s, out_e})
+      for (const Span i : {in_m, in_g, in_e})
+        if (overlap(o, i)) return ONEBIT_ERR_INVALID_ARG;
+    if (overlap(out_b, out_s) || overlap(out_b, out_e) || overlap(out_s, out_e)) return ONEBIT_ERR_INVALID_ARG;
   }
   double* part = nullptr;
   if (scratch_for_current_device(&part) != cudaSuccess) {

@@ -19,6 +19,9 @@ those models' sizes stand in for them:
   coordinates (drawn once) multiplied by 100 (heavy tail).
 
 "N(0, s)" in the workload text is read with s as the standard deviation.
+
+One more law serves the parity tests of the norms' range: ``tensor_std`` gives tensor k gradients
+N(0, tensor_std[k]^2), so that whole tensors sit at extreme magnitudes (1e-30, 1e25, ...).
 """
 from __future__ import annotations
 
@@ -53,8 +56,9 @@ class Workload:
     numel: tuple
     n_workers: int
     grad_dtype: int
-    law: str                  # "iid", "block_sigma", "heavy_tail"
+    law: str                  # "iid", "block_sigma", "heavy_tail", "tensor_std"
     grad_std: float = 1e-3
+    tensor_std: tuple = ()    # per-tensor standard deviations of the "tensor_std" law
     warmup_steps: int = 5
     compress_steps: int = 5
     seed: int = 0
@@ -141,6 +145,11 @@ class GradSource:
         elif w.law == "heavy_tail":
             z.mul_(w.grad_std)
             z[self._heavy] *= 100.0
+        elif w.law == "tensor_std":
+            off = 0
+            for L, sd in zip(w.numel, w.tensor_std):
+                z[off: off + int(L)].mul_(sd)
+                off += int(L)
         else:
             raise ValueError(w.law)
         return z.to(TORCH_DTYPE[w.grad_dtype])

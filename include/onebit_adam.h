@@ -92,13 +92,14 @@ typedef enum {
   ONEBIT_K_WARMUP = 0,         /* fused worker-average + Adam */
   ONEBIT_K_FREEZE = 1,         /* den = sqrt(v)+eps */
   ONEBIT_K_WORKER = 2,         /* momentum + error + sign pack + norm partials, all workers */
-  ONEBIT_K_WORKER_SCALE = 3,   /* worker scales from the partials */
+  ONEBIT_K_WORKER_SCALE = 3,   /* worker scales from the partials (and the partials' exact-range repair) */
   ONEBIT_K_SERVER = 4,         /* unpack + ordered average + server error + sign pack + partials */
   ONEBIT_K_SERVER_SCALE = 5,   /* server shard scales from the partials */
   ONEBIT_K_UPDATE = 6,         /* unpack broadcast + preconditioned update */
   ONEBIT_K_EXPORT = 7,         /* state export / import */
   ONEBIT_K_EC_UPDATE = 8,      /* Adam on the broadcast gradient (gradient-compression baseline) */
-  ONEBIT_NUM_KERNELS = 9
+  ONEBIT_K_EXCHANGE = 9,       /* multi-GPU form: packing and unpacking of the exchange buffers */
+  ONEBIT_NUM_KERNELS = 10
 } onebit_kernel_t;
 
 typedef struct {
@@ -135,16 +136,26 @@ onebit_status_t onebit_adam_workspace_size(const onebit_adam_config_t* cfg, size
 onebit_status_t onebit_adam_init(const onebit_adam_config_t* cfg, float* const* params, void* workspace,
                                  size_t workspace_bytes, onebit_stream_t stream, onebit_adam_t** out);
 
-/* One warm-up Adam step (legal while phase == WARMUP and t < T_w).  grads: host array [n*T] of
- * device pointers, ordered [worker][tensor], each L_k values of grad_dtype.  t += 1. */
+/* One warm-up Adam step (legal while phase == WARMUP and t < T_w): the mean of the n workers'
+ * gradients, summed in worker order (the uncompressed allreduce of the warm-up stage, Tang et al.
+ * Sec. 4.3 and 6), then m = b1 m + (1-b1) g, v = b2 v + (1-b2) g^2, x -= lr m/(sqrt(v)+eps) (the
+ * AIMech page's summary formulas).  grads: host array [n*T] of device pointers, ordered
+ * [worker][tensor], each L_k values of grad_dtype.  t += 1. */
 onebit_status_t onebit_adam_warmup_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream);
 
-/* Freeze the variance: den = sqrt(v) + eps (v / (1 - b2^t) first with bias correction).  Legal in
- * phase WARMUP after at least one warm-up step; the phase becomes COMPRESS, worker and server
- * errors start at 0 and the first compression step reads the fp32 warm-up momentum. */
+/* Freeze the variance: den = sqrt(v) + eps (v / (1 - b2^t) first with bias correction) -- the
+ * preconditioner V = diag(sqrt(v_Tw) + eps) of the AIMech page, under which the compression stage is
+ * momentum SGD with a coordinate-wise learning rate (Tang et al. Sec. 3.3 and 5).  Legal in phase
+ * WARMUP after at least one warm-up step; the phase becomes COMPRESS, worker and server errors start
+ * at 0 and the first compression step reads the fp32 warm-up momentum. */
 onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t stream);
 
-/* One compression-stage step (legal in phase COMPRESS).  grads as for warmup_step.  t += 1. */
+/* One compression-stage step (legal in phase COMPRESS): the three steps of Tang et al. Sec. 11 --
+ * every worker updates its momentum and compresses it with error compensation (Sec. 4.1, 4.3; the
+ * codewithpapers page's scale), every server shard averages the workers' messages and compresses
+ * again with its own error (the AIMech mechanism "custom compressed allreduce"), and the broadcast
+ * momentum updates the parameters -- as stated at the top of this file.  grads as for warmup_step.
+ * t += 1. */
 onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream);
 
 /* One step of the baseline the method is contrasted with ("1-bit Adam ...", Sec. 3.2 and 4.2):
@@ -199,7 +210,8 @@ onebit_status_t onebit_adam_export(onebit_adam_t* h, int32_t what, int32_t worke
 onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worker, const void* src, onebit_stream_t stream);
 
 /* Bytes one worker sends per compression step (sign words + one fp32 scale per tensor) and the
- * bytes the same vector takes in fp32. */
+ * bytes the same vector takes in fp32: the 1/32 volume behind the codewithpapers page's 97% (96.9%)
+ * reduction against fp32. */
 onebit_status_t onebit_adam_comm_bytes(const onebit_adam_t* h, uint64_t* compressed, uint64_t* fp32_bytes);
 
 /* Per-kernel timing with CUDA events recorded around every launch on the launch stream.
@@ -218,6 +230,17 @@ onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launch
  * warm-up step has run. */
 onebit_status_t onebit_adam_set_variance_monitor(onebit_adam_t* h, int32_t enable);
 onebit_status_t onebit_adam_variance_norm(onebit_adam_t* h, double* norm, int64_t* step);
+
+/* Automatic freeze.  The pages motivate freezing with the variance's norm, which stabilises early in
+ * training (Tang et al. Sec. 3.3) and sets the warm-up length T_w (the AIMech page).  With tol > 0,
+ * every following warm-up step also computes ||v_t||_2 (as the variance monitor does), waits for it
+ * (the call then synchronises `stream`), and freezes the variance before returning -- exactly as
+ * onebit_adam_freeze_variance() does -- at the first step whose norm changed by at most tol relative
+ * to the previous step's (|n_t - n_{t-1}| <= tol * n_{t-1}), or at the step that reaches T_w.  The
+ * caller reads the phase with onebit_adam_get_step().  tol = 0 turns it off; a negative or non-finite
+ * tol is ONEBIT_ERR_INVALID_ARG.  Enabling it allocates the monitor's pinned host slot once
+ * (ONEBIT_ERR_NOMEM if that fails). */
+onebit_status_t onebit_adam_set_auto_freeze(onebit_adam_t* h, double tol);
 
 /* Set the learning rate gamma used by the following steps (warm-up, compression and baseline).  The
  * pages keep gamma constant; this serves the schedules training uses (warm-up ramps, decay).  The
@@ -258,6 +281,68 @@ onebit_status_t onebit_adam_plan_chunks(const onebit_adam_config_t* cfg, int64_t
 onebit_status_t onebit_adam_plan_worker_chunks(const onebit_adam_config_t* cfg, int64_t* rows, int64_t cap,
                                                int64_t* count);
 
+/* ---- Multi-GPU form: the n workers spread over `world` GPUs, one process (rank) per GPU ----
+ *
+ * The pages' system runs the exchange across machines: every worker compresses its momentum, an
+ * all-to-all sends each server the workers' compressed chunks of its shard, every server averages,
+ * compresses again and keeps its own error, and an allgather brings the result to every worker, which
+ * updates its copy of the model (Tang et al. Sec. 6 and Sec. 11 steps 1-3; the AIMech page's
+ * "gather-then-broadcast"; the NCCL backend of the 1-bit LAMB page's abstract).  In this form rank r
+ * of `world` (n a multiple of world, nl = n/world) simulates workers r*nl .. r*nl+nl-1 and serves
+ * shards r*nl .. r*nl+nl-1 of every tensor (or scale block); it keeps a full copy of x, m and den, the
+ * c of its own workers and the server state of its own shards.  A compression step is split at the
+ * exchange: the caller moves the buffers between the calls with its collectives (an all-to-all with
+ * equal blocks, then an all-gather), and each rank's results are bit-identical to a single GPU
+ * simulating all n workers (onebit_adam_init).  The warm-up step takes every worker's gradient (n*T
+ * pointers, e.g. after an all-gather of the ranks' gradients) and computes the same ordered mean on
+ * every rank; compress_step, compress_step_host and ec_adam_step return ONEBIT_ERR_UNSUPPORTED when
+ * world > 1.  Exports: WORKER_ERROR only for this rank's workers (else ONEBIT_ERR_INVALID_ARG);
+ * SERVER_ERROR on this rank's shards (other elements read 0); WORKER_BITS rows of other ranks' workers
+ * hold only this rank's shards.  Imports: WORKER_ERROR for this rank's workers; SERVER_ERROR on this
+ * rank's shards. */
+
+/* Workspace bytes of rank `rank` of `world` (0 <= rank < world, n_workers a multiple of world). */
+onebit_status_t onebit_adam_workspace_size_rank(const onebit_adam_config_t* cfg, int32_t rank, int32_t world,
+                                                size_t* bytes);
+/* Create rank `rank`'s handle; the other arguments as for onebit_adam_init.  world = 1 gives a handle
+ * equal to onebit_adam_init's on which the split step is legal too (its exchange buffers may be NULL). */
+onebit_status_t onebit_adam_init_rank(const onebit_adam_config_t* cfg, int32_t rank, int32_t world,
+                                      float* const* params, void* workspace, size_t workspace_bytes,
+                                      onebit_stream_t stream, onebit_adam_t** out);
+/* Words (uint32) of one block of the all-to-all (send_block; the send and receive buffers hold `world`
+ * blocks each, block q for / from rank q) and of one block of the all-gather (bcast_block; this rank's
+ * contribution, the gathered buffer holds `world` blocks in rank order).  The same on every rank. */
+onebit_status_t onebit_adam_exchange_words(const onebit_adam_t* h, int64_t* send_block, int64_t* bcast_block);
+/* Step 1 (Sec. 11 step 1, workers): this rank's workers form their momentum with error compensation
+ * and compress it; block q of `send` (device, world*send_block words) receives, for each of this
+ * rank's workers, its scales and the sign words of rank q's shards.  grads: host array [nl*T] of
+ * device pointers, [local worker][tensor].  Legal in phase COMPRESS outside a split step.  This
+ * rank's own block of `send` is not written (its data never leaves). */
+onebit_status_t onebit_adam_compress_begin(onebit_adam_t* h, const void* const* grads, uint32_t* send,
+                                           onebit_stream_t stream);
+/* Step 2 (Sec. 11 step 2, servers): `recv` (device, world*send_block words; block p from rank p, as
+ * an all-to-all of the send buffers delivers it) brings every worker's message for this rank's
+ * shards; the shards are averaged, compressed again with the server error, and `bcast` (device,
+ * bcast_block words) receives this rank's server scales and sign words.  Legal after
+ * compress_begin. */
+onebit_status_t onebit_adam_compress_serve(onebit_adam_t* h, const uint32_t* recv, uint32_t* bcast,
+                                           onebit_stream_t stream);
+/* Step 3 (Sec. 11 step 3, broadcast and update): `gathered` (device, world*bcast_block words, the
+ * all-gather of every rank's bcast block in rank order) completes the broadcast momentum, and the
+ * parameters are updated.  Legal after compress_serve; t += 1.  `send`, `recv`, `bcast` and
+ * `gathered` must stay valid until `stream` has passed the call that reads or writes them; with
+ * world = 1 they are not touched and may be NULL. */
+onebit_status_t onebit_adam_compress_end(onebit_adam_t* h, const uint32_t* gathered, onebit_stream_t stream);
+/* The exchange copies of rank `rank` of `world` (host only): up to `cap` rows of eight int64 {stage
+ * (0 begin pack, 1 serve unpack, 2 serve pack, 3 end unpack), source region, source row, source
+ * offset, destination region, destination row, destination offset, words}.  Regions: 0 worker sign
+ * words (row = worker, offset = word in the concatenation of the tensors' words), 1 worker scales (row
+ * = worker, offset = tensor), 2 server sign words (row 0), 3 server scales (row = tensor, offset =
+ * shard), 4 the exchange buffer (row = block, offset = word in the block).  *count receives the number
+ * of rows, *send_block and *bcast_block the block sizes in words. */
+onebit_status_t onebit_adam_plan_exchange(const onebit_adam_config_t* cfg, int32_t rank, int32_t world, int64_t* rows,
+                                          int64_t cap, int64_t* count, int64_t* send_block, int64_t* bcast_block);
+
 /* Largest vector onebit_worker_compress_noalloc() accepts (elements). */
 #define ONEBIT_NOALLOC_MAX_LEN 268435456
 
@@ -276,9 +361,14 @@ onebit_status_t onebit_adam_plan_worker_chunks(const onebit_adam_config_t* cfg, 
  *   bits = [c >= 0] packed (bit b of word w = element 32w+b, padding bits 0);
  *   err_out = c - scale*sign(c).
  * m: len fp32, device.  grad: len values of grad_dtype, device.  err_in: len fp32, device, or NULL
- * for a zero error; it may be the same buffer as err_out but may not partly overlap it.
- * bits_out: ceil(len/32) uint32, device.  scale_out: one fp32, device.  err_out: len fp32, device.
- * 1 <= len <= ONEBIT_NOALLOC_MAX_LEN, otherwise ONEBIT_ERR_INVALID_ARG (nothing is enqueued).
+ * for a zero error.  bits_out: ceil(len/32) uint32, device.  scale_out: one fp32, device.  err_out:
+ * len fp32, device.  Every output must be disjoint from every input and from the other outputs,
+ * except that err_in may be exactly err_out (the error is then updated in place); any other overlap,
+ * a NULL input or output other than err_in, or a len outside 1 <= len <= ONEBIT_NOALLOC_MAX_LEN is
+ * ONEBIT_ERR_INVALID_ARG, and nothing is enqueued.  Pointers of any alignment are accepted (32-byte
+ * aligned fp32 buffers and 16-byte aligned 16-bit gradients take the vector loads).
+ * Non-finite inputs are not reported: the call returns before its kernels run, so a NaN or infinite
+ * norm reaches scale_out (and err_out) as is -- a caller that needs the check tests *scale_out.
  *
  * The first call on a device looks up the scratch array's device address (once per device, with
  * that device current); make that first call before any stream capture.  Every call on a device

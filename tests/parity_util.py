@@ -44,7 +44,8 @@ def _close(name, got, want, mask=None, rtol=RTOL, atol=ATOL):
     want = np.asarray(want, np.float64)
     if mask is not None:
         got, want = got[mask], want[mask]
-    bad = ~(np.abs(got - want) <= atol + rtol * np.abs(want))
+    with np.errstate(invalid="ignore"):
+        bad = ~((got == want) | (np.abs(got - want) <= atol + rtol * np.abs(want)))  # equal infinities pass
     bad |= np.isnan(got) != np.isnan(want)
     if bad.any():
         idx = np.flatnonzero(bad)[:5]
@@ -62,7 +63,7 @@ def _close_t(name, got, want, mask=None, rtol=RTOL, atol=ATOL):
         got, want = got[mask], want[mask]
         if torch.is_tensor(rtol):
             rtol = rtol[mask]
-    bad = ~((got - want).abs() <= atol + rtol * want.abs())
+    bad = ~((got == want) | ((got - want).abs() <= atol + rtol * want.abs()))  # equal infinities pass
     bad |= torch.isnan(got) != torch.isnan(want)
     if bool(bad.any()):
         idx = torch.nonzero(bad)[:5].flatten()

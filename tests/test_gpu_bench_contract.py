@@ -40,10 +40,10 @@ def test_bench_line_has_every_key():
     for k in ("sm_mhz", "sm_max_mhz", "reasons"):
         assert k in c, k
     b = d["cpu_baseline"]
-    for k in ("value", "unit", "cores", "kind", "sample"):
+    for k in ("value", "unit", "cores", "kind", "sample", "d_sample", "host_nproc", "host_cpu", "pinned_core0"):
         assert k in b, k
     assert b["kind"] == "oracle" and b["cores"] >= 1
-    assert d["gpu_launches"] == 5 * 4  # five kernels per compression step
+    assert d["gpu_launches"] == 6 * 4  # six kernels per compression step
 
 
 def test_reference_arm_line():
@@ -51,3 +51,4 @@ def test_reference_arm_line():
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert 0 < d["config"]["d_sample"] <= d["config"]["d"]  # the timed sample is stated beside the workload

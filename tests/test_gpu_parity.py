@@ -393,6 +393,28 @@ def test_degenerate_inputs(dtype):
     p.close()
 
 
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16], ids=["f32", "bf16"])
+def test_norms_at_extreme_magnitudes(dtype):
+    """The scales preserve the magnitude of the compressed vector ("1-bit Adam ...", Sec. 4.3; the
+    codewithpapers "1-bit Adam" scale definition) at any magnitude: whole tensors whose gradients,
+    and hence c and a, sit near 2^-51, at 1e-20 and 1e-30 (squares far below fp32's subnormal range)
+    and at 1e25 (squares beyond fp32's range; v overflows to infinity there, on both sides), beside
+    two ordinary tensors.  Every scale must match the oracle's exact double-precision norm within one ulp
+    (almost all exactly) and every state element within the parity tolerance."""
+    numel = (5000, 4099, 3001, 6000, 2003, 4096 + 7)
+    w = _tiny(numel=numel, n_workers=4, grad_dtype=dtype, law="tensor_std",
+              tensor_std=(1e-3, 2.0 ** -51, 1e-20, 1e-30, 1e25, 1e-3), warmup_steps=2, compress_steps=3, seed=191)
+    p = Pair(w)
+    for _ in range(2):
+        p.warmup()
+    p.freeze()
+    for _ in range(3):
+        p.compress()
+    st = p.stats
+    assert st.scales_exact >= 0.95 * st.scales, st
+    p.close()
+
+
 def test_two_handles_on_two_streams():
     """Two optimizers stepped in interleaved order on two non-default CUDA streams (their kernels
     free to overlap) end bit-identical to the same schedules run alone on the default stream: a
@@ -523,11 +545,12 @@ def test_timing_and_launch_counts():
     p.compress(check=False)
     t = p.gpu.kernel_times()
     assert t["warmup"][1] == 1 and t["freeze"][1] == 1
-    for k in ("worker", "worker_scale", "server", "server_scale", "update"):
+    for k in ("worker", "server", "server_scale", "update"):
         assert t[k][1] == 1 and t[k][0] > 0.0, (k, t[k])
+    assert t["worker_scale"][1] == 2 and t["worker_scale"][0] > 0.0  # the partials' range repair, the scales
     n0 = p.gpu.launch_count()
     p.compress(check=False)
-    assert p.gpu.launch_count() - n0 == 5
+    assert p.gpu.launch_count() - n0 == 6
     p.close()
 
 
@@ -595,6 +618,50 @@ def test_warmup_until_stable_stops_where_the_closed_form_says():
     assert steps == t_star, (steps, t_star)
     assert p.gpu.get_step() == (t_star, ob.PHASE_COMPRESS)
     p.close()
+
+
+def test_auto_freeze_through_the_c_abi():
+    """onebit_adam_set_auto_freeze: the library itself freezes at the first warm-up step whose
+    variance-norm change drops to the tolerance (the constant-gradient closed form above), leaving
+    den, x and m bit-identical to the oracle's warm-up and freeze; with a tolerance never met it
+    freezes at T_w; bad tolerances are refused."""
+    import math
+
+    w = _tiny(numel=(50_000,), n_workers=2, warmup_steps=100, seed=111)
+    p = Pair(w)
+    g_host = p.src.grads(0)
+    g = [t.cuda() for t in g_host]
+    b2 = float(np.float32(w.beta2))
+    r = {t: b2 ** (t - 1) * (1 - b2) / (1 - b2 ** (t - 1)) for t in range(2, 101)}
+    t_star = 21
+    for bad in (-1.0, float("nan"), float("inf")):
+        with pytest.raises(ob.OneBitError) as e:
+            p.gpu.set_auto_freeze(bad)
+        assert e.value.status == ob.ERR_INVALID_ARG
+    p.gpu.set_auto_freeze(math.sqrt(r[t_star] * r[t_star - 1]))
+    t = 0
+    while p.gpu.get_step()[1] == ob.PHASE_WARMUP:
+        p.gpu.warmup_step(g)
+        p.ora.warmup_step([W.to_numpy_grad(x) for x in g_host])
+        t += 1
+    assert t == t_star and p.gpu.get_step() == (t_star, ob.PHASE_COMPRESS)
+    p.ora.freeze()
+    torch.cuda.synchronize()
+    assert np.array_equal(p.gpu.export_state(ob.STATE_V).cpu().numpy().view(np.uint32), p.ora.view("den").view(np.uint32))
+    assert np.array_equal(p.x().view(np.uint32), p.ora.view("x").view(np.uint32))
+    p.close()
+
+    w2 = _tiny(numel=(5000,), n_workers=2, warmup_steps=3, seed=112)
+    q = Pair(w2)
+    q.gpu.set_auto_freeze(1e-30)  # never met: the freeze comes at T_w
+    for step in range(3):
+        assert q.gpu.get_step() == (step, ob.PHASE_WARMUP)
+        q.warmup(check=False)
+    assert q.gpu.get_step() == (3, ob.PHASE_COMPRESS)
+    q.ora.freeze()
+    q.gpu.set_auto_freeze(0.0)
+    q.compress()  # the compression stage continues from the library's own freeze
+    q.close()
 
 
 @pytest.mark.parametrize("numel,n,dtype,bc", [

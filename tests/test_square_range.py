@@ -2,7 +2,8 @@
 norms: p = fl32(c*c) and e = fl32(c*c - p) (one FMA), so that p + e = c*c.  The residual c*c - p
 needs the bits of c*c below p's last place, which land on fp32's subnormal grid once c is small.
 The claim checked here: p + e equals c*c exactly for every fp32 |c| >= 2^-51, and not for every c
-below that.  No GPU needed: an FMA's result is the correctly rounded c*c - p, which double
+below that; and the unit-level range check that sends every unit outside [2^-56, 2^100) to a
+double-precision sum (below).  No GPU needed: an FMA's result is the correctly rounded c*c - p, which double
 arithmetic gives exactly here (c*c and p are exact in double)."""
 import numpy as np
 
@@ -38,3 +39,69 @@ def test_squares_lose_exactness_below_that():
     tiny = np.float32(2.0 ** -76)
     p, e = _pair(np.array([tiny]))
     assert p[0] == 0 and e[0] == 0
+
+
+# ---- the unit-level range check of the kernels' norms
+#
+# The kernels accumulate each thread's squares as an fp32 (hi, lo) pair (exact two-sum of p, plus the
+# FMA residual), promote the pair to double once per work unit and sum the threads.  A unit whose
+# total lies outside [2^-56, 2^100) is summed again from its stored values in double.  The emulation
+# below follows that arithmetic in numpy fp32 (every operation correctly rounded, the FMA residual
+# from exact double arithmetic) and checks the claim the threshold rests on: inside the range the
+# fast total is within 2^-30 of the exact sum (squares that lost bits below 2^-102 cannot move it
+# more), and a unit of only tiny values, or of values whose squares overflow fp32, lands outside it.
+
+LO, HI = 2.0 ** -56, 2.0 ** 100
+
+
+def _fast_unit_total(values, threads=256):
+    """The kernels' fast sum of squares of one unit: thread t takes values t, t+threads, ..."""
+    v = np.asarray(values, np.float32)
+    per = -(-v.size // threads)
+    v = np.concatenate([v, np.zeros(per * threads - v.size, np.float32)]).reshape(per, threads)
+    hi = np.zeros(threads, np.float32)
+    lo = np.zeros(threads, np.float32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        for c in v:
+            p, pe = _pair(c)
+            s = (hi + p).astype(np.float32)
+            bb = (s - hi).astype(np.float32)
+            t = (hi - (s - bb).astype(np.float32)).astype(np.float32)
+            u = (p - bb).astype(np.float32)
+            e = ((t + u).astype(np.float32) + pe).astype(np.float32)
+            lo = (lo + e).astype(np.float32)
+            hi = s
+    return float(np.sum(hi.astype(np.float64) + lo.astype(np.float64)))
+
+
+def _exact_sum(values):
+    import math
+
+    return math.fsum(float(x) * float(x) for x in np.asarray(values, np.float64))
+
+
+def test_fast_total_is_close_inside_the_range():
+    rng = np.random.default_rng(2)
+    inside = 0
+    for trial in range(40):
+        n = 65536 if trial % 4 == 0 else 4096
+        scale = 2.0 ** rng.uniform(-50, 45)
+        v = (rng.standard_normal(n) * scale).astype(np.float32)
+        k = rng.integers(0, n // 2)  # a share of values below 2^-51, whose squares lose bits
+        v[:k] = (rng.standard_normal(k) * 2.0 ** rng.uniform(-80, -52)).astype(np.float32)
+        fast, exact = _fast_unit_total(v), _exact_sum(v)
+        if LO <= fast < HI:
+            inside += 1
+            assert abs(fast - exact) <= 2.0 ** -30 * exact, (trial, fast, exact)
+    assert inside >= 30  # the draws exercise the range, not only the fallback
+
+
+def test_tiny_and_huge_units_leave_the_range():
+    rng = np.random.default_rng(3)
+    for e in (-52, -60, -75, -100, -126):
+        v = (rng.standard_normal(4096) * 2.0 ** e).astype(np.float32)
+        assert not (LO <= _fast_unit_total(v) < HI), e  # summed again in double
+    for e in (50, 60, 64, 100):
+        v = (rng.standard_normal(4096) * 2.0 ** e).astype(np.float32)
+        t = _fast_unit_total(v)
+        assert not (LO <= t < HI), (e, t)  # too large, infinite or NaN: summed again in double
