@@ -395,7 +395,6 @@ struct onebit_adam {
   std::vector<cudaEvent_t> event_pool;
   int64_t launches = 0;
   std::unordered_map<const void*, int> occupancy;
-  bool smem_configured[2] = {false, false};
   std::unordered_set<const void*> dyn_smem_set;  // kernels whose dynamic shared-memory limit is raised
   uint32_t stall_tx = 0;  // fault injection (see onebit_adam_set_fault_injection)
   int fail_allocs = 0;    // allocations still to refuse (fault injection)
@@ -699,17 +698,25 @@ onebit_status_t run_server_v(onebit_adam* h, const StepArgs& A, cudaStream_t st)
     return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
   }
   if (A.n <= kStageMaxWorkers) {
-    // shared-memory staged variant: the tiles of a and the n sign rows arrive by bulk copies
-    auto k = k_server_staged<HE>;
-    const size_t dyn = server_dyn_smem(A.n);
-    if (!h->smem_configured[HE ? 1 : 0]) {
-      cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)server_dyn_smem(kStageMaxWorkers));
-      if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute");
-      h->smem_configured[HE ? 1 : 0] = true;
+    // shared-memory staged variant: the tiles of a and the n sign rows arrive by bulk copies; the
+    // common worker counts have their own compile-time instances
+    auto go = [&](auto k) -> onebit_status_t {
+      const size_t dyn = server_dyn_smem(A.n);
+      if (!h->dyn_smem_set.count((const void*)k)) {
+        cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)server_dyn_smem(kStageMaxWorkers));
+        if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute");
+        h->dyn_smem_set.insert((const void*)k);
+      }
+      return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kStagedThreads, A.n_chunks, dyn),
+                    kStagedThreads, st, A, dyn);
+    };
+    switch (A.n) {
+      case 4: return go(k_server_staged<HE, 4>);
+      case 8: return go(k_server_staged<HE, 8>);
+      case 16: return go(k_server_staged<HE, 16>);
+      default: return go(k_server_staged<HE, 0>);
     }
-    return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kStagedThreads, A.n_chunks, dyn), kStagedThreads,
-                  st, A, dyn);
   }
   auto k = k_server<HE, false>;
   return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);

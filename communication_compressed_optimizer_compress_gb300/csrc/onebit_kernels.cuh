@@ -605,14 +605,18 @@ __device__ __forceinline__ void server_add_worker(float (&s)[8], float si, uint3
 }
 
 // a = sum / n + eps_prev, its sign byte (bits past `cnt` cleared) and the squares of the first cnt.
-template <bool HAS_ERR>
+// NW > 0: the worker count is the compile-time constant NW (the same arithmetic, folded).
+template <bool HAS_ERR, int NW = 0>
 __device__ __forceinline__ uint32_t server_finish(const StepArgs& A, const float (&s)[8], const float (&ap)[8],
                                                   float Sp, int cnt, float (&out)[8], unsigned long long& hi,
                                                   unsigned long long& lo) {
+  constexpr bool kPow2 = NW > 0 && (NW & (NW - 1)) == 0;
   uint32_t byte = 0;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const float avg = A.pow2 ? __fmul_rn(s[q], A.inv_n) : __fdiv_rn(s[q], A.nf);
+    // x / n, as x * (1/n) when n is a power of two (bit-identical); 1/n is exact there
+    const float avg = NW > 0 ? (kPow2 ? __fmul_rn(s[q], 1.0f / NW) : __fdiv_rn(s[q], (float)NW))
+                             : (A.pow2 ? __fmul_rn(s[q], A.inv_n) : __fdiv_rn(s[q], A.nf));
     const float ep = HAS_ERR ? error_of(ap[q], Sp) : 0.0f;
     out[q] = __fadd_rn(avg, ep);
     byte |= (out[q] >= 0.0f ? 1u : 0u) << q;
@@ -828,13 +832,16 @@ __device__ __forceinline__ void build_server_tables_consumers(ServerTables& S, c
   }
 }
 
-template <bool HAS_ERR>
-__global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs A) {
+// NW > 0: compiled for exactly NW workers (the common counts), so that the per-element worker checks,
+// the sign-byte loads and the division by n fold at compile time; NW = 0: any n up to
+// kStageMaxWorkers.  Both compute the same values.
+template <bool HAS_ERR, int NW>
+__global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepArgs A) {
   __shared__ ServerTables S;
   __shared__ volatile int abort_flag;
   __shared__ int redo_squares;  // the chunk's sum of squares is taken again in double
   extern __shared__ __align__(128) unsigned char dyn[];
-  const int n = A.n;
+  const int n = NW > 0 ? NW : A.n;
   const size_t stage_bytes = server_stage_bytes(n);
   uint64_t* full = reinterpret_cast<uint64_t*>(dyn + kStages * stage_bytes);
   uint64_t* empty = full + kStages;
@@ -952,7 +959,7 @@ __global__ void __launch_bounds__(kStagedThreads) k_server_staged(const StepArgs
         server_sum16(S, n, b, sum);
         for (int i = 16; i < n; ++i) server_add_worker(sum, S.ssc[i], bs[i * kRowBytes + boff + gl]);
         float out[8];
-        const uint32_t byte = server_finish<HAS_ERR>(A, sum, ap, Sp, cnt, out, hi, lo);
+        const uint32_t byte = server_finish<HAS_ERR, NW>(A, sum, ap, Sp, cnt, out, hi, lo);
         const int64_t e = (int64_t)ch.off + e0 + gl * 8;
         store_a(A.a, e, cnt, out);
         reinterpret_cast<uint8_t*>(A.sbits)[e >> 3] = (uint8_t)byte;
