@@ -577,20 +577,34 @@ __device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2,
   return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);  // b0 | b1<<8 | ...
 }
 
+// PTX byte permute in its default mode: each selector nibble's low 3 bits pick one of the 8 source
+// bytes, and a set top bit replicates that byte's sign bit over the whole result byte.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 __device__ __forceinline__ void server_sum16(const ServerTables& S, int n, const uint32_t (&b)[16], float (&s)[8]) {
   const int lane = threadIdx.x & 31;
   const uint64_t t0 = transpose8x8(((uint64_t)pack4(b[4], b[5], b[6], b[7]) << 32) | pack4(b[0], b[1], b[2], b[3]));
   uint64_t t1 = 0;
   if (n > 8) t1 = transpose8x8(((uint64_t)pack4(b[12], b[13], b[14], b[15]) << 32) | pack4(b[8], b[9], b[10], b[11]));
+  // byte q of t0: workers 0..7 of element q; of t1: workers 8..15.  Split t1 into workers 8..11 (low
+  // nibbles, mid) and 12..15 (hi), so that one byte permute yields each element's table index.
   const uint32_t t0w[2] = {(uint32_t)t0, (uint32_t)(t0 >> 32)};
-  const uint32_t t1w[2] = {(uint32_t)t1, (uint32_t)(t1 >> 32)};
+  const uint32_t mid[2] = {(uint32_t)t1 & 0x0f0f0f0fu, (uint32_t)(t1 >> 32) & 0x0f0f0f0fu};
+  const uint32_t hiw[2] = {((uint32_t)t1 >> 4) & 0x0f0f0f0fu, ((uint32_t)(t1 >> 32) >> 4) & 0x0f0f0f0fu};
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    // bits 0..7: workers 0..7 of element q; bits 8..15: workers 8..15
-    const uint32_t x = __byte_perm(t0w[q >> 2], t1w[q >> 2], (q & 3) | (((q & 3) + 4) << 4));
-    s[q] = S.lut[x & 0x0fffu];
+    // index bits 0..7: workers 0..7, bits 8..11: workers 8..11; bytes 2-3 are the sign replica of a
+    // byte of mid (whose top bit is 0), i.e. zero
+    const uint32_t r = (q & 3) + 4;
+    const uint32_t x = prmt(t0w[q >> 2], mid[q >> 2], (q & 3) | (r << 4) | ((8 | r) << 8) | ((8 | r) << 12));
+    s[q] = S.lut[x];
     if (n > kLutBits) {  // workers 12..15, in order
-      const float4 qv = S.quad[((x >> 12) & 0x0fu) * 32 + lane];
+      const uint32_t pat = __byte_perm(hiw[q >> 2], 0u, (q & 3) | 0x4440u);
+      const float4 qv = S.quad[pat * 32 + lane];
       s[q] = __fadd_rn(s[q], qv.x);
       if (n > kLutBits + 1) s[q] = __fadd_rn(s[q], qv.y);
       if (n > kLutBits + 2) s[q] = __fadd_rn(s[q], qv.z);
@@ -617,7 +631,10 @@ __device__ __forceinline__ uint32_t server_finish(const StepArgs& A, const float
     // x / n, as x * (1/n) when n is a power of two (bit-identical); 1/n is exact there
     const float avg = NW > 0 ? (kPow2 ? __fmul_rn(s[q], 1.0f / NW) : __fdiv_rn(s[q], (float)NW))
                              : (A.pow2 ? __fmul_rn(s[q], A.inv_n) : __fdiv_rn(s[q], A.nf));
-    const float ep = HAS_ERR ? error_of(ap[q], Sp) : 0.0f;
+    // the server error a - Sp*sign(a), as a - copysign(Sp, a): the same value except for a = -0, which a
+    // kernel never stores (the sum is never -0) and an import stores only with Sp = 0, where either
+    // form gives a zero and avg + ep is unchanged
+    const float ep = HAS_ERR ? __fsub_rn(ap[q], copysignf(Sp, ap[q])) : 0.0f;
     out[q] = __fadd_rn(avg, ep);
     byte |= (out[q] >= 0.0f ? 1u : 0u) << q;
   }
