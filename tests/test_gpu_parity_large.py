@@ -63,6 +63,15 @@ FULL = {
     # the BERT-Large law (16 workers, fp16 block-sigma gradients) on 80e6 parameters: the benchmark's
     # kernels with its 65536-element chunks (16 server tiles per chunk)
     "bert_large_law_d80M": W.WORKLOADS["bert_large"].with_(numel=(80_000_000,), warmup_steps=1, compress_steps=2),
+    # the GPT-2 law (4 workers, bf16 gradients with a 1% heavy tail) on 80e6 parameters: the 4-worker
+    # kernel instances with 65536-element chunks
+    "gpt2_law_d80M": W.WORKLOADS["gpt2_1p5b"].with_(numel=(80_000_000,), warmup_steps=1, compress_steps=2),
+    # the 340-tensor BERT-Large list at full size (334e6 parameters, 8 workers, fp32, per-tensor scales)
+    "ragged_bert_large_full": W.WORKLOADS["ragged_bert_large"].with_(warmup_steps=1, compress_steps=2),
+    # the headline workload itself: BERT-Large, 340e6 parameters, 16 workers, fp16 block-sigma
+    # gradients; one warm-up step stands in for the twenty of the benchmark (the path is the same),
+    # then the first compression step and one steady-state step, every element compared
+    "bert_large_full": W.WORKLOADS["bert_large"].with_(warmup_steps=1, compress_steps=2),
 }
 
 
