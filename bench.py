@@ -297,7 +297,7 @@ def run_reference(args, w):
     K, Wm = max(1, args.steps), max(1, args.warmup)
 
     def make(d):
-        ws = w.with_(numel=(d,))
+        ws = w if d == w.d and args.ref_full else w.with_(numel=(d,))
         src = W.GradSource(ws, "cpu")
         o = oracle.OneBitAdamOracle([d], ws.n_workers, W.params(ws, "cpu")[0].numpy(), ws.beta1, ws.beta2, ws.eps,
                                     ws.lr, grad_dtype=ws.grad_dtype)
@@ -306,17 +306,22 @@ def run_reference(args, w):
         o.freeze()
         return ws, o, sets
 
-    d = min(1 << 21, w.d)
-    ws, o, sets = make(d)
-    t0 = time.perf_counter()
-    o.compress_step(sets[0])  # first warm-up step, also the size probe
-    per = time.perf_counter() - t0
-    while d > (1 << 15) and K * per * 1.1 > budget_s:
-        d //= 2
-        per /= 2
-    if d != ws.d:
+    if args.ref_full:  # the whole workload, no sample (minutes per step and tens of GB of host memory)
+        d = w.d
         ws, o, sets = make(d)
-        o.compress_step(sets[0])
+        Wm = 0
+    else:
+        d = min(1 << 21, w.d)
+        ws, o, sets = make(d)
+        t0 = time.perf_counter()
+        o.compress_step(sets[0])  # first warm-up step, also the size probe
+        per = time.perf_counter() - t0
+        while d > (1 << 15) and K * per * 1.1 > budget_s:
+            d //= 2
+            per /= 2
+        if d != ws.d:
+            ws, o, sets = make(d)
+            o.compress_step(sets[0])
     with pinned_to_core0() as pin:
         for s in range(1, Wm):
             o.compress_step(sets[s % 2])
@@ -327,9 +332,10 @@ def run_reference(args, w):
     value = d * K / total
     ab = algorithmic_bytes(w.n_workers, W.GRAD_BYTES[w.grad_dtype])
     cpu = host_cpu()
-    sample = (f"{ws.name} law, flat d={d} (a sample of the d={w.d} workload), n={ws.n_workers}, "
-              f"{W.DTYPE_NAME[ws.grad_dtype]} grads, {Wm} untimed + {K} timed compression steps, single thread"
-              f"{' pinned to core 0' if pin.pinned else ''}")
+    what = (f"{ws.name}, the whole workload ({ws.n_tensors} tensor(s), d={d})" if args.ref_full else
+            f"{ws.name} law, flat d={d} (a sample of the d={w.d} workload)")
+    sample = (f"{what}, n={ws.n_workers}, {W.DTYPE_NAME[ws.grad_dtype]} grads, {Wm} untimed + {K} timed "
+              f"compression steps, single thread{' pinned to core 0' if pin.pinned else ''}")
     config = workload_config(w, args)
     config["d_sample"] = d  # the elements each timed oracle step processes; value = d_sample / step time
     line = {
@@ -361,6 +367,8 @@ def run_exchange(args, w):
 
     world, rank, local = dist_env()
     n = w.n_workers
+    if args.emulate_ranks:
+        return run_exchange_emulated(args, w, args.emulate_ranks)
     if n % world:
         raise SystemExit(f"--exchange needs the worker count ({n}) to be a multiple of the GPU count ({world})")
     nl, T = n // world, w.n_tensors
@@ -442,6 +450,100 @@ def run_exchange(args, w):
     return 0
 
 
+def run_exchange_emulated(args, w, R):
+    """The multi-GPU form's per-rank work, measured on one GPU: R rank handles run one after another,
+    the all-to-all and the all-gather replaced by the device copies they deliver.  Each rank's kernels
+    (begin: its workers; serve: its shards; end: the update of its full replica) are timed with CUDA
+    events; the copies standing in for the collectives are timed apart and are not a measure of any
+    interconnect.  value = d * steps / (the slowest rank's kernel time): what R GPUs would reach if
+    the exchange were free."""
+    import torch
+
+    import communication_compressed_optimizer_compress_gb300 as ob
+    from communication_compressed_optimizer_compress_gb300 import dist as D
+    from communication_compressed_optimizer_compress_gb300 import workloads as W
+
+    n, T = w.n_workers, w.n_tensors
+    if n % R:
+        raise SystemExit(f"--emulate-ranks needs the worker count ({n}) to be a multiple of R ({R})")
+    nl = n // R
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ob.lib()
+    x0 = W.params(w, dev)
+    src = W.GradSource(w, dev)
+    gsets = [src.grads(s_) for s_ in range(2)]
+    ranks = [D.RankOneBitAdam([t.clone() for t in x0], n, w.warmup_steps, r, R, transport=D.LocalTransport(),
+                              beta1=w.beta1, beta2=w.beta2, eps=w.eps, lr=w.lr,
+                              grad_dtype=W.TORCH_DTYPE[w.grad_dtype]) for r in range(R)]
+    del x0
+    stream = torch.cuda.current_stream()
+
+    def step(s_, timed):
+        g = gsets[s_ % 2]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(3 * R + 2)] if timed else None
+        k = 0
+
+        def mark(i, fn):
+            if timed:
+                ev[i][0].record(stream)
+            fn()
+            if timed:
+                ev[i][1].record(stream)
+        for r, o in enumerate(ranks):
+            mark(k, lambda: o.begin(g[r * nl * T:(r + 1) * nl * T])); k += 1
+        if R > 1:
+            mark(k, lambda: [o.recv.view(R, -1).copy_(torch.stack([ranks[p].send.view(R, -1)[q] for p in range(R)]))
+                             for q, o in enumerate(ranks)])
+        k += 1
+        for o in ranks:
+            mark(k, o.serve); k += 1
+        if R > 1:
+            cat = torch.cat([o.bcast for o in ranks])
+            mark(k, lambda: [o.gathered.copy_(cat) for o in ranks])
+        k += 1
+        for o in ranks:
+            mark(k, o.end); k += 1
+        return ev
+
+    for s_ in range(w.warmup_steps):
+        for o in ranks:
+            ob.OneBitAdam.warmup_step(o, gsets[s_ % 2])
+    for o in ranks:
+        o.freeze_variance()
+    for s_ in range(max(3, args.warmup)):
+        step(s_, False)
+    torch.cuda.synchronize()
+    per_rank = [0.0] * R
+    copies = 0.0
+    records = [step(s_, True) for s_ in range(args.steps)]
+    torch.cuda.synchronize()
+    for ev in records:
+        el = [a.elapsed_time(b) if R > 1 or i not in (R, 2 * R + 1) else 0.0 for i, (a, b) in enumerate(ev)]
+        for r in range(R):
+            per_rank[r] += el[r] + el[R + 1 + r] + el[2 * R + 2 + r]
+        copies += el[R] + el[2 * R + 1]
+    per_rank = [v / args.steps for v in per_rank]
+    status = max(o.get_status() for o in ranks)
+    line = {
+        "metric": METRIC + " (multi-GPU form, per-rank kernels emulated on one GPU)",
+        "value": w.d / (max(per_rank) / 1e3), "unit": "params/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max(per_rank), "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(w, args), parallelism=f"{R} emulated ranks x {nl} workers"),
+        "emulated_ranks": R, "per_rank_kernel_ms": per_rank,
+        "collective_stand_in_copies_ms_per_step": copies / args.steps,
+        "exchange_bytes_per_step_per_rank": ranks[0].exchange_bytes(),
+        "status": ob.error_string(status),
+        "note": "each rank's kernels measured on this GPU one rank at a time; the interconnect time is not "
+                "measured: value and ms_per_step assume the exchange is free",
+    }
+    print(json.dumps(line), flush=True)
+    for o in ranks:
+        o.free()
+    return 0
+
+
 METRIC = "compression-stage optimizer step params/s and HBM GB/s (% of 8 TB/s) at 1 GB300"
 STEP_METRIC = {
     "warmup": "warm-up (uncompressed) Adam step params/s and HBM GB/s at 1 GB300",
@@ -483,6 +585,12 @@ def main():
     ap.add_argument("--scale-block", type=int, default=0,
                     help="per-block scale granularity: every block of this many elements (a multiple of 32) "
                          "gets its own worker scales and server shards; 0 = per tensor")
+    ap.add_argument("--ref-full", action="store_true",
+                    help="with --impl reference: time the oracle on the whole workload instead of a sample")
+    ap.add_argument("--emulate-ranks", type=int, default=0,
+                    help="with --exchange at one GPU: run R ranks' handles one after another on this GPU, the "
+                         "collectives replaced by the device copies they deliver, and report each rank's kernel "
+                         "time (the interconnect is not measured)")
     ap.add_argument("--exchange", action="store_true",
                     help="the multi-GPU form: the n workers split over the ranks (n/N per GPU), the compressed "
                          "messages exchanged with an NCCL all-to-all and all-gather between the library's split "

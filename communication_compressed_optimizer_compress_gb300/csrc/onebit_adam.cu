@@ -1379,7 +1379,8 @@ onebit_status_t onebit_adam_compress_step_host(onebit_adam_t* h, const void* con
   return guarded([&]() -> onebit_status_t {
     NvtxRange trace("onebit_adam_compress_step_host");
     if (!h || !host_grads) return ONEBIT_ERR_INVALID_ARG;
-    if (h->phase != ONEBIT_PHASE_COMPRESS) return ONEBIT_ERR_PHASE;
+    if (h->phase != ONEBIT_PHASE_COMPRESS || h->xstage) return ONEBIT_ERR_PHASE;
+    if (h->plan.world > 1) return ONEBIT_ERR_UNSUPPORTED;  // checked before anything is staged
     DeviceGuard g(h->device);
     std::vector<const void*> dev;
     int idx = 0;
@@ -1522,6 +1523,7 @@ onebit_status_t onebit_adam_import(onebit_adam_t* h, int32_t what, int32_t worke
   return guarded([&]() -> onebit_status_t {
     NvtxRange trace("onebit_adam_import");
     if (!h || !src) return ONEBIT_ERR_INVALID_ARG;
+    if (h->xstage) return ONEBIT_ERR_PHASE;  // not in the middle of a split step
     const Plan& P = h->plan;
     DeviceGuard g(h->device);
     cudaStream_t st = as_stream(stream);

@@ -141,6 +141,10 @@ class HostTransport:
 
 # ---------------------------------------------------------------------------------- the rank optimizer
 
+class ExchangeError(RuntimeError):
+    """A collective of a compression step failed; the step was abandoned (see RankOneBitAdam)."""
+
+
 class RankOneBitAdam(OneBitAdam):
     """Rank `rank` of `world` of the multi-GPU 1-bit Adam step (n_workers a multiple of world).
 
@@ -249,10 +253,43 @@ class RankOneBitAdam(OneBitAdam):
         # the collectives run on the same stream as the library's kernels, so that they are ordered
         with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
             self.begin(local_grads, stream)
-            self.transport.all_to_all(self.recv, self.send)
-            self.serve(stream)
-            self.transport.all_gather(self.gathered, self.bcast)
+            try:
+                self.transport.all_to_all(self.recv, self.send)
+                self.serve(stream)
+                self.transport.all_gather(self.gathered, self.bcast)
+            except Exception as e:  # a peer failed or left: leave the split step, report, keep the handle usable
+                t, phase = self.get_step()
+                self.set_step(t, phase, stream)
+                raise ExchangeError(f"rank {self.rank} of {self.world}: the exchange of compression step {t + 1} "
+                                    f"failed ({e}); the step was abandoned and the optimizer state is not "
+                                    "meaningful: restore it with load_state_dict()") from e
             self.end(stream)
+
+    # ---- checkpoints: this rank's share of the state
+    def state_dict(self, stream=None):
+        """The step count and phase, m, v (den after the freeze), the errors of this rank's workers and
+        the server error of its shards (other elements 0), as fp32 CUDA tensors."""
+        from . import STATE_M, STATE_SERVER_ERROR, STATE_V, STATE_WORKER_ERROR
+
+        t, phase = self.get_step()
+        return {"t": t, "phase": phase, "rank": self.rank, "world": self.world,
+                "m": self.export_state(STATE_M, stream=stream), "v": self.export_state(STATE_V, stream=stream),
+                "server_error": self.export_state(STATE_SERVER_ERROR, stream=stream),
+                "worker_error": {i: self.export_state(STATE_WORKER_ERROR, i, stream=stream)
+                                 for i in range(self.rank * self.nl, (self.rank + 1) * self.nl)}}
+
+    def load_state_dict(self, d, stream=None):
+        """Restore a state_dict() taken on the same rank of the same configuration."""
+        from . import STATE_M, STATE_SERVER_ERROR, STATE_V, STATE_WORKER_ERROR
+
+        if (d.get("rank"), d.get("world")) != (self.rank, self.world):
+            raise ValueError("the checkpoint belongs to another rank or world size")
+        self.set_step(d["t"], d["phase"], stream=stream)
+        self.import_state(STATE_M, d["m"], stream=stream)
+        self.import_state(STATE_V, d["v"], stream=stream)
+        self.import_state(STATE_SERVER_ERROR, d["server_error"], stream=stream)
+        for i, e in d["worker_error"].items():
+            self.import_state(STATE_WORKER_ERROR, e, int(i), stream=stream)
 
     def exchange_bytes(self):
         """Bytes this rank sends per compression step: all-to-all blocks to the other ranks, then its
@@ -261,5 +298,5 @@ class RankOneBitAdam(OneBitAdam):
         return 4 * (w - 1) * (self.send_block + self.bcast_block)
 
 
-__all__ = ["RankOneBitAdam", "DeviceTransport", "HostTransport", "LocalTransport", "plan_exchange",
+__all__ = ["RankOneBitAdam", "ExchangeError", "DeviceTransport", "HostTransport", "LocalTransport", "plan_exchange",
            "workspace_size_rank", "OK", "PHASE_WARMUP"]

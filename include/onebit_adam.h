@@ -331,7 +331,10 @@ onebit_status_t onebit_adam_compress_serve(onebit_adam_t* h, const uint32_t* rec
  * all-gather of every rank's bcast block in rank order) completes the broadcast momentum, and the
  * parameters are updated.  Legal after compress_serve; t += 1.  `send`, `recv`, `bcast` and
  * `gathered` must stay valid until `stream` has passed the call that reads or writes them; with
- * world = 1 they are not touched and may be NULL. */
+ * world = 1 they are not touched and may be NULL.  Between compress_begin and compress_end the
+ * handle is inside a split step: every other step call and every import returns ONEBIT_ERR_PHASE.
+ * A split step that cannot be completed (a collective failed) is abandoned with
+ * onebit_adam_set_step, after which the state is restored from a checkpoint (onebit_adam_import). */
 onebit_status_t onebit_adam_compress_end(onebit_adam_t* h, const uint32_t* gathered, onebit_stream_t stream);
 /* The exchange copies of rank `rank` of `world` (host only): up to `cap` rows of eight int64 {stage
  * (0 begin pack, 1 serve unpack, 2 serve pack, 3 end unpack), source region, source row, source

@@ -222,3 +222,59 @@ def test_two_processes_share_the_gpu(numel, n, dtype):
     import torch.multiprocessing as mp
 
     mp.spawn(_proc_main, args=(2, _free_port(), numel, n, dtype), nprocs=2, join=True)
+
+
+def _leave_main(rank, world, port):
+    import datetime
+    import time
+
+    import torch.distributed as tdist
+
+    tdist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world,
+                             timeout=datetime.timedelta(seconds=15))
+    torch.cuda.set_device(0)
+    n, T = 2, 1
+    w = W.WORKLOADS["tiny"].with_(numel=(50_000,), n_workers=n, warmup_steps=2, seed=431)
+    src = W.GradSource(w, "cpu")
+    o = D.RankOneBitAdam([t.cuda() for t in W.params(w, "cpu")], n, 2, rank, world, transport=D.HostTransport())
+    for step in range(4):
+        local = [t.cuda() for t in src.grads(step)][rank * T:(rank + 1) * T]
+        if step < 2:
+            o.warmup_step(local)
+            continue
+        if step == 2:
+            o.freeze_variance()
+        o.compress_step(local)
+    ckpt = o.state_dict()
+    torch.cuda.synchronize()
+    tdist.barrier()
+    if rank == 1:  # leaves between steps: none of its kernels or collectives in flight
+        o.free()
+        return
+    local = [t.cuda() for t in src.grads(4)][:T]
+    t0 = time.time()
+    with pytest.raises(D.ExchangeError):
+        o.compress_step(local)  # the all-to-all fails: the peer is gone
+    assert time.time() - t0 < 90
+    assert o.get_step() == (ckpt["t"], ob.PHASE_COMPRESS)  # the step did not count
+    o.load_state_dict(ckpt)
+    again = o.state_dict()
+    torch.cuda.synchronize()
+    assert o.get_status() == ob.OK
+    for k in ("m", "v", "server_error"):
+        assert _same(again[k], ckpt[k]), k
+    assert _same(again["worker_error"][0], ckpt["worker_error"][0])
+    o.free()
+    try:
+        tdist.destroy_process_group()
+    except Exception:
+        pass
+
+
+def test_a_rank_that_leaves_is_reported_and_the_state_restores():
+    """Failure detection of the multi-GPU form without a GPU fault: one rank leaves between steps;
+    the other's next step fails in its collective within the process group's timeout, the library
+    leaves the split step (ExchangeError), and the rank's checkpoint restores its state bit for bit."""
+    import torch.multiprocessing as mp
+
+    mp.spawn(_leave_main, args=(2, _free_port()), nprocs=2, join=True)
