@@ -9,9 +9,11 @@ variance freeze.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl gb300|reference]
 
-Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the method's workers
-are simulated inside one GPU, so there is nothing to exchange across GPUs); the timed region is
-bracketed by a barrier and a device synchronisation and the slowest rank's time is reported.
+Under torchrun (N > 1) every rank runs an independent replica of the workload on its own GPU (its n
+workers simulated inside that GPU); the timed region is bracketed by a barrier and a device
+synchronisation and the slowest rank's time is reported.  With --exchange the n workers are instead
+spread over the N GPUs (the multi-GPU form: an all-to-all and an all-gather of the compressed
+messages per step).
 """
 from __future__ import annotations
 

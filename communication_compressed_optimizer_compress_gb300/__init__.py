@@ -1,4 +1,5 @@
-"""GB300-native 1-bit Adam optimizer step (data-parallel hot path, n workers simulated on one GPU).
+"""GB300-native 1-bit Adam optimizer step (data-parallel hot path, n workers simulated on one GPU;
+``dist.RankOneBitAdam`` spreads them over several GPUs).
 
 Thin Python binding over the C ABI in ``include/onebit_adam.h`` (``libonebit_adam.so``, built by
 ``_build.build()``).  Every step of the method runs in the library's CUDA kernels; this module only

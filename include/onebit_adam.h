@@ -11,9 +11,12 @@
  *     1-bit compression through a gather-then-broadcast exchange (Sec. 6 and Sec. 11; AIMech
  *     mechanism "custom compressed allreduce": worker error delta^(i), server error epsilon).
  *
- * All n data-parallel workers are simulated on ONE GPU: worker i's gradient is one of the n
- * gradient buffers passed to a step, and the exchange is index arithmetic over the workers' packed
- * messages in this GPU's memory.  Nothing here communicates across GPUs.
+ * Two forms.  In the single-GPU form (onebit_adam_init) all n data-parallel workers are simulated on
+ * one GPU: worker i's gradient is one of the n gradient buffers passed to a step, and the exchange is
+ * index arithmetic over the workers' packed messages in this GPU's memory.  In the multi-GPU form
+ * (onebit_adam_init_rank, near the end of this file) every GPU holds a share of the workers and of the
+ * server shards, and the caller's collectives carry the packed messages between the library's calls.
+ * The library itself never communicates across GPUs.
  *
  * Per compression step, for every tensor k of the parameter list:
  *   worker i:   m_i = b1*m + (1-b1)*g_i;  c_i = m_i + delta_i;
