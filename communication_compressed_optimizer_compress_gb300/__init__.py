@@ -208,9 +208,10 @@ class OneBitAdam:
         self.h = h
 
     # -------------------------------------------------------------- steps
-    def _grad_array(self, grads, cuda=True):
-        if len(grads) != self.n * self.T:
-            raise ValueError(f"expected {self.n * self.T} gradient tensors, got {len(grads)}")
+    def _grad_array(self, grads, cuda=True, count=None):
+        count = self.n * self.T if count is None else count  # [worker][tensor] pointers of `count` tensors
+        if len(grads) != count:
+            raise ValueError(f"expected {count} gradient tensors, got {len(grads)}")
         arr = (ctypes.c_void_p * len(grads))()
         for q, g in enumerate(grads):
             if g.is_cuda != cuda or not g.is_contiguous() or g.numel() != self.numel[q % self.T]:

@@ -202,21 +202,6 @@ class RankOneBitAdam(OneBitAdam):
     def _local_grad_array(self, grads):
         return self._grad_array(grads, count=self.nl * self.T)
 
-    def _grad_array(self, grads, cuda=True, count=None):
-        from . import _torch_dtype_code
-
-        count = self.n * self.T if count is None else count
-        if len(grads) != count:
-            raise ValueError(f"expected {count} gradient tensors, got {len(grads)}")
-        arr = (ctypes.c_void_p * len(grads))()
-        for q, g in enumerate(grads):
-            if g.is_cuda != cuda or not g.is_contiguous() or g.numel() != self.numel[q % self.T]:
-                raise ValueError(f"gradient {q}: wrong device, layout or size")
-            if _torch_dtype_code(g.dtype) != self.grad_dtype:
-                raise ValueError(f"gradient {q}: dtype {g.dtype} does not match the config")
-            arr[q] = g.data_ptr()
-        return arr
-
     def all_gradients(self, local_grads):
         """Every worker's gradients ([worker][tensor], n*T tensors) from each rank's nl*T: the warm-up's
         uncompressed exchange, as an all-gather."""
