@@ -85,3 +85,34 @@ def test_full_size_chunks(name):
     assert st.scales_exact >= 0.99 * st.scales, st
     assert st.excluded_worker <= 1e-4 * st.worker_draws, st
     p.close()
+
+
+def test_baseline_step_at_the_benchmark_chunk_length():
+    """The gradient-compression baseline ("1-bit Adam ...", Sec. 3.2 and 4.2: error-compensated 1-bit
+    compression of the gradients, then Adam on the broadcast) on the BERT-Large law at 80e6 elements,
+    16 workers, fp16: 65536-element chunks, two baseline steps (without and with error memories), a
+    warm-up step, the freeze and a compression step, every element compared with the oracle."""
+    w = W.WORKLOADS["bert_large"].with_(numel=(80_000_000,), warmup_steps=5)
+    assert _max_chunk(w) == (65536, 65536)
+    p = Pair(w, gen_device="cuda")
+    for _ in range(2):
+        p.ec_adam()
+    p.warmup()
+    p.freeze()
+    p.compress()
+    assert p.stats.scales_exact >= 0.99 * p.stats.scales, p.stats
+    p.close()
+
+
+def test_per_block_scales_at_size():
+    """Per-block scales (the per-chunk parameter-server form of Sec. 11) with 65536-element blocks on
+    the BERT-Large law at 24e6 elements, 16 workers: 4096-element shards, so the worker kernel's
+    chunks each hold several whole shards (and look up each group's own broadcast scale); two
+    compression steps compared element by element with the oracle."""
+    w = W.WORKLOADS["bert_large"].with_(numel=(24_000_011,), warmup_steps=2, compress_steps=2)
+    cfg = ob.make_config(list(w.numel), w.n_workers, w.warmup_steps, grad_dtype=w.grad_dtype, scale_block=65536)
+    assert any(r[5] for r in ob.plan_worker_chunks(cfg))  # chunks spanning several shards
+    p = Pair(w, scale_block=65536, gen_device="cuda")
+    st = p.run()
+    assert st.scales_exact >= 0.99 * st.scales, st
+    p.close()
