@@ -9,7 +9,7 @@
  *   - compression: the variance is frozen as V = diag(sqrt(v_Tw) + eps) (Sec. 3.3 and 5: momentum
  *     SGD with a coordinate-wise learning rate) and momentum is exchanged with error-compensated
  *     1-bit compression through a gather-then-broadcast exchange (Sec. 6 and Sec. 11; AIMech
- *     mechanism "custom compressed allreduce": worker error delta^(i), server error epsilon).
+ *     page's compressed-allreduce mechanism: worker error delta^(i), server error epsilon).
  *
  * Two forms.  In the single-GPU form (onebit_adam_init) all n data-parallel workers are simulated on
  * one GPU: worker i's gradient is one of the n gradient buffers passed to a step, and the exchange is
@@ -156,7 +156,7 @@ onebit_status_t onebit_adam_freeze_variance(onebit_adam_t* h, onebit_stream_t st
 /* One compression-stage step (legal in phase COMPRESS): the three steps of Tang et al. Sec. 11 --
  * every worker updates its momentum and compresses it with error compensation (Sec. 4.1, 4.3; the
  * codewithpapers page's scale), every server shard averages the workers' messages and compresses
- * again with its own error (the AIMech mechanism "custom compressed allreduce"), and the broadcast
+ * again with its own error (the AIMech page's compressed-allreduce mechanism), and the broadcast
  * momentum updates the parameters -- as stated at the top of this file.  grads as for warmup_step.
  * t += 1. */
 onebit_status_t onebit_adam_compress_step(onebit_adam_t* h, const void* const* grads, onebit_stream_t stream);
@@ -225,7 +225,7 @@ onebit_status_t onebit_adam_kernel_times(onebit_adam_t* h, double* ms, int64_t* 
 /* Kernel launches enqueued by this handle since init. */
 onebit_status_t onebit_adam_launch_count(const onebit_adam_t* h, int64_t* launches);
 
-/* Variance-norm monitor ("1-bit Adam ...", Sec. 3.3: the fused variance norm stabilises early in
+/* Variance-norm monitor ("1-bit Adam ...", Sec. 3.3: the variance's norm settles early in
  * training, which is why the variance can be frozen).  While enabled, every warm-up step also
  * computes ||v_t||_2 over the whole parameter list (exact squares, double accumulation) and copies
  * it to a pinned host slot (enabling allocates that slot).  variance_norm() waits for the last

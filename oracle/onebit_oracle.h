@@ -74,7 +74,7 @@ void ora_unpack_signs(const uint32_t* words, int64_t len, float scale, float* ou
 /* scale = ora_rms(c); words = signs of c; err = c - scale * sign(c).  Returns the scale. */
 float ora_compress(const float* c, int64_t len, uint32_t* words, float* err);
 
-/* ||v||_2 in double (exact squares, compensated sum, one sqrt): the "fused variance norm" whose
+/* ||v||_2 in double (exact squares, compensated sum, one sqrt): the norm of the variance whose
  * stabilisation during warm-up motivates freezing the variance ([P1] Sec. 3.3). */
 double ora_norm2(const float* v, int64_t len);
 
