@@ -689,34 +689,39 @@ onebit_status_t run_worker(onebit_adam* h, const StepArgs& A, bool vec, cudaStre
   return he ? run_worker_v<GT, kMomBits, true>(h, A, vec, st) : run_worker_v<GT, kMomBits, false>(h, A, vec, st);
 }
 
+template <bool HE, bool CONTIG>
+onebit_status_t run_server_staged(onebit_adam* h, const StepArgs& A, cudaStream_t st) {
+  // shared-memory staged variant: the tiles of a and the n sign rows arrive by bulk copies; the
+  // common worker counts have their own compile-time instances
+  auto go = [&](auto k) -> onebit_status_t {
+    const size_t dyn = server_dyn_smem(A.n);
+    if (!h->dyn_smem_set.count((const void*)k)) {
+      cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)server_dyn_smem(kStageMaxWorkers));
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute");
+      h->dyn_smem_set.insert((const void*)k);
+    }
+    return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kStagedThreads, A.n_chunks, dyn),
+                  kStagedThreads, st, A, dyn);
+  };
+  switch (A.n) {
+    case 4: return go(k_server_staged<HE, 4, CONTIG>);
+    case 8: return go(k_server_staged<HE, 8, CONTIG>);
+    case 16: return go(k_server_staged<HE, 16, CONTIG>);
+    default: return go(k_server_staged<HE, 0, CONTIG>);
+  }
+}
+
 template <bool HE>
 onebit_status_t run_server_v(onebit_adam* h, const StepArgs& A, cudaStream_t st) {
+  // CONTIG (many short tensors or scale blocks): contiguous runs of chunks, so that the sum tables
+  // are rebuilt once per segment and CTA
+  if (A.n <= kStageMaxWorkers)
+    return A.contig ? run_server_staged<HE, true>(h, A, st) : run_server_staged<HE, false>(h, A, st);
+  // register variant for larger n
   if (A.contig) {
-    // many short tensors: the register variant over contiguous runs of chunks, so that the sum
-    // tables are rebuilt once per tensor and CTA
     auto k = k_server<HE, true>;
     return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
-  }
-  if (A.n <= kStageMaxWorkers) {
-    // shared-memory staged variant: the tiles of a and the n sign rows arrive by bulk copies; the
-    // common worker counts have their own compile-time instances
-    auto go = [&](auto k) -> onebit_status_t {
-      const size_t dyn = server_dyn_smem(A.n);
-      if (!h->dyn_smem_set.count((const void*)k)) {
-        cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)server_dyn_smem(kStageMaxWorkers));
-        if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute");
-        h->dyn_smem_set.insert((const void*)k);
-      }
-      return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kStagedThreads, A.n_chunks, dyn),
-                    kStagedThreads, st, A, dyn);
-    };
-    switch (A.n) {
-      case 4: return go(k_server_staged<HE, 4>);
-      case 8: return go(k_server_staged<HE, 8>);
-      case 16: return go(k_server_staged<HE, 16>);
-      default: return go(k_server_staged<HE, 0>);
-    }
   }
   auto k = k_server<HE, false>;
   return launch(h, ONEBIT_K_SERVER, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);

@@ -183,25 +183,10 @@ __device__ __forceinline__ double block_sum(double v, double* red) {
   return r;  // valid in thread 0
 }
 
-// The same fixed-order reduction, its result returned to every thread (red: NT/32 + 1 slots).
-template <int NT>
-__device__ __forceinline__ double block_sum_all(double v, double* red) {
-  v = warp_sum(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    double r = lane < NT / 32 ? red[lane] : 0.0;
-    r = warp_sum(r);
-    if (lane == 0) red[NT / 32] = r;
-  }
-  __syncthreads();
-  return red[NT / 32];
-}
-
 // Sum of squares without rounding error at the element level: c*c = p + pe exactly (FMA), p is
 // added to the running fp32 sum with an exact two-sum, and the two error terms are collected in a
-// second fp32 word.  (hi, lo) carries ~44 bits; it is promoted to double once per work unit.  This
+// second fp32 word.  (hi, lo) carries ~44 bits; the block sums the pairs as pairs (below) and promotes
+// one total to double per work unit.  This
 // keeps the scales equal to a double-precision evaluation (1 ulp at most, almost always 0) without
 // using the GPU's slow fp64 pipe per element.  Written with Blackwell's packed fp32x2 arithmetic for
 // two elements at once: (hi, lo) hold two independent (hi, lo) accumulators, one per half.
@@ -223,9 +208,62 @@ __device__ __forceinline__ void add_square2(unsigned long long& hi, unsigned lon
       : "+l"(hi), "+l"(lo)
       : "f"(c0), "f"(c1));
 }
-__device__ __forceinline__ double square_total(unsigned long long hi, unsigned long long lo) {
-  return ((double)__uint_as_float((uint32_t)hi) + (double)__uint_as_float((uint32_t)(hi >> 32))) +
-         ((double)__uint_as_float((uint32_t)lo) + (double)__uint_as_float((uint32_t)(lo >> 32)));
+
+// The threads' (hi, lo) accumulators are summed across the block as fp32 pairs too: s + e, where s
+// takes each addition's rounded sum and e collects its exact rounding error (two-sum) along with the
+// error words.  Only the block's final pair is promoted to double, once per unit: the GPU's fp64
+// pipe is slow (about two operations per clock and SM), and a double reduction over every thread
+// held it for over a thousand cycles per unit.  Each pair addition is symmetric in its operands, so
+// the butterfly leaves the same value in every lane; e's own roundings stay below 2^-40 of the total.
+struct SqPair {
+  float s, e;
+};
+__device__ __forceinline__ SqPair sq_add(SqPair a, SqPair b) {
+  const float s = __fadd_rn(a.s, b.s);
+  const float bb = __fsub_rn(s, a.s);
+  const float err = __fadd_rn(__fsub_rn(a.s, __fsub_rn(s, bb)), __fsub_rn(b.s, bb));  // a.s + b.s - s, exactly
+  return {s, __fadd_rn(__fadd_rn(a.e, b.e), err)};
+}
+// this thread's two (hi, lo) halves as one pair
+__device__ __forceinline__ SqPair sq_of(unsigned long long hi, unsigned long long lo) {
+  return sq_add({__uint_as_float((uint32_t)hi), __uint_as_float((uint32_t)lo)},
+                {__uint_as_float((uint32_t)(hi >> 32)), __uint_as_float((uint32_t)(lo >> 32))});
+}
+// butterfly over the first W lanes of the warp (W a power of two; the others hold zeros or are ignored)
+template <int W>
+__device__ __forceinline__ SqPair warp_sq(SqPair p) {
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1)
+    p = sq_add(p, {__shfl_xor_sync(0xffffffffu, p.s, o), __shfl_xor_sync(0xffffffffu, p.e, o)});
+  return p;
+}
+__device__ __forceinline__ double sq_value(SqPair p) { return (double)p.s + (double)p.e; }
+
+// Fixed-order block total of the threads' pairs: the warps' butterflies, then warp 0 over the warp
+// totals (red: NT/32 slots of 8 bytes at least).  In thread 0 (block_sq) or every thread
+// (block_sq_all, red: NT/32 + 1 slots).
+template <int NT>
+__device__ __forceinline__ double block_sq(SqPair p, double* red) {
+  static_assert(NT % 32 == 0 && ((NT / 32) & (NT / 32 - 1)) == 0, "a power-of-two number of warps");
+  float2* r2 = reinterpret_cast<float2*>(red);
+  p = warp_sq<32>(p);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) r2[warp] = make_float2(p.s, p.e);
+  __syncthreads();
+  double r = 0.0;
+  if (warp == 0) {
+    const float2 v = lane < NT / 32 ? r2[lane] : make_float2(0.0f, 0.0f);
+    r = sq_value(warp_sq<NT / 32>({v.x, v.y}));
+  }
+  __syncthreads();
+  return r;
+}
+template <int NT>
+__device__ __forceinline__ double block_sq_all(SqPair p, double* red) {
+  const double r = block_sq<NT>(p, red);
+  if (threadIdx.x == 0) red[NT / 32] = r;
+  __syncthreads();
+  return red[NT / 32];
 }
 
 // Range of the fp32-pair accumulation.  Each square is exact for |c| >= 2^-51 (below that its
@@ -270,7 +308,7 @@ __device__ __forceinline__ double unit_squares_fp64(const float* v, int len, dou
 template <int NT>
 __device__ __forceinline__ double unit_squares(unsigned long long hi, unsigned long long lo, const float* v, int len,
                                                double* red) {
-  const double tot = block_sum_all<NT>(square_total(hi, lo), red);
+  const double tot = block_sq_all<NT>(sq_of(hi, lo), red);
   return squares_inexact(tot) ? unit_squares_fp64<NT>(v, len, red) : tot;
 }
 
@@ -418,7 +456,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       }
       wb[ng] = (uint8_t)byte;
     }
-    const double tot = block_sum<kThreads>(square_total(hi, lo), red);
+    const double tot = block_sq<kThreads>(sq_of(hi, lo), red);
     if (threadIdx.x == 0) A.wpart[(int64_t)il * A.n_wchunks + ci] = tot;
   }
 }
@@ -661,8 +699,8 @@ __device__ __forceinline__ void store_a(float* a, int64_t e, int cnt, const floa
 }
 
 // Which chunks a server CTA takes.  Normally every gridDim.x-th chunk.  For lists of many short
-// tensors (CONTIG, register variant only) one contiguous run instead, so that consecutive chunks of a
-// tensor share one CTA and its sum tables are rebuilt once per tensor and CTA, not once per chunk;
+// tensors or scale blocks (CONTIG) one contiguous run instead, so that consecutive chunks of a
+// segment share one CTA and its sum tables are rebuilt once per segment and CTA, not once per chunk;
 // the runs split the elements evenly (the first chunk whose element offset reaches b*D/gridDim.x).
 __device__ __forceinline__ int run_begin(const StepArgs& A, int b) {
   if (b >= (int)gridDim.x) return A.n_chunks;
@@ -790,16 +828,18 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 }
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory"); }
 
-// The consumer warps' fixed-order sum of one double per consumer thread, left in red[kConsumerWarps]
-// (red: kConsumerWarps + 1 slots at least).  *redo is set when that total lies outside the exact range of the
-// fp32-pair squares and the block has not aborted.
-__device__ __forceinline__ void consumers_total(double v, double* red, int* redo, const volatile int* abort) {
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+// The consumer warps' fixed-order total of the consumer threads' squares (the pair reduction of
+// block_sq), left in red[kConsumerWarps] (red: kConsumerWarps + 1 slots at least).  *redo is set when
+// that total lies outside the exact range of the fp32-pair squares and the block has not aborted.
+__device__ __forceinline__ void consumers_total(SqPair p, double* red, int* redo, const volatile int* abort) {
+  static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "a power-of-two number of consumer warps");
+  float2* r2 = reinterpret_cast<float2*>(red);
+  p = warp_sq<32>(p);
+  if ((threadIdx.x & 31) == 0) r2[threadIdx.x >> 5] = make_float2(p.s, p.e);
   consumers_sync();
   if (threadIdx.x < 32) {
-    double r = threadIdx.x < kConsumerWarps ? red[threadIdx.x] : 0.0;
-    r = warp_sum(r);
+    const float2 v = threadIdx.x < kConsumerWarps ? r2[threadIdx.x] : make_float2(0.0f, 0.0f);
+    const double r = sq_value(warp_sq<kConsumerWarps>({v.x, v.y}));
     if (threadIdx.x == 0) {
       red[kConsumerWarps] = r;
       *redo = squares_inexact(r) && !*abort;
@@ -851,8 +891,9 @@ __device__ __forceinline__ void build_server_tables_consumers(ServerTables& S, c
 
 // NW > 0: compiled for exactly NW workers (the common counts), so that the per-element worker checks,
 // the sign-byte loads and the division by n fold at compile time; NW = 0: any n up to
-// kStageMaxWorkers.  Both compute the same values.
-template <bool HAS_ERR, int NW>
+// kStageMaxWorkers.  Both compute the same values.  CONTIG: the block walks one contiguous run of
+// chunks (run_begin) instead of every gridDim.x-th chunk; the values do not depend on the walk.
+template <bool HAS_ERR, int NW, bool CONTIG>
 __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepArgs A) {
   __shared__ ServerTables S;
   __shared__ volatile int abort_flag;
@@ -875,6 +916,12 @@ __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepA
   }
   __syncthreads();
 
+  // this block's chunks: every gridDim.x-th from blockIdx.x, or (CONTIG) the run from
+  // run_begin(blockIdx.x) up to u_end.  The strided walk reads its first chunk inside each role's
+  // branch and its bound and stride from the launch parameters: the same bounds read once before
+  // the branch cost the per-tensor kernel 2%, measured.
+  const int u_end = CONTIG ? run_begin(A, blockIdx.x + 1) : 0;
+  auto in_walk = [&](int u) { return CONTIG ? u < u_end : u < A.n_chunks; };
   // a cursor over this block's (chunk, tile) sequence that keeps the current chunk's descriptor in
   // registers, so that it is read from memory once per chunk rather than at every tile
   struct Cur {
@@ -882,7 +929,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepA
     Chunk ch;
   };
   auto load = [&](Cur& c) {
-    if (c.u < A.n_chunks) {
+    if (in_walk(c.u)) {
       c.ch = A.chunks[c.u];
       c.nt = tiles_of(c.ch);
     }
@@ -890,7 +937,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepA
   auto advance = [&](Cur& c) {
     if (++c.t >= c.nt) {
       c.t = 0;
-      c.u += gridDim.x;
+      c.u += CONTIG ? 1 : (int)gridDim.x;
       load(c);
     }
   };
@@ -898,10 +945,10 @@ __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepA
   if (threadIdx.x >= kThreads) {
     // ---------------- producer warp (one elected lane issues the copies)
     if (threadIdx.x != kThreads) return;
-    Cur c{(int)blockIdx.x, 0, 0, {}};
+    Cur c{CONTIG ? run_begin(A, blockIdx.x) : (int)blockIdx.x, 0, 0, {}};
     load(c);
     int j = 0;
-    for (; c.u < A.n_chunks; ++j, advance(c)) {
+    for (; in_walk(c.u); ++j, advance(c)) {
       const int st = j % kStages;
       if (j >= kStages && !abort_flag && !mbar_wait(&empty[st], (uint32_t)((j / kStages - 1) & 1))) {
         atomicOr(A.status, 2u);
@@ -936,12 +983,12 @@ __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepA
 
   // ---------------- consumer warps
   const int lane = threadIdx.x & 31;
-  Cur cons{(int)blockIdx.x, 0, 0, {}};
+  Cur cons{CONTIG ? run_begin(A, blockIdx.x) : (int)blockIdx.x, 0, 0, {}};
   load(cons);
   int k = 0;
   int cur_seg = -1;
   unsigned long long hi = 0, lo = 0;
-  while (cons.u < A.n_chunks) {
+  while (in_walk(cons.u)) {
     const Chunk ch = cons.ch;
     if (cons.t == 0 && ch.seg != cur_seg) {
       build_server_tables_consumers(S, A, ch.seg);
@@ -1000,7 +1047,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepA
     const int u_done = cons.u;
     advance(cons);
     if (last_tile) {  // chunk total among the consumers (fixed order)
-      consumers_total(square_total(hi, lo), S.red, &redo_squares, &abort_flag);
+      consumers_total(sq_of(hi, lo), S.red, &redo_squares, &abort_flag);
       if (redo_squares && threadIdx.x < 32) {  // outside the exact range: warp 0 sums the chunk again in double
         const Chunk cd = A.chunks[u_done];  // reloaded: keeping the descriptor live costs registers
         const double r = warp_sum(squares_fp64(A.a + cd.off, cd.len, threadIdx.x, 32));
@@ -1435,7 +1482,7 @@ __global__ void __launch_bounds__(kStagedThreads) k_warmup_staged(const StepArgs
     const int u_done = cons.u;
     advance(cons);
     if (MON && last_tile) {  // chunk total of v^2 among the consumers (fixed order)
-      consumers_total(square_total(vhi, vlo), red, &redo_squares, &abort_flag);
+      consumers_total(sq_of(vhi, vlo), red, &redo_squares, &abort_flag);
       if (redo_squares && threadIdx.x < 32) {  // outside the exact range: warp 0 sums the chunk again in double
         const Chunk cd = A.chunks[u_done];
         const double r = warp_sum(squares_fp64(A.v + cd.off, cd.len, threadIdx.x, 32));

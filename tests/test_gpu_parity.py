@@ -44,8 +44,9 @@ def test_odd_sizes(numel, n, dtype):
     """Ragged tensors, tails that are not a multiple of 8 or 32, empty tensors and shards, several
     chunks per shard, worker counts that are not powers of two, all gradient dtypes.  The worker
     counts cover the server's paths: table only (n <= 12), table + ordered float4 adds (13..16),
-    further workers added one by one (17..128, staged kernel), the register kernel (129..256, one
-    flat buffer; and short-tensor lists at any n), and the library's maximum n = 256."""
+    further workers added one by one (17..128, staged kernel, strided or over contiguous runs for
+    short-tensor lists), the register kernel (129..256, strided on one flat buffer, contiguous runs on
+    short-tensor lists), and the library's maximum n = 256."""
     w = _tiny(numel=tuple(numel), n_workers=n, grad_dtype=dtype, warmup_steps=2, compress_steps=3,
               seed=7 + n + len(numel))
     p = Pair(w)

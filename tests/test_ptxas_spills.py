@@ -1,6 +1,6 @@
 """Register spills in the CUDA kernels, from ptxas's own per-kernel summary (-Xptxas -v): the kernels
 on the timed path must not spill.  The one known exception is allowed, with its current size as the
-ceiling: the register variant of the server kernel (contiguous-run plans and n > 128), a few bytes.
+ceiling: the register variant of the server kernel (n > 128 only), a few bytes.
 No GPU needed: nvcc compiles for sm_103a here."""
 import os
 import re
