@@ -276,11 +276,13 @@ def test_allocation_failure_is_reported_and_changes_nothing():
 
 
 @pytest.mark.parametrize("numel,n,dtype", [((300_000,), 16, W.F16), ((70_001, 33, 0, 5, 4096), 16, W.F16),
-                                           ((50_000, 7), 33, W.BF16)],
-                         ids=["flat_n16_staged", "ragged_n16_runs", "n33_register"])
+                                           ((50_000, 7), 33, W.BF16), ((60_000,), 129, W.F16)],
+                         ids=["flat_n16_staged", "ragged_n16_runs", "n33_runs", "n129_register"])
 def test_results_do_not_depend_on_the_grid(numel, n, dtype):
     """The same schedule with every streaming launch capped at 1, 7 or 152 CTAs, or uncapped, leaves
-    bit-identical state: partial sums are per chunk and reduced in a fixed order, whatever the grid."""
+    bit-identical state: partial sums are per chunk and reduced in a fixed order, whatever the grid.
+    The cases reach the staged server's strided walk, its walk over contiguous runs (whose split
+    depends on the grid), and the register server (n > 128)."""
     w = _tiny(numel=numel, n_workers=n, grad_dtype=dtype, warmup_steps=2, seed=151)
     src = W.GradSource(w, "cpu")
     g = [[t.cuda() for t in src.grads(s)] for s in range(5)]
