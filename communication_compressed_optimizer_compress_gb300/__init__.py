@@ -12,14 +12,19 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libonebit_adam.so")
+# ONEBIT_LIBRARY=checked selects the checked build (kernels check their units of work against their
+# buffers and report, instead of touching, any that would leave them); it is built on request by
+# _build.build(checked=True)
+CHECKED = os.environ.get("ONEBIT_LIBRARY", "") == "checked"
+LIB_PATH = os.path.join(_HERE, "libonebit_adam_checked.so" if CHECKED else "libonebit_adam.so")
 
-OK, ERR_INVALID_ARG, ERR_PHASE, ERR_CUDA, ERR_NOMEM, ERR_WORKSPACE, ERR_NONFINITE, ERR_UNSUPPORTED = range(8)
+(OK, ERR_INVALID_ARG, ERR_PHASE, ERR_CUDA, ERR_NOMEM, ERR_WORKSPACE, ERR_NONFINITE, ERR_UNSUPPORTED,
+ ERR_BOUNDS) = range(9)
 F32, F16, BF16 = 0, 1, 2
 PHASE_WARMUP, PHASE_COMPRESS = 0, 1
 (STATE_M, STATE_V, STATE_WORKER_ERROR, STATE_SERVER_ERROR, STATE_WORKER_BITS, STATE_SERVER_BITS,
  STATE_WORKER_SCALES, STATE_SERVER_SCALES) = range(8)
-FAULT_NONE, FAULT_STALL_COPIES, FAULT_FAIL_ALLOC = 0, 1, 2
+FAULT_NONE, FAULT_STALL_COPIES, FAULT_FAIL_ALLOC, FAULT_TIGHTEN_BOUNDS = 0, 1, 2, 3
 KERNEL_NAMES = ["warmup", "freeze", "worker", "worker_scale", "server", "server_scale", "update", "export",
                 "ec_update", "exchange"]
 NUM_KERNELS = len(KERNEL_NAMES)
@@ -60,7 +65,9 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(
                 f"CUDA library {LIB_PATH} is missing: build it with "
-                "`python -c 'import __graft_entry__ as g; g.build()'`")
+                + ("`python -c 'from communication_compressed_optimizer_compress_gb300 import _build; "
+                   "_build.build(checked=True)'`" if CHECKED else
+                   "`python -c 'import __graft_entry__ as g; g.build()'`"))
         L = ctypes.CDLL(LIB_PATH)
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         cfgp = ctypes.POINTER(Config)

@@ -397,6 +397,7 @@ struct onebit_adam {
   std::unordered_map<const void*, int> occupancy;
   std::unordered_set<const void*> dyn_smem_set;  // kernels whose dynamic shared-memory limit is raised
   uint32_t stall_tx = 0;  // fault injection (see onebit_adam_set_fault_injection)
+  int64_t check_margin = 0;  // checked builds: padded elements the bounds checks withhold (test hook)
   int fail_allocs = 0;    // allocations still to refuse (fault injection)
   int max_ctas = 0;       // cap on the CTAs of a streaming launch (0: fill the GPU)
   // variance-norm monitor (warm-up)
@@ -575,6 +576,9 @@ StepArgs base_args(onebit_adam* h) {
   A.stall_tx = h->stall_tx;
   A.nl = P.nl;
   A.w0 = P.w0;
+#ifdef ONEBIT_CHECKS
+  A.check_margin = h->check_margin;
+#endif
   return A;
 }
 
@@ -898,6 +902,15 @@ onebit_status_t run_exchange_copy(onebit_adam* h, int stage, const void* buf, cu
   X.base[2] = h->at<uint32_t>(h->lay.sbits);
   X.base[3] = reinterpret_cast<uint32_t*>(h->at<float>(h->lay.sscale) + cur * nt);
   X.base[4] = const_cast<uint32_t*>(static_cast<const uint32_t*>(buf));
+#ifdef ONEBIT_CHECKS
+  const Plan& P = h->plan;
+  X.words[0] = (int64_t)P.n * P.Wr;
+  X.words[1] = (int64_t)nt;
+  X.words[2] = P.Wp;
+  X.words[3] = (int64_t)nt;
+  X.words[4] = stage == 2 ? P.xbcast : (int64_t)P.world * (stage < 2 ? P.xsend : P.xbcast);
+  X.status = h->at<unsigned int>(h->lay.status);
+#endif
   return launch(h, ONEBIT_K_EXCHANGE, k_exchange_copy, grid_for(h, (const void*)k_exchange_copy, kThreads, X.n),
                 kThreads, st, X);
 }
@@ -962,6 +975,13 @@ onebit_status_t run_export(onebit_adam* h, int kind, const float* src, const uin
   X.bits = bits;
   X.scales = scales;
   X.dst = dst;
+#ifdef ONEBIT_CHECKS
+  X.Dp = h->plan.Dp;
+  X.D = h->plan.D;
+  // the callers pass either a whole [T][n] server-scale buffer (shard_mul 1) or one worker's T scales
+  X.n_scales = shard_mul ? (int64_t)h->plan.n * h->plan.T : h->plan.T;
+  X.status = h->at<unsigned int>(h->lay.status);
+#endif
   return launch(h, ONEBIT_K_EXPORT, k_export, grid_for(h, (const void*)k_export, kThreads, X.n_chunks), kThreads, st, X);
 }
 
@@ -1089,6 +1109,7 @@ const char* onebit_adam_error_string(onebit_status_t s) {
     case ONEBIT_ERR_WORKSPACE: return "workspace too small or misaligned";
     case ONEBIT_ERR_NONFINITE: return "non-finite scale (NaN or Inf in the gradients or state)";
     case ONEBIT_ERR_UNSUPPORTED: return "unsupported request";
+    case ONEBIT_ERR_BOUNDS: return "a bounds check of the checked build failed";
   }
   return "unknown status";
 }
@@ -1415,6 +1436,15 @@ onebit_status_t onebit_adam_get_status(onebit_adam_t* h, onebit_stream_t stream)
     cudaStream_t st = as_stream(stream);
     ONEBIT_CUDA(h, cudaMemcpyAsync(&flag, h->ws + h->lay.status, sizeof flag, cudaMemcpyDeviceToHost, st));
     ONEBIT_CUDA(h, cudaStreamSynchronize(st));
+    if (flag & kStatusBounds) {  // checked builds only
+      static const char* names[ONEBIT_NUM_KERNELS] = {"warmup", "freeze", "worker", "worker_scale", "server",
+                                                      "server_scale", "update", "export", "ec_update", "exchange"};
+      std::string which;
+      for (int k = 0; k < ONEBIT_NUM_KERNELS; ++k)
+        if (flag & (1u << (8 + k))) which += (which.empty() ? "" : ", ") + std::string(names[k]);
+      h->last_error = "a bounds check skipped work in: " + which;
+      return ONEBIT_ERR_BOUNDS;
+    }
     if (flag & 2u) {
       h->last_error = "a kernel's wait for its asynchronous copies timed out";
       return ONEBIT_ERR_CUDA;
@@ -1662,6 +1692,7 @@ onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, 
     case ONEBIT_FAULT_NONE:
       h->stall_tx = 0;
       h->fail_allocs = 0;
+      h->check_margin = 0;
       return ONEBIT_OK;
     case ONEBIT_FAULT_STALL_COPIES:
       if (value < 1 || value > (1 << 20)) return ONEBIT_ERR_INVALID_ARG;
@@ -1671,6 +1702,14 @@ onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, 
       if (value < 1 || value > 1000) return ONEBIT_ERR_INVALID_ARG;
       h->fail_allocs = (int)value;
       return ONEBIT_OK;
+    case ONEBIT_FAULT_TIGHTEN_BOUNDS:
+#ifdef ONEBIT_CHECKS
+      if (value < 1 || value % 32 || value > h->plan.Dp) return ONEBIT_ERR_INVALID_ARG;
+      h->check_margin = value;
+      return ONEBIT_OK;
+#else
+      return ONEBIT_ERR_UNSUPPORTED;  // a normal build has no bounds checks to tighten
+#endif
     default: return ONEBIT_ERR_INVALID_ARG;
   }
 }

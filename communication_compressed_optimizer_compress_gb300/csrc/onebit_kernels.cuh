@@ -99,7 +99,67 @@ struct StepArgs {
   int64_t D;                 // elements (unpadded)
   int32_t nl;                // workers whose momentum this launch compresses (all n, or one rank's share)
   int32_t w0;                // the first of them: global workers w0 .. w0+nl-1 (c, wpart and gptr rows 0..nl-1)
+#ifdef ONEBIT_CHECKS
+  int64_t check_margin;      // test hook: padded elements the checks withhold from the end of the rows
+#endif
 };
+
+// ------------------------------------------------------------------------------------------------
+// Checked builds (compiled with -DONEBIT_CHECKS).  Before a kernel touches a unit of work (a chunk,
+// a scale, an exchange range) it checks that the unit's descriptor keeps every access of the unit
+// inside its buffers: the padded state rows in whole 32-element words (as the bulk copies read them),
+// the caller's tensors, the sign rows, and the tensor, shard, worker and partial tables.  A unit that
+// fails is skipped -- all threads of the block or warp that share it skip it together -- and the
+// status word records it: bit 2, and bit 8 + the kernel's number (onebit_kernel_t).  Nothing traps.
+// In normal builds the checks expand to nothing.
+
+constexpr unsigned int kStatusBounds = 4u;
+
+#ifdef ONEBIT_CHECKS
+static __device__ __noinline__ void bounds_fail(unsigned int* status, int kernel) {
+  atomicOr(status, kStatusBounds | (1u << (8 + kernel)));
+}
+// a chunk of the state: whole words inside the padded rows (less the test hook's margin), a valid
+// tensor and shard, and its elements inside that tensor's caller buffers
+__device__ __forceinline__ bool chunk_ok(const StepArgs& A, const Chunk& ch) {
+  return ch.len > 0 && ch.len <= kChunk && ch.off >= 0 && (ch.off & 31) == 0 &&
+         ch.off + ((ch.len + 31) & ~31) <= A.Dp - A.check_margin && ch.seg >= 0 && ch.seg < A.T &&
+         ch.shard >= 0 && ch.shard < A.n && ch.start >= 0 && ch.start + ch.len <= A.wseg_ranges[ch.seg].len;
+}
+// a worker unit: its chunk, the shards its groups look up, and its worker row
+__device__ __forceinline__ bool worker_unit_ok(const StepArgs& A, const Chunk& ch, int il) {
+  return chunk_ok(A, ch) && ch.per >= 0 && (ch.per == 0 || ch.shard + (ch.len - 1) / ch.per < A.n) && il >= 0 &&
+         il < A.nl && A.w0 >= 0 && A.w0 + il < A.n;
+}
+// a run of partials inside a table of `parts`
+__device__ __forceinline__ bool range_ok(const Range& r, int64_t parts) {
+  return r.first >= 0 && r.count >= 0 && (int64_t)r.first + r.count <= parts && r.len >= 0;
+}
+// inside a loop over units: skip this one
+#define ONEBIT_CHECK_UNIT(ok, status, kernel) \
+  if (!(ok)) {                                \
+    ::onebit::bounds_fail(status, kernel);    \
+    continue;                                 \
+  }
+// one item per thread group: give it up
+#define ONEBIT_CHECK_ITEM(ok, status, kernel) \
+  if (!(ok)) {                                \
+    ::onebit::bounds_fail(status, kernel);    \
+    return;                                   \
+  }
+// the staged kernels' chunk cursors: every role of the block moves its cursor past the same failing
+// chunks (u, u + step, ... below end), so that the roles stay in step
+__device__ __forceinline__ int skip_bad_chunks(const StepArgs& A, int u, int end, int step, int kernel) {
+  for (; u < end && !chunk_ok(A, A.chunks[u]); u += step)
+    if (threadIdx.x == 0) bounds_fail(A.status, kernel);
+  return u;
+}
+#define ONEBIT_SKIP_BAD_CHUNKS(u, end, step, kernel) u = ::onebit::skip_bad_chunks(A, u, end, step, kernel)
+#else
+#define ONEBIT_CHECK_UNIT(ok, status, kernel)
+#define ONEBIT_CHECK_ITEM(ok, status, kernel)
+#define ONEBIT_SKIP_BAD_CHUNKS(u, end, step, kernel)
+#endif
 
 // ------------------------------------------------------------------------------------------------
 // memory helpers (inline PTX): 256-bit accesses for fp32 state, 128-bit for 16-bit gradients.
@@ -362,6 +422,7 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
     const int il = (int)(u - (int64_t)ci * A.nl);  // local worker; global worker i
     const int i = A.w0 + il;
     const Chunk ch = A.wchunks[ci];
+    ONEBIT_CHECK_UNIT(worker_unit_ok(A, ch, il), A.status, ONEBIT_K_WORKER)
     const GT* __restrict__ g = static_cast<const GT*>(A.gptr[(int64_t)il * A.T + ch.seg]) + ch.start;
     float* __restrict__ c = A.c + (int64_t)il * A.Dp + ch.off;
     uint8_t* __restrict__ wb = reinterpret_cast<uint8_t*>(A.wbits + (int64_t)i * A.Wr) + (ch.off >> 3);
@@ -481,6 +542,7 @@ static __global__ void __launch_bounds__(kThreads) k_worker_exact(const StepArgs
       const int64_t qq = base + found[f];
       const int il = (int)(qq / A.n_wchunks), ci = (int)(qq - (int64_t)il * A.n_wchunks);
       const Chunk ch = A.wchunks[ci];
+      ONEBIT_CHECK_UNIT(worker_unit_ok(A, ch, il), A.status, ONEBIT_K_WORKER_SCALE)
       const double tot = unit_squares_fp64<kThreads>(A.c + (int64_t)il * A.Dp + ch.off, ch.len, red);
       if (threadIdx.x == 0) A.wpart[qq] = tot;
     }
@@ -509,12 +571,16 @@ __device__ __forceinline__ float finish_scale(const double* part, const Range r,
 static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale(const StepArgs A) {
   __shared__ double red[kScaleThreads / 32];
   const int il = blockIdx.x / A.T, k = blockIdx.x % A.T;
+  ONEBIT_CHECK_ITEM(range_ok(A.wseg_ranges[k], A.n_wchunks) && il < A.nl && A.w0 + il < A.n, A.status,
+                    ONEBIT_K_WORKER_SCALE)
   const float s = finish_scale(A.wpart + (int64_t)il * A.n_wchunks, A.wseg_ranges[k], A.status, red);
   if (threadIdx.x == 0) A.wscale_cur[(int64_t)A.w0 * A.T + blockIdx.x] = s;
 }
 
 static __global__ void __launch_bounds__(kScaleThreads) k_server_scale(const StepArgs A) {
   __shared__ double red[kScaleThreads / 32];
+  ONEBIT_CHECK_ITEM(range_ok(A.shard_ranges[blockIdx.x], A.n_chunks) && (int)blockIdx.x < A.n * A.T, A.status,
+                    ONEBIT_K_SERVER_SCALE)
   const float s = finish_scale(A.spart, A.shard_ranges[blockIdx.x], A.status, red);
   if (threadIdx.x == 0) A.sscale_cur[blockIdx.x] = s;
 }
@@ -540,6 +606,7 @@ static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale_warp(cons
   const int item = blockIdx.x * (kScaleThreads / 32) + (threadIdx.x >> 5);
   if (item >= A.nl * A.T) return;  // the whole warp
   const int il = item / A.T, k = item % A.T;
+  ONEBIT_CHECK_ITEM(range_ok(A.wseg_ranges[k], A.n_wchunks) && A.w0 + il < A.n, A.status, ONEBIT_K_WORKER_SCALE)
   const float s = finish_scale_warp(A.wpart + (int64_t)il * A.n_wchunks, A.wseg_ranges[k], A.status);
   if ((threadIdx.x & 31) == 0) A.wscale_cur[(int64_t)A.w0 * A.T + item] = s;
 }
@@ -547,6 +614,7 @@ static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale_warp(cons
 static __global__ void __launch_bounds__(kScaleThreads) k_server_scale_warp(const StepArgs A) {
   const int item = blockIdx.x * (kScaleThreads / 32) + (threadIdx.x >> 5);
   if (item >= A.n * A.T) return;
+  ONEBIT_CHECK_ITEM(range_ok(A.shard_ranges[item], A.n_chunks), A.status, ONEBIT_K_SERVER_SCALE)
   const float s = finish_scale_warp(A.spart, A.shard_ranges[item], A.status);
   if ((threadIdx.x & 31) == 0) A.sscale_cur[item] = s;
 }
@@ -730,6 +798,7 @@ __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
   }
   for (int u = u_begin; u < u_end; u += u_step) {
     const Chunk ch = A.chunks[u];
+    ONEBIT_CHECK_UNIT(chunk_ok(A, ch), A.status, ONEBIT_K_SERVER)
     if (ch.seg != cur_seg) {  // block-uniform
       build_server_tables(S, A, ch.seg);
       cur_seg = ch.seg;
@@ -929,6 +998,7 @@ __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepA
     Chunk ch;
   };
   auto load = [&](Cur& c) {
+    ONEBIT_SKIP_BAD_CHUNKS(c.u, CONTIG ? u_end : A.n_chunks, CONTIG ? 1 : (int)gridDim.x, ONEBIT_K_SERVER);
     if (in_walk(c.u)) {
       c.ch = A.chunks[c.u];
       c.nt = tiles_of(c.ch);
@@ -1067,6 +1137,7 @@ __global__ void __launch_bounds__(kThreads) k_update(const StepArgs A) {
   const float lr = A.lr;
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
     const Chunk ch = A.chunks[u];
+    ONEBIT_CHECK_UNIT(chunk_ok(A, ch), A.status, ONEBIT_K_UPDATE)
     const float S = A.sscale_cur[(int64_t)ch.seg * A.n + ch.shard];
     float* __restrict__ x = A.pptr[ch.seg] + ch.start;
     const float* __restrict__ den = A.v + ch.off;
@@ -1128,6 +1199,7 @@ template <bool BC, bool VEC>
 __global__ void __launch_bounds__(kThreads) k_ec_adam_update(const StepArgs A) {
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
     const Chunk ch = A.chunks[u];
+    ONEBIT_CHECK_UNIT(chunk_ok(A, ch), A.status, ONEBIT_K_EC_UPDATE)
     const float S = A.sscale_cur[(int64_t)ch.seg * A.n + ch.shard];
     float* __restrict__ x = A.pptr[ch.seg] + ch.start;
     float* __restrict__ m = A.m + ch.off;
@@ -1227,6 +1299,7 @@ __global__ void __launch_bounds__(kThreads, SMALL ? 3 : 2) k_warmup(const StepAr
   for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
     unsigned long long vhi = 0, vlo = 0;
     const Chunk ch = A.chunks[u];
+    ONEBIT_CHECK_UNIT(chunk_ok(A, ch), A.status, ONEBIT_K_WARMUP)
     __syncthreads();
     for (int i = threadIdx.x; i < A.n; i += kThreads)
       gsm[i] = static_cast<const GT*>(A.gptr[(int64_t)i * A.T + ch.seg]) + ch.start;
@@ -1354,6 +1427,7 @@ __global__ void __launch_bounds__(kStagedThreads) k_warmup_staged(const StepArgs
     if (++c.t >= (A.chunks[c.u].len + kWTile - 1) / kWTile) {
       c.t = 0;
       c.u += gridDim.x;
+      ONEBIT_SKIP_BAD_CHUNKS(c.u, A.n_chunks, (int)gridDim.x, ONEBIT_K_WARMUP);
     }
   };
   const size_t mofs = (size_t)n * kWTile * 2;  // stage layout: n gradient rows, then m, v, x
@@ -1362,6 +1436,7 @@ __global__ void __launch_bounds__(kStagedThreads) k_warmup_staged(const StepArgs
     // ---------------- producer warp (one elected lane issues the copies)
     if (threadIdx.x != kThreads) return;
     TileCursor c{(int)blockIdx.x, 0};
+    ONEBIT_SKIP_BAD_CHUNKS(c.u, A.n_chunks, (int)gridDim.x, ONEBIT_K_WARMUP);
     int j = 0;
     for (; c.u < A.n_chunks; ++j, advance(c)) {
       const int st = j % kWStages;
@@ -1396,6 +1471,7 @@ __global__ void __launch_bounds__(kStagedThreads) k_warmup_staged(const StepArgs
   // ---------------- consumer warps: thread t owns elements [8t, 8t+8) of every tile
   const int lane = threadIdx.x & 31;
   TileCursor cons{(int)blockIdx.x, 0};
+  ONEBIT_SKIP_BAD_CHUNKS(cons.u, A.n_chunks, (int)gridDim.x, ONEBIT_K_WARMUP);
   int k = 0;
   unsigned long long vhi = 0, vlo = 0;
   while (cons.u < A.n_chunks) {
@@ -1536,11 +1612,19 @@ struct XArgs {
   const XRange* r;
   int32_t n;
   uint32_t* base[5];
+#ifdef ONEBIT_CHECKS
+  int64_t words[5];       // each region's extent in words
+  unsigned int* status;
+#endif
 };
 
 static __global__ void __launch_bounds__(kThreads) k_exchange_copy(const XArgs X) {
   for (int q = blockIdx.x; q < X.n; q += gridDim.x) {
     const XRange r = X.r[q];
+    ONEBIT_CHECK_UNIT(r.len >= 0 && r.len <= kXPiece && r.sreg >= 0 && r.sreg < 5 && r.dreg >= 0 && r.dreg < 5 &&
+                          r.src >= 0 && r.src + r.len <= X.words[r.sreg] && r.dst >= 0 &&
+                          r.dst + r.len <= X.words[r.dreg],
+                      X.status, ONEBIT_K_EXCHANGE)
     const uint32_t* s = X.base[r.sreg] + r.src;
     uint32_t* d = X.base[r.dreg] + r.dst;
     for (int e = threadIdx.x; e < r.len; e += kThreads) d[e] = s[e];
@@ -1570,11 +1654,22 @@ struct ExportArgs {
   const uint32_t* bits;  // sign words for kExportBits
   const float* scales;
   float* dst;
+#ifdef ONEBIT_CHECKS
+  int64_t Dp, D;          // padded and unpadded elements of the state and of the caller's buffer
+  int64_t n_scales;       // entries of `scales`
+  unsigned int* status;
+#endif
 };
 
 static __global__ void __launch_bounds__(kThreads) k_export(const ExportArgs X) {
   for (int u = blockIdx.x; u < X.n_chunks; u += gridDim.x) {
     const Chunk ch = X.chunks[u];
+    ONEBIT_CHECK_UNIT(ch.len >= 0 && ch.off >= 0 && ch.off + ch.len <= X.Dp && ch.uoff >= 0 &&
+                          ch.uoff + ch.len <= X.D &&
+                          (!X.scales || ((int64_t)ch.seg * X.scale_seg_mul + (int64_t)ch.shard * X.scale_shard_mul >= 0 &&
+                                         (int64_t)ch.seg * X.scale_seg_mul + (int64_t)ch.shard * X.scale_shard_mul <
+                                             X.n_scales)),
+                      X.status, ONEBIT_K_EXPORT)
     const float s = X.scales ? X.scales[(int64_t)ch.seg * X.scale_seg_mul + (int64_t)ch.shard * X.scale_shard_mul]
                              : 0.0f;
     for (int e = threadIdx.x; e < ch.len; e += kThreads) {

@@ -71,7 +71,9 @@ typedef enum {
   ONEBIT_ERR_NOMEM = 4,       /* a library allocation failed */
   ONEBIT_ERR_WORKSPACE = 5,   /* the caller's workspace is too small or misaligned */
   ONEBIT_ERR_NONFINITE = 6,   /* a worker or server scale was NaN or infinite */
-  ONEBIT_ERR_UNSUPPORTED = 7  /* a valid request the library does not support */
+  ONEBIT_ERR_UNSUPPORTED = 7, /* a valid request the library does not support */
+  ONEBIT_ERR_BOUNDS = 8       /* checked builds only: a kernel's bounds check found a unit of work whose
+                               * accesses would leave its buffers, and skipped it */
 } onebit_status_t;
 
 typedef enum { ONEBIT_F32 = 0, ONEBIT_F16 = 1, ONEBIT_BF16 = 2 } onebit_dtype_t;
@@ -186,7 +188,11 @@ onebit_status_t onebit_adam_free(onebit_adam_t* h);
 
 /* Synchronise `stream` and report the sticky device flags: ONEBIT_OK, ONEBIT_ERR_NONFINITE (a scale
  * was NaN or infinite), or ONEBIT_ERR_CUDA when a kernel gave up waiting (about one second) for its
- * own asynchronous copies and stopped early (onebit_adam_last_error() says so). */
+ * own asynchronous copies and stopped early (onebit_adam_last_error() says so).  A checked build
+ * (the library compiled with -DONEBIT_CHECKS) also reports ONEBIT_ERR_BOUNDS, first of all: some
+ * kernel found a chunk, scale range or exchange range whose accesses would leave its buffers and
+ * skipped it (onebit_adam_last_error() names the kernels); the state of that step is not
+ * meaningful.  A normal build has no such checks. */
 onebit_status_t onebit_adam_get_status(onebit_adam_t* h, onebit_stream_t stream);
 /* Clear the sticky device flag (enqueued on `stream`). */
 onebit_status_t onebit_adam_clear_status(onebit_adam_t* h, onebit_stream_t stream);
@@ -266,8 +272,18 @@ onebit_status_t onebit_adam_set_max_ctas(onebit_adam_t* h, int32_t max_ctas);
  *   ONEBIT_FAULT_FAIL_ALLOC makes the handle's next `value` (1..1000) device or pinned allocations
  *     fail as if memory were exhausted (the host-gradient staging buffers, the variance monitor's
  *     slot): the call returns ONEBIT_ERR_NOMEM and, like every failed check, changes no state.
- *   ONEBIT_FAULT_NONE turns both off. */
-typedef enum { ONEBIT_FAULT_NONE = 0, ONEBIT_FAULT_STALL_COPIES = 1, ONEBIT_FAULT_FAIL_ALLOC = 2 } onebit_fault_t;
+ *   ONEBIT_FAULT_TIGHTEN_BOUNDS (checked builds only; ONEBIT_ERR_UNSUPPORTED otherwise) makes the
+ *     bounds checks withhold the last `value` padded elements (a multiple of 32, 32..the padded
+ *     total) from every state row.  The units that reach into them are skipped as if their
+ *     descriptors were out of bounds and get_status() returns ONEBIT_ERR_BOUNDS.  The checks only get
+ *     stricter: no access leaves the buffers.
+ *   ONEBIT_FAULT_NONE turns all of them off. */
+typedef enum {
+  ONEBIT_FAULT_NONE = 0,
+  ONEBIT_FAULT_STALL_COPIES = 1,
+  ONEBIT_FAULT_FAIL_ALLOC = 2,
+  ONEBIT_FAULT_TIGHTEN_BOUNDS = 3
+} onebit_fault_t;
 onebit_status_t onebit_adam_set_fault_injection(onebit_adam_t* h, int32_t kind, int64_t value);
 
 /* The work chunks the kernels use for a config (host only, no GPU needed): up to `cap` rows of

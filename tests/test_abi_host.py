@@ -40,8 +40,8 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_error_strings():
-    for s in range(8):
-        assert ob.error_string(s)
+    for s in range(9):
+        assert ob.error_string(s) and "unknown" not in ob.error_string(s)
     assert "unknown" in ob.error_string(99)
 
 
@@ -336,6 +336,7 @@ def test_binding_constants_and_config_layout_match_the_header(tmp_path):
         "ONEBIT_OK": ob.OK, "ONEBIT_ERR_INVALID_ARG": ob.ERR_INVALID_ARG, "ONEBIT_ERR_PHASE": ob.ERR_PHASE,
         "ONEBIT_ERR_CUDA": ob.ERR_CUDA, "ONEBIT_ERR_NOMEM": ob.ERR_NOMEM, "ONEBIT_ERR_WORKSPACE": ob.ERR_WORKSPACE,
         "ONEBIT_ERR_NONFINITE": ob.ERR_NONFINITE, "ONEBIT_ERR_UNSUPPORTED": ob.ERR_UNSUPPORTED,
+        "ONEBIT_ERR_BOUNDS": ob.ERR_BOUNDS,
         "ONEBIT_F32": ob.F32, "ONEBIT_F16": ob.F16, "ONEBIT_BF16": ob.BF16,
         "ONEBIT_PHASE_WARMUP": ob.PHASE_WARMUP, "ONEBIT_PHASE_COMPRESS": ob.PHASE_COMPRESS,
         "ONEBIT_STATE_M": ob.STATE_M, "ONEBIT_STATE_V": ob.STATE_V, "ONEBIT_STATE_WORKER_ERROR": ob.STATE_WORKER_ERROR,
@@ -343,9 +344,10 @@ def test_binding_constants_and_config_layout_match_the_header(tmp_path):
         "ONEBIT_STATE_SERVER_BITS": ob.STATE_SERVER_BITS, "ONEBIT_STATE_WORKER_SCALES": ob.STATE_WORKER_SCALES,
         "ONEBIT_STATE_SERVER_SCALES": ob.STATE_SERVER_SCALES,
         "ONEBIT_FAULT_NONE": ob.FAULT_NONE, "ONEBIT_FAULT_STALL_COPIES": ob.FAULT_STALL_COPIES,
-        "ONEBIT_FAULT_FAIL_ALLOC": ob.FAULT_FAIL_ALLOC, "ONEBIT_NUM_KERNELS": ob.NUM_KERNELS,
+        "ONEBIT_FAULT_FAIL_ALLOC": ob.FAULT_FAIL_ALLOC, "ONEBIT_FAULT_TIGHTEN_BOUNDS": ob.FAULT_TIGHTEN_BOUNDS,
+        "ONEBIT_NUM_KERNELS": ob.NUM_KERNELS,
     }
-    kernels = ["WARMUP", "FREEZE", "WORKER", "WORKER_SCALE", "SERVER", "SERVER_SCALE", "UPDATE", "EXPORT", "EC_UPDATE"]
+    kernels = ["WARMUP", "FREEZE", "WORKER", "WORKER_SCALE", "SERVER", "SERVER_SCALE", "UPDATE", "EXPORT", "EC_UPDATE", "EXCHANGE"]
     for k, name in enumerate(kernels):
         enums[f"ONEBIT_K_{name}"] = ob.KERNEL_NAMES.index(name.lower())
     fields = [f[0] for f in ob.Config._fields_]
