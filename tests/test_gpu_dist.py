@@ -34,6 +34,10 @@ CASES = {
     "blocks_n8_r4_f16": dict(numel=(20_000, 77, 4096), n=8, R=4, dtype=W.F16, block=96),
     "n3_r3_f32": dict(numel=(1000, 31), n=3, R=3, dtype=W.F32, block=0),
     "rank_of_one_n4": dict(numel=(50_000,), n=4, R=1, dtype=W.F32, block=0),
+    # 8192-element server chunks (two staged tiles each) in every rank's narrowed chunk table
+    "flat_n16_r4_f16_d8M": dict(numel=(8_000_037,), n=16, R=4, dtype=W.F16, block=0),
+    # per-block scales at size: the staged server's walk over contiguous runs of a rank's own chunks
+    "blocks_n16_r2_bf16_d6M": dict(numel=(6_000_011,), n=16, R=2, dtype=W.BF16, block=65536),
 }
 
 
