@@ -735,6 +735,17 @@ onebit_status_t run_server(onebit_adam* h, const StepArgs& A, cudaStream_t st) {
   return h->serr_zero ? run_server_v<false>(h, A, st) : run_server_v<true>(h, A, st);
 }
 
+// The broadcast and update over the whole replica.  Plans whose worker chunks hold several whole
+// shards (short scale blocks) walk those: the units stay long, and each group finds its own shard.
+onebit_status_t run_update(onebit_adam* h, const StepArgs& A, cudaStream_t st) {
+  auto go = [&](auto k, int units) {
+    return launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, units), kThreads, st, A);
+  };
+  if (h->plan.worker_spans)
+    return h->params_aligned ? go(k_update<true, true>, A.n_wchunks) : go(k_update<false, true>, A.n_wchunks);
+  return h->params_aligned ? go(k_update<true, false>, A.n_chunks) : go(k_update<false, false>, A.n_chunks);
+}
+
 // den = sqrt(v) + eps in place (v / (1 - b2^t) first with bias correction); the compression stage
 // starts from zero errors and the dense warm-up momentum.
 onebit_status_t do_freeze(onebit_adam* h, cudaStream_t st) {
@@ -875,12 +886,8 @@ onebit_status_t do_compress(onebit_adam* h, const void* const* grads, cudaStream
     const bool bc = h->cfg.bias_correction != 0;
     if (bc) s = h->params_aligned ? go(k_ec_adam_update<true, true>) : go(k_ec_adam_update<true, false>);
     else s = h->params_aligned ? go(k_ec_adam_update<false, true>) : go(k_ec_adam_update<false, false>);
-  } else if (h->params_aligned) {
-    auto k = k_update<true>;
-    s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
   } else {
-    auto k = k_update<false>;
-    s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
+    s = run_update(h, A, st);
   }
   if (s) return s;
   finish_step(h, ec_adam);
@@ -944,14 +951,7 @@ onebit_status_t do_end(onebit_adam* h, const void* gathered, cudaStream_t st) {
   if (h->plan.world > 1 && !gathered) return ONEBIT_ERR_INVALID_ARG;
   onebit_status_t s = run_exchange_copy(h, 3, gathered, st);
   if (s) return s;
-  StepArgs A = base_args(h);
-  if (h->params_aligned) {
-    auto k = k_update<true>;
-    s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
-  } else {
-    auto k = k_update<false>;
-    s = launch(h, ONEBIT_K_UPDATE, k, grid_for(h, (const void*)k, kThreads, A.n_chunks), kThreads, st, A);
-  }
+  s = run_update(h, base_args(h), st);
   if (s) return s;
   finish_step(h, false);
   h->xstage = 0;

@@ -1131,20 +1131,28 @@ __global__ void __launch_bounds__(kStagedThreads, 3) k_server_staged(const StepA
 
 // ------------------------------------------------------------------------------------------------
 // K3: broadcast unpack + preconditioned update  x = x - lr * (m / den),  m = S_kj * sign(a).
+// SPANS: walk the worker-side chunks instead of the server-side ones.  Plans whose shards are much
+// shorter than a chunk (short scale blocks) have worker chunks that hold several whole shards; each
+// 8-element group then takes the scale of its own shard, and the units stay long.
 
-template <bool VEC>
+template <bool VEC, bool SPANS = false>
 __global__ void __launch_bounds__(kThreads) k_update(const StepArgs A) {
   const float lr = A.lr;
-  for (int u = blockIdx.x; u < A.n_chunks; u += gridDim.x) {
-    const Chunk ch = A.chunks[u];
-    ONEBIT_CHECK_UNIT(chunk_ok(A, ch), A.status, ONEBIT_K_UPDATE)
+  for (int u = blockIdx.x; u < (SPANS ? A.n_wchunks : A.n_chunks); u += gridDim.x) {
+    const Chunk ch = (SPANS ? A.wchunks : A.chunks)[u];
+    ONEBIT_CHECK_UNIT(chunk_ok(A, ch) && ch.per >= 0 && (ch.per == 0 || ch.shard + (ch.len - 1) / ch.per < A.n),
+                      A.status, ONEBIT_K_UPDATE)
     const float S = A.sscale_cur[(int64_t)ch.seg * A.n + ch.shard];
+    // SPANS: a group's shard is the chunk's first plus its offset / the shard length
+    const float* __restrict__ Sseg = A.sscale_cur + (int64_t)ch.seg * A.n + ch.shard;
+    auto scale_of = [&](int gi) { return ch.per ? Sseg[(uint32_t)(gi * 8) / (uint32_t)ch.per] : S; };
     float* __restrict__ x = A.pptr[ch.seg] + ch.start;
     const float* __restrict__ den = A.v + ch.off;
     const uint8_t* __restrict__ sb = reinterpret_cast<const uint8_t*>(A.sbits) + (ch.off >> 3);
     struct In {
       float x[8], d[8];
       uint32_t b;
+      float S;
     };
     auto load = [&](In& r, int gi) {
       const int64_t e = (int64_t)gi * 8;
@@ -1154,12 +1162,14 @@ __global__ void __launch_bounds__(kThreads) k_update(const StepArgs A) {
         for (int q = 0; q < 8; ++q) r.x[q] = x[e + q];
       ld8_stream(den + e, r.d);
       r.b = sb[gi];
+      if (SPANS) r.S = scale_of(gi);
     };
     auto work = [&](In& r, int gi) {
       const int64_t e = (int64_t)gi * 8;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float mq = ((r.b >> q) & 1u) ? S : -S;
+        const float Sg = SPANS ? r.S : S;
+        const float mq = ((r.b >> q) & 1u) ? Sg : -Sg;
         r.x[q] = __fsub_rn(r.x[q], __fmul_rn(lr, __fdiv_rn(mq, r.d[q])));
       }
       if (VEC) st8(x + e, r.x);
@@ -1184,8 +1194,9 @@ __global__ void __launch_bounds__(kThreads) k_update(const StepArgs A) {
     const int rem = ch.len & 7;
     if (rem && threadIdx.x == (ng % kThreads)) {
       const int64_t e0 = (int64_t)ng * 8;
+      const float St = SPANS ? scale_of(ng) : S;
       for (int q = 0; q < rem; ++q) {
-        const float mq = ((sb[ng] >> q) & 1u) ? S : -S;
+        const float mq = ((sb[ng] >> q) & 1u) ? St : -St;
         x[e0 + q] = __fsub_rn(x[e0 + q], __fmul_rn(lr, __fdiv_rn(mq, den[e0 + q])));
       }
     }
