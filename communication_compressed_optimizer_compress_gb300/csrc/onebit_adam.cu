@@ -840,7 +840,11 @@ onebit_status_t run_worker_half(onebit_adam* h, const void* const* grads, cudaSt
              grid_for(h, (const void*)k_worker_exact, kThreads, (parts + kThreads - 1) / kThreads), kThreads, st, A);
   if (s) return s;
   const int nt = h->plan.nl * h->plan.T;
-  // many short ranges: one warp per scale; otherwise one CTA per scale
+  // one partial per range at most: one thread per scale; many short ranges: one warp per scale;
+  // otherwise one CTA per scale
+  if (h->plan.max_wseg_count <= 1)
+    return launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale_one, (nt + kScaleThreads - 1) / kScaleThreads,
+                  kScaleThreads, st, A);
   constexpr int kPerCta = kScaleThreads / 32;
   if (h->plan.max_wseg_count <= kWarpScaleMax)
     return launch(h, ONEBIT_K_WORKER_SCALE, k_worker_scale_warp, (nt + kPerCta - 1) / kPerCta, kScaleThreads, st, A);
@@ -854,6 +858,9 @@ onebit_status_t run_server_half(onebit_adam* h, cudaStream_t st) {
   onebit_status_t s = run_server(h, A, st);
   if (s) return s;
   const int nt = h->plan.n * h->plan.T;
+  if (h->plan.max_shard_count <= 1)  // (a rank's own ranges are no longer than the plan's)
+    return launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale_one, (nt + kScaleThreads - 1) / kScaleThreads,
+                  kScaleThreads, st, A);
   constexpr int kPerCta = kScaleThreads / 32;
   if (h->plan.max_shard_count <= kWarpScaleMax)
     return launch(h, ONEBIT_K_SERVER_SCALE, k_server_scale_warp, (nt + kPerCta - 1) / kPerCta, kScaleThreads, st, A);

@@ -619,6 +619,34 @@ static __global__ void __launch_bounds__(kScaleThreads) k_server_scale_warp(cons
   if ((threadIdx.x & 31) == 0) A.sscale_cur[item] = s;
 }
 
+// Plans whose every range holds at most one partial (short scale blocks: one chunk per shard or per
+// block): one thread per scale.  The sum of a single partial involves no rounding, so the scales equal
+// the warp form's bit for bit, at a 32nd of its fp64 instructions (GB300's fp64 pipe is slow).
+__device__ __forceinline__ float scale_of_one(const double* part, const Range r, unsigned int* status) {
+  const double tot = r.count > 0 ? __ldcg(part + r.first) : 0.0;
+  const float s = r.len > 0 ? __double2float_rn(sqrt(tot / (double)r.len)) : 0.0f;
+  if (!isfinite(s)) atomicOr(status, 1u);
+  return s;
+}
+
+static __global__ void __launch_bounds__(kScaleThreads) k_worker_scale_one(const StepArgs A) {
+  const int item = blockIdx.x * kScaleThreads + threadIdx.x;
+  if (item >= A.nl * A.T) return;
+  const int il = item / A.T, k = item % A.T;
+  ONEBIT_CHECK_ITEM(range_ok(A.wseg_ranges[k], A.n_wchunks) && A.wseg_ranges[k].count <= 1 && A.w0 + il < A.n,
+                    A.status, ONEBIT_K_WORKER_SCALE)
+  A.wscale_cur[(int64_t)A.w0 * A.T + item] =
+      scale_of_one(A.wpart + (int64_t)il * A.n_wchunks, A.wseg_ranges[k], A.status);
+}
+
+static __global__ void __launch_bounds__(kScaleThreads) k_server_scale_one(const StepArgs A) {
+  const int item = blockIdx.x * kScaleThreads + threadIdx.x;
+  if (item >= A.n * A.T) return;
+  ONEBIT_CHECK_ITEM(range_ok(A.shard_ranges[item], A.n_chunks) && A.shard_ranges[item].count <= 1, A.status,
+                    ONEBIT_K_SERVER_SCALE)
+  A.sscale_cur[item] = scale_of_one(A.spart, A.shard_ranges[item], A.status);
+}
+
 // ------------------------------------------------------------------------------------------------
 // K2: server.  For every element the n decompressed worker messages are summed in worker order in
 // fp32, divided by n, and the server error is added; the result a is written with its sign byte, and
