@@ -201,7 +201,7 @@ onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
   // The server rebuilds its sum tables (about 2^min(n,12) entries) whenever a CTA moves to another
   // tensor.  Striding over the chunks, that happens at nearly every chunk once tensors are shorter
   // than a grid's worth of chunks.  When those rebuilds would cost more than about 5% of the
-  // elements, the register variant of the server kernel walks contiguous runs of chunks instead.
+  // elements, the server kernel walks contiguous runs of chunks instead (both of its variants).
   const int64_t table = (int64_t(1) << std::min(P->n, 12)) + (P->n > 12 ? 512 : 0);
   P->contig = P->T > 1 && table * (int64_t)P->chunks.size() * 20 > P->D;
   P->Wp = off / 32;

@@ -95,7 +95,7 @@ struct StepArgs {
   const Chunk* wchunks;      // worker-side chunks: never cross a tensor; may span several shards
   const Range* wseg_ranges;  // [T]   worker chunks of each tensor
   int32_t n_wchunks;
-  int32_t contig;            // the register server kernel walks contiguous runs (many short tensors)
+  int32_t contig;            // the server kernel walks contiguous runs of chunks (many short segments)
   int64_t D;                 // elements (unpadded)
   int32_t nl;                // workers whose momentum this launch compresses (all n, or one rank's share)
   int32_t w0;                // the first of them: global workers w0 .. w0+nl-1 (c, wpart and gptr rows 0..nl-1)
@@ -811,7 +811,8 @@ __device__ __forceinline__ int run_begin(const StepArgs& A, int b) {
 }
 
 
-// K2, register variant (any n): every thread loads its group's sign bytes and a directly.
+// K2, register variant (any n; launched for n > 128, where the staged ring no longer fits): every
+// thread loads its group's sign bytes and a directly.
 template <bool HAS_ERR, bool CONTIG>
 __global__ void __launch_bounds__(kThreads) k_server(const StepArgs A) {
   __shared__ ServerTables S;
