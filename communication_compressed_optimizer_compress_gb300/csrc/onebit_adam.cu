@@ -53,6 +53,7 @@ struct Plan {
   std::vector<Chunk> wchunks;       // worker-side chunks (never cross a tensor; may span shards)
   std::vector<Range> wseg_ranges;   // [T]
   int32_t max_wseg_count = 0, max_shard_count = 0;
+  int32_t max_wchunk_len = 0;  // the longest worker-side chunk
   bool worker_spans = false;  // some worker chunk holds several shards
   bool contig = false;        // server kernels walk contiguous runs (see make_plan)
   // Multi-GPU form (make_rank_plan): rank `rank` of `world` holds the nl = n/world workers
@@ -197,7 +198,10 @@ onebit_status_t make_plan(const onebit_adam_config_t* cfg, Plan* P) {
   }
   P->Dp = off;
   P->D = uoff;
-  for (const Chunk& c : P->wchunks) P->worker_spans |= c.per != 0;
+  for (const Chunk& c : P->wchunks) {
+    P->worker_spans |= c.per != 0;
+    P->max_wchunk_len = std::max(P->max_wchunk_len, c.len);
+  }
   // The server rebuilds its sum tables (about 2^min(n,12) entries) whenever a CTA moves to another
   // tensor.  Striding over the chunks, that happens at nearly every chunk once tensors are shorter
   // than a grid's worth of chunks.  When those rebuilds would cost more than about 5% of the
@@ -675,6 +679,14 @@ onebit_status_t run_warmup(onebit_adam* h, StepArgs A, bool vec, cudaStream_t st
 template <typename GT, int DM, bool HE>
 onebit_status_t run_worker_v(onebit_adam* h, const StepArgs& A, bool vec, cudaStream_t st) {
   const int64_t units = (int64_t)A.n_wchunks * A.nl;
+  if constexpr (DM == kMomBits || DM == kMomBitsShards) {
+    // short units, and enough of them to give every SM 32 warps: one warp each
+    if (h->plan.max_wchunk_len <= kWarpUnitMax && units >= (int64_t)32 * h->num_sms) {
+      const int64_t blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
+      auto k = vec ? k_worker<GT, DM, HE, true, true> : k_worker<GT, DM, HE, false, true>;
+      return launch(h, ONEBIT_K_WORKER, k, grid_for(h, (const void*)k, kThreads, blocks), kThreads, st, A);
+    }
+  }
   if (vec) {
     auto k = k_worker<GT, DM, HE, true>;
     return launch(h, ONEBIT_K_WORKER, k, grid_for(h, (const void*)k, kThreads, units), kThreads, st, A);

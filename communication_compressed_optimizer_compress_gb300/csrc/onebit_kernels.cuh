@@ -411,13 +411,19 @@ enum MomentumSource : int {
   kMomBitsShards = 3   // as kMomBits, for plans whose worker chunks may hold several shards
 };
 
-template <typename GT, int MSRC, bool HAS_ERR, bool VEC>
+// WU: one warp per unit instead of one block (plans whose worker chunks are all short, at most
+// kWarpUnitMax elements): eight units per block, and each unit's sum of squares is a warp butterfly,
+// with no block barrier per unit.
+constexpr int kWarpUnitMax = 8192;
+
+template <typename GT, int MSRC, bool HAS_ERR, bool VEC, bool WU = false>
 __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
   constexpr bool DENSE_M = MSRC == kMomDense;
   constexpr bool BITS = MSRC == kMomBits || MSRC == kMomBitsShards;
   __shared__ double red[kThreads / 32];
   const int64_t n_units = (int64_t)A.n_wchunks * A.nl;
-  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+  for (int64_t u = WU ? (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5) : (int64_t)blockIdx.x;
+       u < n_units; u += WU ? (int64_t)gridDim.x * (kThreads / 32) : (int64_t)gridDim.x) {
     const int ci = (int)(u / A.nl);
     const int il = (int)(u - (int64_t)ci * A.nl);  // local worker; global worker i
     const int i = A.w0 + il;
@@ -482,21 +488,22 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
     };
 
     const int ng = ch.len >> 3;
-    int gi = threadIdx.x;
-    for (; gi + (kWorkerUnroll - 1) * kThreads < ng; gi += kWorkerUnroll * kThreads) {
+    constexpr int NT = WU ? 32 : kThreads;  // threads sharing the unit
+    int gi = WU ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
+    for (; gi + (kWorkerUnroll - 1) * NT < ng; gi += kWorkerUnroll * NT) {
       In r[kWorkerUnroll];  // all loads of kWorkerUnroll groups in flight, then the math
 #pragma unroll
-      for (int j = 0; j < kWorkerUnroll; ++j) load(r[j], gi + j * kThreads);
+      for (int j = 0; j < kWorkerUnroll; ++j) load(r[j], gi + j * NT);
 #pragma unroll
-      for (int j = 0; j < kWorkerUnroll; ++j) work(r[j], gi + j * kThreads);
+      for (int j = 0; j < kWorkerUnroll; ++j) work(r[j], gi + j * NT);
     }
-    for (; gi < ng; gi += kThreads) {
+    for (; gi < ng; gi += NT) {
       In r0;
       load(r0, gi);
       work(r0, gi);
     }
     const int rem = ch.len & 7;
-    if (rem && threadIdx.x == (ng % kThreads)) {  // the ragged end of a tensor: scalar
+    if (rem && (WU ? (int)(threadIdx.x & 31) : (int)threadIdx.x) == (ng % NT)) {  // the ragged end of a tensor: scalar
       const int64_t e0 = (int64_t)ng * 8;
       const float St = MSRC == kMomBitsShards ? scale_of(ng) : Sp;
       uint32_t byte = 0;
@@ -517,8 +524,13 @@ __global__ void __launch_bounds__(kThreads) k_worker(const StepArgs A) {
       }
       wb[ng] = (uint8_t)byte;
     }
-    const double tot = block_sq<kThreads>(sq_of(hi, lo), red);
-    if (threadIdx.x == 0) A.wpart[(int64_t)il * A.n_wchunks + ci] = tot;
+    if (WU) {
+      const double tot = sq_value(warp_sq<32>(sq_of(hi, lo)));
+      if ((threadIdx.x & 31) == 0) A.wpart[(int64_t)il * A.n_wchunks + ci] = tot;
+    } else {
+      const double tot = block_sq<kThreads>(sq_of(hi, lo), red);
+      if (threadIdx.x == 0) A.wpart[(int64_t)il * A.n_wchunks + ci] = tot;
+    }
   }
 }
 

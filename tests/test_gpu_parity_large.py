@@ -116,3 +116,22 @@ def test_per_block_scales_at_size():
     st = p.run()
     assert st.scales_exact >= 0.99 * st.scales, st
     p.close()
+
+
+def test_short_scale_blocks_at_size():
+    """Short scale blocks (4096 elements, n = 16: 256-element shards) on 2e6 elements of the BERT-Large
+    law: worker chunks of one block each, holding sixteen shards, enough of them that the worker kernel
+    runs one warp per unit; the update walks the same chunks and every scale is one partial.  Three
+    compression steps compared element by element with the oracle ("1-bit Adam ...", Sec. 11)."""
+    import torch
+
+    w = W.WORKLOADS["bert_large"].with_(numel=(2_000_011,), warmup_steps=2, compress_steps=3)
+    cfg = ob.make_config(list(w.numel), w.n_workers, w.warmup_steps, grad_dtype=w.grad_dtype, scale_block=4096)
+    wrows = ob.plan_worker_chunks(cfg)
+    assert any(r[5] for r in wrows) and max(r[3] for r in wrows) <= 8192  # spanning, short units
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert len(wrows) * w.n_workers >= 32 * sms  # enough units for one warp each
+    p = Pair(w, scale_block=4096, gen_device="cuda")
+    st = p.run()
+    assert st.scales_exact >= 0.99 * st.scales, st
+    p.close()
